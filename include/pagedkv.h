@@ -1,0 +1,271 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv: decode-step PagedAttention over a
+ * block-paged KV cache on one GB300 (sm_103a).
+ *
+ * Sources (page title, section):
+ *  [P1] "micro-vLLM" wiki -- execution chain: the KVCacheManager manages
+ *       logical blocks, the block table, the prefix cache, and allocation and
+ *       release; the ModelRunner owns the physical KV cache.
+ *  [P2] "MinivLLM -- 用最小代码读懂 vLLM 推理内核" -- 使用教程 step 5 and
+ *       核心亮点: a self-written PagedAttention serves the decode stage.
+ *  [P3] "从零手写 vLLM 核心：mini-vllm 项目深度解析" -- §2 分页KV缓存: the cache
+ *       is cut into fixed 16-token blocks, allocated and released on demand,
+ *       shareable between sequences (prefix cache, parallel sampling), and
+ *       correct under pressure through admission control; §关键工程决策
+ *       item 1: each layer reads its own cache length; item 3: K and V
+ *       pools are separate and layer-major, with the block-size axis before
+ *       the KV-head axis, and attention reads views, not strided copies.
+ *
+ * Conventions shared by every device entry point:
+ *  - All pointers to tensors are DEVICE pointers owned by the caller unless a
+ *    parameter says "host".  The library never allocates, frees or keeps a
+ *    reference to caller memory after the call returns; work is enqueued on
+ *    `stream` (a cudaStream_t; NULL = the legacy default stream) and the call
+ *    does not synchronise.
+ *  - One layer's pool (K or V) is contiguous [num_blocks][16][num_kv_heads]
+ *    [head_dim] of 16-bit elements ([P3] item 3).  A layer-major stack of L
+ *    pools is L such arrays back to back; pass the base of one layer.
+ *  - q, K, V and out share one dtype (PKV_F16 or PKV_BF16); arithmetic is
+ *    fp32 inside the kernels; outputs are rounded to nearest even.
+ *  - block_tables [num_seqs][max_blocks_per_seq] int32 map logical block j
+ *    of sequence s to a physical block id in [0, num_blocks) ([P1]).  Only
+ *    entries j < ceil(context_lens[s] / 16) are read.
+ *  - context_lens [num_seqs] int32 count the tokens of each sequence INCLUDING
+ *    the token written this step (it sits at position context_len - 1).  A
+ *    length of 0 is a padding row whose attention output is all zeros.
+ *  - Arguments are validated on the host; a bad argument returns an error
+ *    and enqueues nothing.  Values that live on the device (block ids,
+ *    lengths, slots) are checked by the kernels themselves: a bad value is
+ *    never dereferenced, the affected row is skipped or zero-filled, and a
+ *    bit is set in the device status word (pkv_device_status).  No kernel
+ *    traps, asserts or spins without a bound.
+ */
+#ifndef PAGEDKV_H_
+#define PAGEDKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (struct CUstream_st*), spelled without CUDA headers. */
+typedef struct CUstream_st* pkv_stream_t;
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,   /* null pointer, bad size, inconsistent shapes */
+    PKV_ERR_UNSUPPORTED = 2,   /* a valid shape this build has no kernel for */
+    PKV_ERR_NO_BLOCKS = 3,     /* allocator: not enough free blocks (nothing taken) */
+    PKV_ERR_BAD_BLOCK_ID = 4,  /* allocator: id out of range or not allocated */
+    PKV_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed */
+    PKV_ERR_WORKSPACE = 6      /* workspace null or smaller than required */
+} pkv_status;
+
+typedef enum { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype;
+
+/* Tokens per physical block, fixed by [P3] §2. */
+#define PKV_BLOCK_SIZE 16
+
+/* Bits of the device status word (see pkv_device_status). */
+#define PKV_DEV_BAD_BLOCK_ID 0x1u   /* a table entry outside [0, num_blocks) was skipped */
+#define PKV_DEV_BAD_LENGTH   0x2u   /* a context length < 0 or beyond the table / bound */
+#define PKV_DEV_BAD_SLOT     0x4u   /* a slot >= num_blocks * 16 was skipped by the write */
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int pkv_version(void);
+
+/* Static text for a status code. */
+const char* pkv_status_string(pkv_status status);
+
+/* Bytes of ONE pool (K or V) holding `num_layers` layer-major layers of
+ * [num_blocks][block_size][num_kv_heads][head_dim] ([P3] item 3).  Returns 0
+ * for a non-positive size or a block_size other than 16. */
+size_t pkv_cache_bytes(int num_layers, int num_blocks, int block_size, int num_kv_heads,
+                       int head_dim, pkv_dtype dtype);
+
+/* ---------------------------------------------------------------------------
+ * Host block allocator ([P1] KVCacheManager; [P3] §2: on-demand allocation
+ * and release, sharing through reference counts, admission control).  Plain
+ * host memory owned by the handle; not thread-safe (one owner thread).
+ * ------------------------------------------------------------------------- */
+typedef struct pkv_allocator pkv_allocator;
+
+/* Creates an allocator over block ids [0, num_blocks), all free. */
+pkv_status paged_kv_alloc_create(int num_blocks, pkv_allocator** out);
+void paged_kv_alloc_destroy(pkv_allocator* a);
+
+/* Takes n free blocks (reference count 1 each) into out_block_ids[n] (host).
+ * All or nothing: with fewer than n free blocks nothing is taken and
+ * PKV_ERR_NO_BLOCKS is returned, so a scheduler can refuse admission. */
+pkv_status paged_kv_alloc(pkv_allocator* a, int n, int32_t* out_block_ids);
+
+/* Adds one reference to each listed allocated block (a sequence starts
+ * sharing a prefix block).  All or nothing: PKV_ERR_BAD_BLOCK_ID if any id is
+ * out of range or free. */
+pkv_status paged_kv_share(pkv_allocator* a, int n, const int32_t* block_ids);
+
+/* Drops one reference from each listed block; a block whose count reaches 0
+ * returns to the free list.  All or nothing, as for paged_kv_share. */
+pkv_status paged_kv_free(pkv_allocator* a, int n, const int32_t* block_ids);
+
+int paged_kv_num_free(const pkv_allocator* a);
+
+/* Reference count of one block (0 = free), or -1 for an id out of range. */
+int paged_kv_refcount(const pkv_allocator* a, int32_t block_id);
+
+/* ---------------------------------------------------------------------------
+ * Device operations
+ * ------------------------------------------------------------------------- */
+
+/* Block-table plumbing ([P1] block table; [P3] §2 16-token blocks, item 1):
+ * for each sequence s with n = context_lens[s] > 0,
+ *     slot_mapping[s] = block_tables[s][(n-1)/16] * 16 + (n-1) % 16
+ * (the slot of this step's token); n == 0 gives -1.  A length beyond the
+ * table or a table entry outside [0, num_blocks) gives -1 and sets a status
+ * bit.  slot_mapping: [num_seqs] int64, device. */
+pkv_status paged_kv_slot_mapping(const int32_t* block_tables, int max_blocks_per_seq,
+                                 const int32_t* context_lens, int num_seqs, int num_blocks,
+                                 int64_t* slot_mapping, pkv_stream_t stream);
+
+/* The KV write ([P3] item 3 layout): for each token t with slot =
+ * slot_mapping[t] >= 0, copies k_new[t] and v_new[t] ([num_kv_heads][head_dim]
+ * each) into row slot % 16 of physical block slot / 16 of one layer's pools.
+ * slot < 0 marks a padding token (skipped); slot >= num_blocks * 16 is
+ * skipped and flagged.  Slots must be unique within a call.  Bit-exact copy.
+ * k_new, v_new: [num_tokens][num_kv_heads][head_dim]; k_cache, v_cache: one
+ * layer's pools; head_dim * 2 bytes must be a multiple of 16. */
+pkv_status reshape_and_cache(const void* k_new, const void* v_new, void* k_cache,
+                             void* v_cache, const int64_t* slot_mapping, int num_tokens,
+                             int num_blocks, int num_kv_heads, int head_dim, pkv_dtype dtype,
+                             pkv_stream_t stream);
+
+/* Workspace (bytes) paged_attention_decode needs for these sizes: the
+ * split-context partials (running max, running sum and unnormalised output
+ * per partition and query head, fp32) plus partition offsets.  The caller
+ * allocates it (device, 256-byte aligned) and may reuse it across calls on
+ * the same stream; its contents need no initialisation. */
+size_t paged_attention_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
+                                       int max_context_len);
+
+/* Decode attention ([P2] step 5; [P3] §2, items 1 and 3): for each sequence s
+ * and query head i, with n = context_lens[s] and KV head h = i / (num_q_heads
+ * / num_kv_heads), over the n tokens found through block_tables[s]:
+ *     z_t = scale * <q[s][i], K_t[h]>,  w = softmax(z),  out[s][i] = sum_t w_t V_t[h].
+ * Long contexts are split into partitions processed in parallel; each keeps
+ * a running max and sum (online softmax) and a merge kernel combines them by
+ * log-sum-exp.
+ *  q, out:     [num_seqs][num_q_heads][head_dim], dtype.
+ *  k_cache, v_cache: one layer's pools, dtype.
+ *  max_context_len: host upper bound on every context_lens[s] (sizes grids
+ *              and the workspace); a device length above it (or above
+ *              max_blocks_per_seq * 16, or negative) is flagged and its output
+ *              row is written as zeros.
+ *  workspace:  >= paged_attention_workspace_bytes(num_seqs, num_q_heads,
+ *              head_dim, max_context_len) bytes, else PKV_ERR_WORKSPACE.
+ * Supported: head_dim 64 or 128, num_q_heads / num_kv_heads in 1..8,
+ * num_seqs <= 8192; else PKV_ERR_UNSUPPORTED. */
+pkv_status paged_attention_decode(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_tables, int max_blocks_per_seq,
+                                  const int32_t* context_lens, int max_context_len,
+                                  int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                  int num_blocks, float scale, void* out, void* workspace,
+                                  size_t workspace_bytes, pkv_dtype dtype, pkv_stream_t stream);
+
+/* As paged_attention_decode, with the partition length fixed by the caller:
+ * partition_blocks > 0 physical blocks (16 tokens each) per partition; 0
+ * picks it from the device-side lengths as paged_attention_decode does.
+ * The result does not depend on the partition length beyond fp32 rounding.
+ * partition_blocks must be >= paged_attention_min_partition_blocks(
+ * max_context_len) so that the workspace bound holds. */
+pkv_status paged_attention_decode_partitioned(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, int num_seqs,
+    int num_q_heads, int num_kv_heads, int head_dim, int num_blocks, float scale, void* out,
+    void* workspace, size_t workspace_bytes, int partition_blocks, pkv_dtype dtype,
+    pkv_stream_t stream);
+
+/* Smallest partition length (blocks) the workspace bound allows. */
+int paged_attention_min_partition_blocks(int max_context_len);
+
+/* The two passes of paged_attention_decode_partitioned, enqueued separately
+ * (same arguments, same workspace, same partition_blocks; call the partition
+ * pass first).  The partition pass computes, per (partition, KV head), the
+ * running max, running sum and unnormalised output of each query head and
+ * writes sequences that fit in one partition straight to `out`; the merge
+ * pass combines the partitions of the other sequences by log-sum-exp:
+ *     M = max_p m_p,  L = sum_p l_p e^(m_p - M),  out = sum_p o_p e^(m_p - M) / L.
+ * The merge pass enqueues nothing when no sequence can span two partitions. */
+pkv_status paged_attention_partition_pass(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, int num_seqs,
+    int num_q_heads, int num_kv_heads, int head_dim, int num_blocks, float scale, void* out,
+    void* workspace, size_t workspace_bytes, int partition_blocks, pkv_dtype dtype,
+    pkv_stream_t stream);
+pkv_status paged_attention_merge_pass(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, int num_seqs,
+    int num_q_heads, int num_kv_heads, int head_dim, int num_blocks, float scale, void* out,
+    void* workspace, size_t workspace_bytes, int partition_blocks, pkv_dtype dtype,
+    pkv_stream_t stream);
+
+/* The write half of a decode step ([P3] §2 and item 1): for each sequence
+ * with n = context_lens[s] > 0, copies k_new[s] and v_new[s]
+ * ([num_seqs][num_kv_heads][head_dim]) to the slot of position n - 1
+ * (as paged_kv_slot_mapping computes it) in one layer's pools.  An empty or
+ * invalid row writes nothing (invalid values are flagged).  slot_mapping_out
+ * may be NULL. */
+pkv_status paged_kv_write_new_tokens(const void* k_new, const void* v_new, void* k_cache,
+                                     void* v_cache, const int32_t* block_tables,
+                                     int max_blocks_per_seq, const int32_t* context_lens,
+                                     int num_seqs, int num_blocks, int num_kv_heads,
+                                     int head_dim, int64_t* slot_mapping_out, pkv_dtype dtype,
+                                     pkv_stream_t stream);
+
+/* One decode step of one layer ([P3] §2 and item 1: write, then attend):
+ * paged_kv_write_new_tokens followed by paged_attention_decode.
+ * slot_mapping_out may be NULL; if not, it receives the slots ([num_seqs]
+ * int64, device). */
+pkv_status paged_kv_decode_step(const void* q, const void* k_new, const void* v_new,
+                                void* k_cache, void* v_cache, const int32_t* block_tables,
+                                int max_blocks_per_seq, const int32_t* context_lens,
+                                int max_context_len, int num_seqs, int num_q_heads,
+                                int num_kv_heads, int head_dim, int num_blocks, float scale,
+                                void* out, int64_t* slot_mapping_out, void* workspace,
+                                size_t workspace_bytes, pkv_dtype dtype, pkv_stream_t stream);
+
+/* Device staging bytes paged_kv_decode_step_host needs: device copies of q,
+ * k_new, v_new, block_tables, context_lens and out, each 256-byte aligned. */
+size_t paged_kv_decode_step_staging_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                          int head_dim, int max_blocks_per_seq);
+
+/* paged_kv_decode_step with the step's inputs and its output in HOST memory
+ * (page-locked, so that the copies are asynchronous): q_host, k_new_host,
+ * v_new_host, block_tables_host and context_lens_host are copied into the
+ * caller's device `staging` buffer on `stream` (one cudaMemcpyAsync each),
+ * the step runs on the device-resident pools, and the attention output is
+ * copied back to out_host.  The call returns once everything is enqueued:
+ * synchronise `stream` before reading out_host.  Shapes and dtypes as for
+ * paged_kv_decode_step; staging_bytes must be at least
+ * paged_kv_decode_step_staging_bytes(...). */
+pkv_status paged_kv_decode_step_host(const void* q_host, const void* k_new_host,
+                                     const void* v_new_host, const int32_t* block_tables_host,
+                                     const int32_t* context_lens_host, void* out_host,
+                                     void* staging, size_t staging_bytes, void* k_cache,
+                                     void* v_cache, int max_blocks_per_seq, int max_context_len,
+                                     int num_seqs, int num_q_heads, int num_kv_heads,
+                                     int head_dim, int num_blocks, float scale, void* workspace,
+                                     size_t workspace_bytes, pkv_dtype dtype,
+                                     pkv_stream_t stream);
+
+/* Device status word of the current device: returns (in *flags) the
+ * PKV_DEV_* bits set by kernels since the last reset, and clears them if
+ * `reset` is non-zero.  Synchronises the device. */
+pkv_status pkv_device_status(unsigned int* flags, int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H_ */

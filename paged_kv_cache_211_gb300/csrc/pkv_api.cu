@@ -1,0 +1,156 @@
+// pkv_api.cu -- library-wide entry points: version, status text, pool sizing,
+// the device status word, and the host-buffer decode step.
+#include <mutex>
+
+#include "pkv_internal.cuh"
+
+namespace {
+
+// Sticky flags set by kernels that met a bad device-side value (see the
+// PKV_DEV_* bits in pagedkv.h).  One word per device (module memory).
+__device__ unsigned int g_status_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned int* g_status_ptr[kMaxDevices];
+int g_sm_count[kMaxDevices];
+
+int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    return (dev >= 0 && dev < kMaxDevices) ? dev : -1;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+namespace pkv {
+
+unsigned int* status_word() {
+    int dev = current_device();
+    if (dev < 0) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<unsigned int*>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+int sm_count() {
+    int dev = current_device();
+    if (dev < 0) return 0;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_sm_count[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        g_sm_count[dev] = n;
+    }
+    return g_sm_count[dev];
+}
+
+}  // namespace pkv
+
+extern "C" {
+
+int pkv_version(void) { return 100; }
+
+const char* pkv_status_string(pkv_status s) {
+    switch (s) {
+        case PKV_OK: return "ok";
+        case PKV_ERR_INVALID_ARG: return "invalid argument";
+        case PKV_ERR_UNSUPPORTED: return "unsupported shape";
+        case PKV_ERR_NO_BLOCKS: return "not enough free blocks";
+        case PKV_ERR_BAD_BLOCK_ID: return "bad block id";
+        case PKV_ERR_CUDA: return "CUDA error";
+        case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+size_t pkv_cache_bytes(int num_layers, int num_blocks, int block_size, int num_kv_heads,
+                       int head_dim, pkv_dtype dtype) {
+    if (num_layers <= 0 || num_blocks <= 0 || num_kv_heads <= 0 || head_dim <= 0) return 0;
+    if (block_size != PKV_BLOCK_SIZE) return 0;
+    if (dtype != PKV_F16 && dtype != PKV_BF16) return 0;
+    return (size_t)num_layers * (size_t)num_blocks * (size_t)block_size *
+           (size_t)num_kv_heads * (size_t)head_dim * 2u;
+}
+
+pkv_status pkv_device_status(unsigned int* flags, int reset) {
+    if (!flags) return PKV_ERR_INVALID_ARG;
+    unsigned int* p = pkv::status_word();
+    if (!p) return PKV_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaMemcpy(flags, p, sizeof(unsigned int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (reset && cudaMemset(p, 0, sizeof(unsigned int)) != cudaSuccess) return PKV_ERR_CUDA;
+    if (reset && cudaDeviceSynchronize() != cudaSuccess) return PKV_ERR_CUDA;
+    return PKV_OK;
+}
+
+size_t paged_kv_decode_step_staging_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
+                                          int head_dim, int max_blocks_per_seq) {
+    if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        max_blocks_per_seq <= 0)
+        return 0;
+    const size_t B = (size_t)num_seqs;
+    size_t total = 0;
+    total += align_up(B * num_q_heads * head_dim * 2, 256);          // q
+    total += 2 * align_up(B * num_kv_heads * head_dim * 2, 256);     // k_new, v_new
+    total += align_up(B * (size_t)max_blocks_per_seq * 4, 256);      // block_tables
+    total += align_up(B * 4, 256);                                   // context_lens
+    total += align_up(B * num_q_heads * head_dim * 2, 256);          // out
+    return total;
+}
+
+pkv_status paged_kv_decode_step_host(const void* q_host, const void* k_new_host,
+                                     const void* v_new_host, const int32_t* block_tables_host,
+                                     const int32_t* context_lens_host, void* out_host,
+                                     void* staging, size_t staging_bytes, void* k_cache,
+                                     void* v_cache, int max_blocks_per_seq, int max_context_len,
+                                     int num_seqs, int num_q_heads, int num_kv_heads,
+                                     int head_dim, int num_blocks, float scale, void* workspace,
+                                     size_t workspace_bytes, pkv_dtype dtype,
+                                     pkv_stream_t stream) {
+    if (!q_host || !k_new_host || !v_new_host || !block_tables_host || !context_lens_host ||
+        !out_host || !staging)
+        return PKV_ERR_INVALID_ARG;
+    const size_t need = paged_kv_decode_step_staging_bytes(num_seqs, num_q_heads, num_kv_heads,
+                                                           head_dim, max_blocks_per_seq);
+    if (need == 0) return PKV_ERR_INVALID_ARG;
+    if (staging_bytes < need || (reinterpret_cast<uintptr_t>(staging) & 255u))
+        return PKV_ERR_WORKSPACE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const size_t B = (size_t)num_seqs;
+    const size_t q_bytes = B * num_q_heads * head_dim * 2;
+    const size_t kv_bytes = B * num_kv_heads * head_dim * 2;
+    const size_t bt_bytes = B * (size_t)max_blocks_per_seq * 4;
+    char* p = static_cast<char*>(staging);
+    void* q_d = p;                p += align_up(q_bytes, 256);
+    void* kn_d = p;               p += align_up(kv_bytes, 256);
+    void* vn_d = p;               p += align_up(kv_bytes, 256);
+    int32_t* bt_d = reinterpret_cast<int32_t*>(p);  p += align_up(bt_bytes, 256);
+    int32_t* cl_d = reinterpret_cast<int32_t*>(p);  p += align_up(B * 4, 256);
+    void* out_d = p;
+    const cudaMemcpyKind h2d = cudaMemcpyHostToDevice;
+    if (cudaMemcpyAsync(q_d, q_host, q_bytes, h2d, st) != cudaSuccess ||
+        cudaMemcpyAsync(kn_d, k_new_host, kv_bytes, h2d, st) != cudaSuccess ||
+        cudaMemcpyAsync(vn_d, v_new_host, kv_bytes, h2d, st) != cudaSuccess ||
+        cudaMemcpyAsync(bt_d, block_tables_host, bt_bytes, h2d, st) != cudaSuccess ||
+        cudaMemcpyAsync(cl_d, context_lens_host, B * 4, h2d, st) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    pkv_status rc = paged_kv_decode_step(q_d, kn_d, vn_d, k_cache, v_cache, bt_d,
+                                         max_blocks_per_seq, cl_d, max_context_len, num_seqs,
+                                         num_q_heads, num_kv_heads, head_dim, num_blocks, scale,
+                                         out_d, nullptr, workspace, workspace_bytes, dtype,
+                                         stream);
+    if (rc != PKV_OK) return rc;
+    if (cudaMemcpyAsync(out_host, out_d, q_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    return PKV_OK;
+}
+
+}  // extern "C"

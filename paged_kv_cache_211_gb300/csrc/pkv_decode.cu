@@ -1,0 +1,786 @@
+// pkv_decode.cu -- decode-step PagedAttention: split-context partition pass
+// and log-sum-exp merge.
+//
+// What is computed ("MinivLLM" 使用教程 step 5 / 核心亮点: PagedAttention for
+// the decode stage; "从零手写 vLLM 核心：mini-vllm 项目深度解析" §2: 16-token
+// blocks reached through a block table; §关键工程决策 item 1: per-layer
+// lengths; item 3: [num_blocks][16][num_kv_heads][head_dim] pools): for every
+// sequence s and query head i (KV head h = i / g, g = Hq / Hkv)
+//     out[s][i] = sum_t softmax_t(scale * <q[s][i], K_t[h]>) * V_t[h]
+// over the t < context_lens[s] tokens of the sequence.
+//
+// Work decomposition.  A sequence's logical blocks are cut into partitions
+// of PB blocks; a work item is (partition, KV head).  Each CTA of the
+// persistent partition kernel walks items with a grid stride.  Inside an
+// item, warp w takes the item's blocks w, w + 4, w + 8, ... and keeps an
+// online softmax (running max m, running sum l, unnormalised output o) for
+// the g query heads of its KV head; the four warps are combined through
+// shared memory at the end of the item.  A sequence with one partition gets
+// its output written directly; otherwise the item leaves (m, l, o) in the
+// workspace and the merge kernel combines the partitions by log-sum-exp.
+//
+// Per 16-token block and KV head, a warp does the two contractions on the
+// tensor cores with mma.sync m16n8k16 (fp32 accumulate):
+//   scores  S^T[16 tok x 8 heads] = K[16 tok x D] . Q^T[D x 8 heads]
+//   output  O^T[D x 8 heads]     += V^T[D x 16 tok] . P^T[16 tok x 8 heads]
+// The g <= 8 query heads of the group form the n = 8 side, so each K/V row
+// is read from HBM once per KV head, not once per query head.  K and V are
+// loaded straight from global memory into the MMA operand registers with
+// 16-byte loads: lane (r = lane/4, c = lane%4) reads, for K, rows r and r+8
+// of the block (16-byte chunks 4j + c) and, for V, rows 2c, 2c+1, 2c+8, 2c+9
+// (chunks r and r + 8).  The reduction index D of the score MMA may be
+// permuted freely as long as q uses the same permutation, which is what
+// makes the K chunks usable as-is; V rows are paired into token pairs with
+// byte permutes, and P is brought from the score layout to the operand
+// layout of the second MMA with two 8x8 movmatrix transposes.  Loads of the
+// next block are issued before the current block is computed (two register
+// stages).
+#include <algorithm>
+#include <cmath>
+
+#include "pkv_internal.cuh"
+
+namespace pkv {
+
+pkv_status launch_decode_step_write(const void* k_new, const void* v_new, void* k_cache,
+                                    void* v_cache, const int32_t* block_tables,
+                                    int max_blocks_per_seq, const int32_t* context_lens,
+                                    int num_seqs, int num_blocks, int num_kv_heads, int head_dim,
+                                    int64_t* slot_out, cudaStream_t stream);
+
+namespace {
+
+constexpr int kWarps = 4;                 // warps per CTA of the partition kernel
+constexpr int kThreads = kWarps * 32;
+constexpr int kMaxGroup = 8;              // query heads per KV head (the MMA's n = 8)
+constexpr int kMaxSeqs = 8192;            // per call (lengths and offsets live in smem)
+constexpr int kMaxPartitionsPerSeq = 64;  // bounds the workspace
+constexpr int kAdaptiveMinBlocks = 8;     // adaptive partitions are at least this long
+constexpr int kAdaptiveMaxBlocks = 512;
+constexpr int kItemsPerCta = 4;           // adaptive partitioning aims at this many per CTA
+constexpr float kLog2e = 1.4426950408889634f;
+
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+int min_partition_blocks(int max_context_len) {
+    const int mb = ceil_div(std::max(max_context_len, 0), PKV_BLOCK_SIZE);
+    return std::max(1, ceil_div(mb, kMaxPartitionsPerSeq));
+}
+
+struct WsLayout {
+    size_t offsets, m, l, o, total;
+};
+
+WsLayout ws_layout(int num_seqs, int num_q_heads, int head_dim, int max_context_len) {
+    const int mb = ceil_div(std::max(max_context_len, 0), PKV_BLOCK_SIZE);
+    const int parts = std::max(1, ceil_div(mb, min_partition_blocks(max_context_len)));
+    const size_t rows = (size_t)num_seqs * parts * num_q_heads;
+    WsLayout w;
+    w.offsets = 0;
+    w.m = align256((size_t)(num_seqs + 1) * 4);
+    w.l = w.m + align256(rows * 4);
+    w.o = w.l + align256(rows * 4);
+    w.total = w.o + align256(rows * head_dim * 4);
+    return w;
+}
+
+struct DecodeParams {
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    void* out;
+    int* ws_offsets;
+    float* ws_m;
+    float* ws_l;
+    float* ws_o;
+    unsigned int* status;
+    int num_seqs, num_q_heads, num_kv_heads, group;
+    int max_blocks_per_seq, num_blocks, len_bound;
+    int partition_blocks;      // > 0: fixed partition length (blocks)
+    int min_partition_blocks;  // lower bound of the adaptive choice
+    int target_items;
+    float scale_log2;          // scale * log2(e): scores live in base 2
+};
+
+// Sum over the CTA; every thread gets the result.
+__device__ __forceinline__ int cta_sum(int v, int* red) {
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    int t = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) t += red[w];
+    return t;
+}
+
+// Exclusive prefix sum over the CTA (thread order); *total gets the sum.
+__device__ __forceinline__ int cta_exclusive_scan(int v, int* red, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+    }
+    __syncthreads();
+    if (lane == 31) red[warp] = incl;
+    __syncthreads();
+    int before = 0, all = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        if (w < warp) before += red[w];
+        all += red[w];
+    }
+    *total = all;
+    return before + incl - v;
+}
+
+__device__ __forceinline__ int parts_of(int n, int pb) {
+    const int nblk = (n + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
+    return nblk == 0 ? 1 : (nblk + pb - 1) / pb;  // an empty sequence keeps one (empty) partition
+}
+
+// Operand registers of one 16-token block for one lane (see the file comment).
+template <int D>
+struct BlockFrag {
+    static constexpr int KC = D / 32;  // K: 16-byte chunks per row (rows r and r+8)
+    static constexpr int VC = D / 64;  // V: 16-byte chunks per token (4 tokens)
+    uint4 k[2][KC];
+    uint4 v[VC][4];
+    bool bad;
+};
+
+template <typename T, int D>
+__device__ __forceinline__ void fetch_block(BlockFrag<D>& f, const T* kbase, const T* vbase,
+                                            int id, size_t row_stride, int gid, int tig) {
+    f.bad = id < 0;
+    const size_t blk = (size_t)(f.bad ? 0 : id) * PKV_BLOCK_SIZE;
+    const T* kr0 = kbase + (blk + gid) * row_stride;
+    const T* kr1 = kr0 + 8 * row_stride;
+#pragma unroll
+    for (int j = 0; j < BlockFrag<D>::KC; ++j) {
+        f.k[0][j] = ld_stream(kr0 + (4 * j + tig) * 8);
+        f.k[1][j] = ld_stream(kr1 + (4 * j + tig) * 8);
+    }
+#pragma unroll
+    for (int c = 0; c < BlockFrag<D>::VC; ++c) {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int tok = 2 * tig + (t & 1) + (t >> 1) * 8;
+            f.v[c][t] = ld_stream(vbase + (blk + tok) * row_stride + (gid + 8 * c) * 8);
+        }
+    }
+}
+
+template <typename T, int D>
+struct WarpState {
+    static constexpr int NT = D / 16;  // 16-row tiles of the output's D axis
+    float m0, m1;                      // running max (base 2) of heads 2c, 2c+1
+    float l0, l1;                      // this lane's share of the running sums
+    float o[NT][4];                    // O^T accumulator fragments
+};
+
+template <typename T, int D>
+__device__ __forceinline__ void compute_block(WarpState<T, D>& st, BlockFrag<D>& f,
+                                              const uint4 (&qf)[D / 32], int nv, float scale_log2,
+                                              int gid, int tig) {
+    using E = Elem<T>;
+    constexpr int KC = BlockFrag<D>::KC;
+    constexpr int NT = WarpState<T, D>::NT;
+    float sa[4] = {0.f, 0.f, 0.f, 0.f};
+    float sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < KC; ++j) {
+        E::mma(sa, f.k[0][j].x, f.k[1][j].x, f.k[0][j].y, f.k[1][j].y, qf[j].x, qf[j].y);
+        E::mma(sb, f.k[0][j].z, f.k[1][j].z, f.k[0][j].w, f.k[1][j].w, qf[j].z, qf[j].w);
+    }
+    // rows: token gid (s0, s1) and gid + 8 (s2, s3); columns: heads 2*tig, 2*tig + 1
+    float s0 = (sa[0] + sb[0]) * scale_log2;
+    float s1 = (sa[1] + sb[1]) * scale_log2;
+    float s2 = (sa[2] + sb[2]) * scale_log2;
+    float s3 = (sa[3] + sb[3]) * scale_log2;
+    if (nv < PKV_BLOCK_SIZE) {  // last (partial) block or a skipped bad block: select, never weight
+        if (gid >= nv) s0 = s1 = -INFINITY;
+        if (gid + 8 >= nv) s2 = s3 = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < BlockFrag<D>::VC; ++c) {
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int tok = 2 * tig + (t & 1) + (t >> 1) * 8;
+                if (tok >= nv) f.v[c][t] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+    }
+    float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(st.m0, mx0), mn1 = fmaxf(st.m1, mx1);
+    const float ms0 = mn0 == -INFINITY ? 0.f : mn0;  // all-masked so far: keep everything 0
+    const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float c0 = fast_exp2(st.m0 - ms0), c1 = fast_exp2(st.m1 - ms1);
+    const float p0 = fast_exp2(s0 - ms0), p1 = fast_exp2(s1 - ms1);
+    const float p2 = fast_exp2(s2 - ms0), p3 = fast_exp2(s3 - ms1);
+    st.l0 = st.l0 * c0 + p0 + p2;
+    st.l1 = st.l1 * c1 + p1 + p3;
+    st.m0 = mn0;
+    st.m1 = mn1;
+#pragma unroll
+    for (int i = 0; i < NT; ++i) {
+        st.o[i][0] *= c0;
+        st.o[i][1] *= c1;
+        st.o[i][2] *= c0;
+        st.o[i][3] *= c1;
+    }
+    // P^T operand: lane (gid, tig) needs head gid at tokens 2tig, 2tig+1 (+8)
+    const uint32_t pt = movmatrix_trans(E::pack(p0, p1));
+    const uint32_t pb = movmatrix_trans(E::pack(p2, p3));
+#pragma unroll
+    for (int i = 0; i < NT; ++i) {
+        const int c = i >> 2, w = i & 3;
+        const uint32_t x0 = word_of(f.v[c][0], w), x1 = word_of(f.v[c][1], w);
+        const uint32_t x2 = word_of(f.v[c][2], w), x3 = word_of(f.v[c][3], w);
+        E::mma(st.o[i], __byte_perm(x0, x1, 0x5410), __byte_perm(x0, x1, 0x7632),
+               __byte_perm(x2, x3, 0x5410), __byte_perm(x2, x3, 0x7632), pt, pb);
+    }
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const DecodeParams p) {
+    constexpr int KC = BlockFrag<D>::KC;
+    constexpr int VC = BlockFrag<D>::VC;
+    constexpr int NT = WarpState<T, D>::NT;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    __shared__ int red[kWarps];
+    const int B = p.num_seqs;
+    float* sm_o = reinterpret_cast<float*>(smem_raw);  // [kWarps][8][D]
+    float* sm_m = sm_o + kWarps * kMaxGroup * D;        // [kWarps][8]
+    float* sm_l = sm_m + kWarps * kMaxGroup;            // [kWarps][8]
+    int* sm_len = reinterpret_cast<int*>(sm_l + kWarps * kMaxGroup);  // [B]
+    int* sm_off = sm_len + B;                                          // [B + 1]
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int gid = lane >> 2, tig = lane & 3;
+
+    // (1) validated lengths and the total number of blocks
+    int my_blocks = 0;
+    for (int s = tid; s < B; s += kThreads) {
+        int n = p.context_lens[s];
+        if (n < 0 || n > p.len_bound) {
+            if (blockIdx.x == 0) atomicOr(p.status, PKV_DEV_BAD_LENGTH);
+            n = 0;  // the row is written as zeros
+        }
+        sm_len[s] = n;
+        my_blocks += (n + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
+    }
+    const int total_blocks = cta_sum(my_blocks, red);
+
+    // (2) partition length: fixed, or enough items for every CTA
+    int PB = p.partition_blocks;
+    if (PB <= 0) {
+        const long long want =
+            ((long long)total_blocks * p.num_kv_heads + p.target_items - 1) / p.target_items;
+        const long long lo = p.min_partition_blocks;
+        const long long hi = kAdaptiveMaxBlocks > lo ? kAdaptiveMaxBlocks : lo;
+        PB = (int)(want < lo ? lo : (want > hi ? hi : want));
+    }
+
+    // (3) partitions per sequence and their exclusive prefix sum
+    const int chunk = (B + kThreads - 1) / kThreads;
+    const int s_lo = min(B, tid * chunk), s_hi = min(B, s_lo + chunk);
+    int mine = 0;
+    for (int s = s_lo; s < s_hi; ++s) mine += parts_of(sm_len[s], PB);
+    int total_parts = 0;
+    int run = cta_exclusive_scan(mine, red, &total_parts);
+    for (int s = s_lo; s < s_hi; ++s) {
+        sm_off[s] = run;
+        run += parts_of(sm_len[s], PB);
+    }
+    if (tid == 0) sm_off[B] = total_parts;
+    __syncthreads();
+    if (blockIdx.x == 0) {
+        for (int s = tid; s <= B; s += kThreads) p.ws_offsets[s] = sm_off[s];
+    }
+
+    const T* __restrict__ q = static_cast<const T*>(p.q);
+    const T* __restrict__ kc = static_cast<const T*>(p.k_cache);
+    const T* __restrict__ vc = static_cast<const T*>(p.v_cache);
+    const int Hq = p.num_q_heads, Hkv = p.num_kv_heads, g = p.group;
+    const size_t row_stride = (size_t)Hkv * D;
+    const int total_items = total_parts * Hkv;
+
+    for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
+        const int gp = item / Hkv;
+        const int h = item - gp * Hkv;
+        int a = 0, b = B - 1;  // the sequence owning global partition gp
+        while (a < b) {
+            const int mid = (a + b + 1) >> 1;
+            if (sm_off[mid] <= gp) a = mid; else b = mid - 1;
+        }
+        const int s = a;
+        const int part = gp - sm_off[s];
+        const int nparts = sm_off[s + 1] - sm_off[s];
+        const int n = sm_len[s];
+        const int nblk = (n + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
+        const int blk_lo = part * PB;
+        const int blk_hi = min(nblk, blk_lo + PB);
+
+        // query fragment: column gid of the score MMA is query head h*g + gid
+        uint4 qf[KC];
+        {
+            const bool live = gid < g;
+            const T* qrow = q + ((size_t)s * Hq + (size_t)h * g + (live ? gid : 0)) * D;
+#pragma unroll
+            for (int j = 0; j < KC; ++j)
+                qf[j] = live ? *reinterpret_cast<const uint4*>(qrow + (4 * j + tig) * 8)
+                             : make_uint4(0u, 0u, 0u, 0u);
+        }
+
+        WarpState<T, D> st;
+        st.m0 = st.m1 = -INFINITY;
+        st.l0 = st.l1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < NT; ++i) st.o[i][0] = st.o[i][1] = st.o[i][2] = st.o[i][3] = 0.f;
+
+        const T* kbase = kc + (size_t)h * D;
+        const T* vbase = vc + (size_t)h * D;
+        const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
+        // physical ids of this warp's blocks, 32 at a time (lane l: block j0 + l*kWarps)
+        auto load_ids = [&](int j0) {
+            const int j = j0 + lane * kWarps;
+            int id = -1;
+            if (j < blk_hi) {
+                id = table[j];
+                if (id < 0 || id >= p.num_blocks) {
+                    atomicOr(p.status, PKV_DEV_BAD_BLOCK_ID);
+                    id = -1;  // never dereferenced; its tokens are masked out
+                }
+            }
+            return id;
+        };
+        int j = blk_lo + warp;
+        int k = 0;  // index of block j among this warp's blocks
+        int ids = 0;
+        BlockFrag<D> fa, fb;
+        if (j < blk_hi) {
+            ids = load_ids(j);
+            fetch_block<T, D>(fa, kbase, vbase, __shfl_sync(0xffffffffu, ids, 0), row_stride,
+                              gid, tig);
+        }
+        while (j < blk_hi) {
+            int jn = j + kWarps;
+            if (jn < blk_hi) {
+                if (((k + 1) & 31) == 0) ids = load_ids(jn);
+                fetch_block<T, D>(fb, kbase, vbase, __shfl_sync(0xffffffffu, ids, (k + 1) & 31),
+                                  row_stride, gid, tig);
+            }
+            compute_block<T, D>(st, fa, qf, fa.bad ? 0 : min(PKV_BLOCK_SIZE, n - j * 16),
+                                p.scale_log2, gid, tig);
+            j = jn;
+            ++k;
+            if (j >= blk_hi) break;
+            jn = j + kWarps;
+            if (jn < blk_hi) {
+                if (((k + 1) & 31) == 0) ids = load_ids(jn);
+                fetch_block<T, D>(fa, kbase, vbase, __shfl_sync(0xffffffffu, ids, (k + 1) & 31),
+                                  row_stride, gid, tig);
+            }
+            compute_block<T, D>(st, fb, qf, fb.bad ? 0 : min(PKV_BLOCK_SIZE, n - j * 16),
+                                p.scale_log2, gid, tig);
+            j = jn;
+            ++k;
+        }
+
+        // full sums over the eight token rows of the fragment
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, off);
+            st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, off);
+        }
+        // this warp's (m, l, o) -> shared memory; lane holds heads 2tig, 2tig+1 at
+        // d = 8*(gid + 8c) + e, e = 0..7, from tiles 4c .. 4c+3
+        float* mo = sm_o + warp * kMaxGroup * D;
+#pragma unroll
+        for (int c = 0; c < VC; ++c) {
+            const int d0 = 8 * (gid + 8 * c);
+            float* r0 = mo + (2 * tig) * D + d0;
+            float* r1 = mo + (2 * tig + 1) * D + d0;
+            *reinterpret_cast<float4*>(r0) =
+                make_float4(st.o[4 * c][0], st.o[4 * c][2], st.o[4 * c + 1][0], st.o[4 * c + 1][2]);
+            *reinterpret_cast<float4*>(r0 + 4) = make_float4(
+                st.o[4 * c + 2][0], st.o[4 * c + 2][2], st.o[4 * c + 3][0], st.o[4 * c + 3][2]);
+            *reinterpret_cast<float4*>(r1) =
+                make_float4(st.o[4 * c][1], st.o[4 * c][3], st.o[4 * c + 1][1], st.o[4 * c + 1][3]);
+            *reinterpret_cast<float4*>(r1 + 4) = make_float4(
+                st.o[4 * c + 2][1], st.o[4 * c + 2][3], st.o[4 * c + 3][1], st.o[4 * c + 3][3]);
+        }
+        if (gid == 0) {
+            sm_m[warp * kMaxGroup + 2 * tig] = st.m0;
+            sm_m[warp * kMaxGroup + 2 * tig + 1] = st.m1;
+            sm_l[warp * kMaxGroup + 2 * tig] = st.l0;
+            sm_l[warp * kMaxGroup + 2 * tig + 1] = st.l1;
+        }
+        __syncthreads();
+
+        // combine the warps: one thread per (query head of the group, 8-wide slice of D)
+        constexpr int SL = D / 8;
+        for (int x = tid; x < g * SL; x += kThreads) {
+            const int hh = x / SL, d0 = (x - hh * SL) * 8;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w * kMaxGroup + hh]);
+            const float Ms = M == -INFINITY ? 0.f : M;
+            float L = 0.f;
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float e = fast_exp2(sm_m[w * kMaxGroup + hh] - Ms);
+                L += e * sm_l[w * kMaxGroup + hh];
+                const float* src = sm_o + (w * kMaxGroup + hh) * D + d0;
+                const float4 u = *reinterpret_cast<const float4*>(src);
+                const float4 v = *reinterpret_cast<const float4*>(src + 4);
+                acc[0] += e * u.x; acc[1] += e * u.y; acc[2] += e * u.z; acc[3] += e * u.w;
+                acc[4] += e * v.x; acc[5] += e * v.y; acc[6] += e * v.z; acc[7] += e * v.w;
+            }
+            const int qh = h * g + hh;
+            if (nparts == 1) {
+                const float inv = L > 0.f ? 1.f / L : 0.f;
+                uint4 packed;
+                packed.x = Elem<T>::pack(acc[0] * inv, acc[1] * inv);
+                packed.y = Elem<T>::pack(acc[2] * inv, acc[3] * inv);
+                packed.z = Elem<T>::pack(acc[4] * inv, acc[5] * inv);
+                packed.w = Elem<T>::pack(acc[6] * inv, acc[7] * inv);
+                *reinterpret_cast<uint4*>(static_cast<T*>(p.out) + ((size_t)s * Hq + qh) * D +
+                                          d0) = packed;
+            } else {
+                const size_t row = (size_t)gp * Hq + qh;
+                float* dst = p.ws_o + row * D + d0;
+                *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+                if (d0 == 0) {
+                    p.ws_m[row] = M;
+                    p.ws_l[row] = L;
+                }
+            }
+        }
+        __syncthreads();  // shared buffers are reused by the next item
+    }
+}
+
+struct MergeParams {
+    const int* ws_offsets;
+    const float* ws_m;
+    const float* ws_l;
+    const float* ws_o;
+    void* out;
+    int num_seqs, num_q_heads;
+};
+
+// Log-sum-exp merge of a sequence's partitions, one warp per (sequence, query head):
+//   M = max_p m_p,  L = sum_p l_p 2^(m_p - M),  out = sum_p o_p 2^(m_p - M) / L.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) decode_merge_kernel(const MergeParams p) {
+    constexpr int PER = D / 32;
+    const int lane = threadIdx.x & 31;
+    const int wg = blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (wg >= p.num_seqs * p.num_q_heads) return;
+    const int Hq = p.num_q_heads;
+    const int s = wg / Hq, qh = wg - s * Hq;
+    const int off = p.ws_offsets[s];
+    const int np = p.ws_offsets[s + 1] - off;
+    if (np <= 1) return;  // written by the partition kernel
+    float M = -INFINITY;
+    for (int i = lane; i < np; i += 32) M = fmaxf(M, p.ws_m[(size_t)(off + i) * Hq + qh]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float Ms = M == -INFINITY ? 0.f : M;
+    float L = 0.f;
+    float acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+#pragma unroll 4
+    for (int i = 0; i < np; ++i) {
+        const size_t r = (size_t)(off + i) * Hq + qh;
+        const float w = fast_exp2(p.ws_m[r] - Ms);
+        L += w * p.ws_l[r];
+        const float* src = p.ws_o + r * D + lane * PER;
+        if constexpr (PER == 4) {
+            const float4 u = *reinterpret_cast<const float4*>(src);
+            acc[0] += w * u.x; acc[1] += w * u.y; acc[2] += w * u.z; acc[3] += w * u.w;
+        } else {
+            const float2 u = *reinterpret_cast<const float2*>(src);
+            acc[0] += w * u.x; acc[1] += w * u.y;
+        }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    T* dst = static_cast<T*>(p.out) + ((size_t)s * Hq + qh) * D + lane * PER;
+    if constexpr (PER == 4) {
+        uint2 packed;
+        packed.x = Elem<T>::pack(acc[0] * inv, acc[1] * inv);
+        packed.y = Elem<T>::pack(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2*>(dst) = packed;
+    } else {
+        *reinterpret_cast<uint32_t*>(dst) = Elem<T>::pack(acc[0] * inv, acc[1] * inv);
+    }
+}
+
+size_t partition_smem_bytes(int head_dim, int num_seqs) {
+    return (size_t)kWarps * kMaxGroup * head_dim * 4 + 2 * kWarps * kMaxGroup * 4 +
+           (size_t)(2 * num_seqs + 1) * 4;
+}
+
+constexpr int kPassPartition = 1;
+constexpr int kPassMerge = 2;
+
+template <typename T, int D>
+pkv_status launch_decode(const DecodeParams& prm_in, const MergeParams& mp, int pb_lower,
+                         int max_blocks, bool need_merge, int passes, cudaStream_t stream) {
+    DecodeParams prm = prm_in;
+    auto kern = decode_partition_kernel<T, D>;
+    const size_t smem = partition_smem_bytes(D, prm.num_seqs);
+    if (smem > 48 * 1024) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return PKV_ERR_CUDA;
+    }
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    const int sms = sm_count();
+    if (sms <= 0) return PKV_ERR_CUDA;
+    const long long parts_upper = (long long)prm.num_seqs * std::max(1, ceil_div(max_blocks, pb_lower));
+    const long long items_upper = parts_upper * prm.num_kv_heads;
+    const int grid = (int)std::max<long long>(1, std::min<long long>(items_upper, (long long)std::max(occ, 1) * sms));
+    prm.target_items = grid * kItemsPerCta;
+    if (passes & kPassPartition) {
+        kern<<<grid, kThreads, smem, stream>>>(prm);
+        if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    }
+    if ((passes & kPassMerge) && need_merge) {
+        const int warps = prm.num_seqs * prm.num_q_heads;
+        decode_merge_kernel<T, D><<<(warps + 3) / 4, 128, 0, stream>>>(mp);
+        if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    }
+    return PKV_OK;
+}
+
+pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, int max_blocks_per_seq,
+                       const int32_t* context_lens, int max_context_len, int num_seqs,
+                       int num_q_heads, int num_kv_heads, int head_dim, int num_blocks,
+                       float scale, void* out, void* workspace, size_t workspace_bytes,
+                       int partition_blocks, pkv_dtype dtype, int passes,
+                       cudaStream_t stream) {
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        max_blocks_per_seq <= 0 || num_blocks <= 0 || max_context_len < 0 ||
+        partition_blocks < 0)
+        return PKV_ERR_INVALID_ARG;
+    if (num_q_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+    if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return PKV_ERR_INVALID_ARG;
+    const int g = num_q_heads / num_kv_heads;
+    if (g > kMaxGroup || (head_dim != 64 && head_dim != 128) || num_seqs > kMaxSeqs)
+        return PKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PKV_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+        return PKV_ERR_INVALID_ARG;
+    const WsLayout ws = ws_layout(num_seqs, num_q_heads, head_dim, max_context_len);
+    if (!workspace || workspace_bytes < ws.total ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return PKV_ERR_WORKSPACE;
+    const int min_pb = min_partition_blocks(max_context_len);
+    if (partition_blocks > 0 && partition_blocks < min_pb) return PKV_ERR_INVALID_ARG;
+    unsigned int* status = status_word();
+    if (!status) return PKV_ERR_CUDA;
+
+    const int len_bound = (int)std::min<long long>(max_context_len,
+                                                   (long long)max_blocks_per_seq * PKV_BLOCK_SIZE);
+    const int max_blocks = ceil_div(len_bound, PKV_BLOCK_SIZE);
+    const int pb_lower =
+        partition_blocks > 0 ? partition_blocks : std::max(min_pb, kAdaptiveMinBlocks);
+    const bool need_merge = max_blocks > pb_lower;
+
+    char* wsb = static_cast<char*>(workspace);
+    DecodeParams prm;
+    prm.q = q;
+    prm.k_cache = k_cache;
+    prm.v_cache = v_cache;
+    prm.block_tables = block_tables;
+    prm.context_lens = context_lens;
+    prm.out = out;
+    prm.ws_offsets = reinterpret_cast<int*>(wsb + ws.offsets);
+    prm.ws_m = reinterpret_cast<float*>(wsb + ws.m);
+    prm.ws_l = reinterpret_cast<float*>(wsb + ws.l);
+    prm.ws_o = reinterpret_cast<float*>(wsb + ws.o);
+    prm.status = status;
+    prm.num_seqs = num_seqs;
+    prm.num_q_heads = num_q_heads;
+    prm.num_kv_heads = num_kv_heads;
+    prm.group = g;
+    prm.max_blocks_per_seq = max_blocks_per_seq;
+    prm.num_blocks = num_blocks;
+    prm.len_bound = len_bound;
+    prm.partition_blocks = partition_blocks;
+    prm.min_partition_blocks = pb_lower;
+    prm.target_items = 0;
+    prm.scale_log2 = scale * kLog2e;
+
+    MergeParams mp;
+    mp.ws_offsets = prm.ws_offsets;
+    mp.ws_m = prm.ws_m;
+    mp.ws_l = prm.ws_l;
+    mp.ws_o = prm.ws_o;
+    mp.out = out;
+    mp.num_seqs = num_seqs;
+    mp.num_q_heads = num_q_heads;
+
+    if (dtype == PKV_BF16) {
+        return head_dim == 128 ? launch_decode<__nv_bfloat16, 128>(prm, mp, pb_lower, max_blocks,
+                                                                   need_merge, passes, stream)
+                               : launch_decode<__nv_bfloat16, 64>(prm, mp, pb_lower, max_blocks,
+                                                                  need_merge, passes, stream);
+    }
+    return head_dim == 128
+               ? launch_decode<__half, 128>(prm, mp, pb_lower, max_blocks, need_merge, passes,
+                                            stream)
+               : launch_decode<__half, 64>(prm, mp, pb_lower, max_blocks, need_merge, passes,
+                                           stream);
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" {
+
+int paged_attention_min_partition_blocks(int max_context_len) {
+    return pkv::min_partition_blocks(max_context_len);
+}
+
+size_t paged_attention_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
+                                       int max_context_len) {
+    if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len < 0) return 0;
+    return pkv::ws_layout(num_seqs, num_q_heads, head_dim, max_context_len).total;
+}
+
+pkv_status paged_attention_decode(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_tables, int max_blocks_per_seq,
+                                  const int32_t* context_lens, int max_context_len,
+                                  int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                  int num_blocks, float scale, void* out, void* workspace,
+                                  size_t workspace_bytes, pkv_dtype dtype, pkv_stream_t stream) {
+    return pkv::decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                            max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                            num_blocks, scale, out, workspace, workspace_bytes, 0, dtype,
+                            pkv::kPassPartition | pkv::kPassMerge,
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status paged_attention_decode_partitioned(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, int num_seqs,
+    int num_q_heads, int num_kv_heads, int head_dim, int num_blocks, float scale, void* out,
+    void* workspace, size_t workspace_bytes, int partition_blocks, pkv_dtype dtype,
+    pkv_stream_t stream) {
+    return pkv::decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                            max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                            num_blocks, scale, out, workspace, workspace_bytes, partition_blocks,
+                            dtype, pkv::kPassPartition | pkv::kPassMerge,
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status paged_attention_partition_pass(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, int num_seqs,
+    int num_q_heads, int num_kv_heads, int head_dim, int num_blocks, float scale, void* out,
+    void* workspace, size_t workspace_bytes, int partition_blocks, pkv_dtype dtype,
+    pkv_stream_t stream) {
+    return pkv::decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                            max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                            num_blocks, scale, out, workspace, workspace_bytes, partition_blocks,
+                            dtype, pkv::kPassPartition, reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status paged_attention_merge_pass(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    int max_blocks_per_seq, const int32_t* context_lens, int max_context_len, int num_seqs,
+    int num_q_heads, int num_kv_heads, int head_dim, int num_blocks, float scale, void* out,
+    void* workspace, size_t workspace_bytes, int partition_blocks, pkv_dtype dtype,
+    pkv_stream_t stream) {
+    return pkv::decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                            max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                            num_blocks, scale, out, workspace, workspace_bytes, partition_blocks,
+                            dtype, pkv::kPassMerge, reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status paged_kv_write_new_tokens(const void* k_new, const void* v_new, void* k_cache,
+                                     void* v_cache, const int32_t* block_tables,
+                                     int max_blocks_per_seq, const int32_t* context_lens,
+                                     int num_seqs, int num_blocks, int num_kv_heads,
+                                     int head_dim, int64_t* slot_mapping_out, pkv_dtype dtype,
+                                     pkv_stream_t stream) {
+    if (num_seqs < 0 || num_kv_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0 ||
+        num_blocks <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+    if ((head_dim * 2) % 16 != 0) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PKV_OK;
+    if (!k_new || !v_new || !k_cache || !v_cache || !block_tables || !context_lens)
+        return PKV_ERR_INVALID_ARG;
+    if (!pkv::aligned16(k_new) || !pkv::aligned16(v_new) || !pkv::aligned16(k_cache) ||
+        !pkv::aligned16(v_cache))
+        return PKV_ERR_INVALID_ARG;
+    return pkv::launch_decode_step_write(k_new, v_new, k_cache, v_cache, block_tables,
+                                         max_blocks_per_seq, context_lens, num_seqs, num_blocks,
+                                         num_kv_heads, head_dim, slot_mapping_out,
+                                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status paged_kv_decode_step(const void* q, const void* k_new, const void* v_new,
+                                void* k_cache, void* v_cache, const int32_t* block_tables,
+                                int max_blocks_per_seq, const int32_t* context_lens,
+                                int max_context_len, int num_seqs, int num_q_heads,
+                                int num_kv_heads, int head_dim, int num_blocks, float scale,
+                                void* out, int64_t* slot_mapping_out, void* workspace,
+                                size_t workspace_bytes, pkv_dtype dtype, pkv_stream_t stream) {
+    if (num_seqs < 0 || num_kv_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0 ||
+        num_blocks <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PKV_OK;
+    if (!k_new || !v_new || !pkv::aligned16(k_new) || !pkv::aligned16(v_new))
+        return PKV_ERR_INVALID_ARG;
+    // validate the attention arguments before anything is enqueued
+    if (num_q_heads <= 0 || num_q_heads % num_kv_heads) return PKV_ERR_INVALID_ARG;
+    if (num_q_heads / num_kv_heads > pkv::kMaxGroup || (head_dim != 64 && head_dim != 128) ||
+        num_seqs > pkv::kMaxSeqs)
+        return PKV_ERR_UNSUPPORTED;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+        return PKV_ERR_INVALID_ARG;
+    if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+    if (!pkv::aligned16(q) || !pkv::aligned16(k_cache) || !pkv::aligned16(v_cache) ||
+        !pkv::aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return PKV_ERR_INVALID_ARG;
+    if (!workspace ||
+        workspace_bytes < paged_attention_workspace_bytes(num_seqs, num_q_heads, head_dim,
+                                                          max_context_len))
+        return PKV_ERR_WORKSPACE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    pkv_status rc = pkv::launch_decode_step_write(k_new, v_new, k_cache, v_cache, block_tables,
+                                                  max_blocks_per_seq, context_lens, num_seqs,
+                                                  num_blocks, num_kv_heads, head_dim,
+                                                  slot_mapping_out, st);
+    if (rc != PKV_OK) return rc;
+    return pkv::decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                            max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                            num_blocks, scale, out, workspace, workspace_bytes, 0, dtype,
+                            pkv::kPassPartition | pkv::kPassMerge, st);
+}
+
+}  // extern "C"

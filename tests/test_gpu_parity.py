@@ -1,0 +1,274 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the CPU oracle.
+
+Cache writes and slot mapping are compared bit for bit; decode attention
+within the stated tolerance (elementwise max(4e-3, 1e-2 |oracle|), and
+1e-2 relative to the largest |oracle|).  Every workload runs in the launch
+configuration the benchmark times (paged_kv_decode_step with the adaptive
+partitioning); the oracle runs on every sequence where it finishes in
+seconds and on sampled sequences otherwise.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_211_gb300 as pkv
+from paged_kv_cache_211_gb300 import workloads as wl
+from gpu_helpers import assert_attention_close, compact_oracle_step, dtype_code, sample_seqs
+from pkv_testutil import bits
+
+pytestmark = pytest.mark.gpu
+
+# sequences the oracle checks per workload (None = all)
+ORACLE_SEQS = {"tiny": None, "qwen3_0p6b": None, "tinyllama_1p1b": 24, "llama7b_long": 5,
+               "prefix_shared": 40}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built(cuda_device):
+    import __graft_entry__
+    __graft_entry__.build()
+    pkv.pkv_device_status(reset=True)
+
+
+def _run_step(inp, dev):
+    w = inp["workload"]
+    q, kc, vc = inp["q"], inp["k_cache"][0], inp["v_cache"][0]
+    max_len = int(inp["context_lens_host"].max())
+    out = torch.empty_like(q)
+    ws = pkv.new_workspace(w.num_seqs, w.num_q_heads, w.head_dim, max_len, dev)
+    slots = torch.full((w.num_seqs,), -7, dtype=torch.int64, device=dev)
+    pkv.paged_kv_decode_step(q, inp["k_new"][0], inp["v_new"][0], kc, vc, inp["block_tables"],
+                             inp["context_lens"], max_len, w.scale, out, ws,
+                             slot_mapping_out=slots)
+    torch.cuda.synchronize()
+    return out, slots
+
+
+@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+def test_decode_step_parity(name, cuda_device):
+    w = wl.WORKLOADS[name]
+    inp = wl.make_inputs(w, device=cuda_device, num_layers=1)
+    lens, tables = inp["context_lens_host"], inp["block_tables_host"]
+    k_orig, v_orig = inp["k_cache"][0].clone(), inp["v_cache"][0].clone()
+    nsel = ORACLE_SEQS[name]
+    seq_ids = np.arange(w.num_seqs) if nsel is None else sample_seqs(lens, nsel, seed=w.seed)
+    want, kn_rows, vn_rows = compact_oracle_step(inp, seq_ids)   # before the GPU touches anything
+
+    out, slots = _run_step(inp, cuda_device)
+    assert pkv.pkv_device_status() == 0
+
+    # block-table plumbing: bit-exact against the oracle on the full tables
+    want_slots = oracle.slot_mapping(tables, lens, 16, w.num_blocks)
+    assert np.array_equal(slots.cpu().numpy(), want_slots)
+
+    # KV write: the written rows equal the oracle's, every other byte is unchanged
+    kc, vc = inp["k_cache"][0], inp["v_cache"][0]
+    flat = lambda t: t.view(-1, w.num_kv_heads, w.head_dim)
+    sl = torch.from_numpy(want_slots).to(cuda_device)
+    sel = torch.from_numpy(seq_ids).to(cuda_device)
+    assert np.array_equal(bits(flat(kc)[sl][sel]), kn_rows)
+    assert np.array_equal(bits(flat(vc)[sl][sel]), vn_rows)
+    keep = torch.ones(w.num_blocks * 16, dtype=torch.bool, device=cuda_device)
+    keep[sl] = False
+    assert torch.equal(flat(kc)[keep].view(torch.int16), flat(k_orig)[keep].view(torch.int16))
+    assert torch.equal(flat(vc)[keep].view(torch.int16), flat(v_orig)[keep].view(torch.int16))
+
+    # attention
+    got = bits(out)[seq_ids]
+    err, rel = assert_attention_close(got, want, dtype_code(w), name)
+    print(f"{name}: {len(seq_ids)} seqs checked, max abs err {err:.2e}, norm-rel {rel:.2e}")
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen3_0p6b"])
+def test_separate_entry_points(name, cuda_device):
+    """reshape_and_cache + paged_attention_decode called one by one."""
+    w = wl.WORKLOADS[name]
+    inp = wl.make_inputs(w, device=cuda_device, num_layers=1)
+    want, _, _ = compact_oracle_step(inp, np.arange(w.num_seqs))
+    kc, vc = inp["k_cache"][0], inp["v_cache"][0]
+    slots = pkv.paged_kv_slot_mapping(inp["block_tables"], inp["context_lens"], w.num_blocks)
+    pkv.reshape_and_cache(inp["k_new"][0], inp["v_new"][0], kc, vc, slots)
+    max_len = int(inp["context_lens_host"].max())
+    out = torch.empty_like(inp["q"])
+    ws = pkv.new_workspace(w.num_seqs, w.num_q_heads, w.head_dim, max_len, cuda_device)
+    pkv.paged_attention_decode(inp["q"], kc, vc, inp["block_tables"], inp["context_lens"],
+                               max_len, w.scale, out, ws)
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_status() == 0
+    assert_attention_close(bits(out), want, dtype_code(w), name)
+
+
+@pytest.mark.parametrize("name", ["tiny", "qwen3_0p6b", "prefix_shared"])
+def test_partition_length_invariance(name, cuda_device):
+    """Partitions of 1, 2, 4, 32 blocks and one partition per sequence all match the
+    oracle, and each other within fp32 rounding."""
+    w = wl.WORKLOADS[name]
+    if name == "prefix_shared":
+        w = w.with_(num_seqs=24)
+    inp = wl.make_inputs(w, device=cuda_device, num_layers=1)
+    want, _, _ = compact_oracle_step(inp, np.arange(w.num_seqs))
+    kc, vc = inp["k_cache"][0], inp["v_cache"][0]
+    slots = pkv.paged_kv_slot_mapping(inp["block_tables"], inp["context_lens"], w.num_blocks)
+    pkv.reshape_and_cache(inp["k_new"][0], inp["v_new"][0], kc, vc, slots)
+    max_len = int(inp["context_lens_host"].max())
+    ws = pkv.new_workspace(w.num_seqs, w.num_q_heads, w.head_dim, max_len, cuda_device)
+    outs = {}
+    min_pb = pkv.paged_attention_min_partition_blocks(max_len)
+    for pb in sorted({max(min_pb, x) for x in (1, 2, 4, 32, w.max_blocks_per_seq)}):
+        out = torch.empty_like(inp["q"])
+        pkv.paged_attention_decode_partitioned(inp["q"], kc, vc, inp["block_tables"],
+                                               inp["context_lens"], max_len, w.scale, out, ws,
+                                               partition_blocks=pb)
+        torch.cuda.synchronize()
+        outs[pb] = out.float()
+        assert_attention_close(bits(out), want, dtype_code(w), f"{name} pb={pb}")
+    ref = outs[w.max_blocks_per_seq]
+    for pb, o in outs.items():
+        assert torch.allclose(o, ref, atol=2e-2, rtol=2e-2), pb
+    assert pkv.pkv_device_status() == 0
+
+
+def _custom(dev, dtype, lens, Hq, Hkv, D, NB, seed, poison=True):
+    w = wl.Workload("custom", seed, len(lens), Hq, Hkv, D, NB, dtype,
+                    "fixed:" + ",".join(str(n) for n in lens),
+                    max(1, (max(lens) + 15) // 16))
+    return w, wl.make_inputs(w, device=dev, num_layers=1, poison=poison)
+
+
+@pytest.mark.parametrize("dtype,Hq,Hkv,D", [("bf16", 8, 8, 128), ("f16", 8, 1, 64),
+                                             ("bf16", 16, 4, 64), ("f16", 6, 3, 128),
+                                             ("bf16", 14, 2, 128)])
+def test_group_sizes_and_ragged_lengths(dtype, Hq, Hkv, D, cuda_device):
+    """MHA (g=1), g=3, 4, 7, 8, D 64/128, lengths on and around block boundaries."""
+    lens = [1, 2, 15, 16, 17, 31, 32, 33, 255, 256, 257, 1000]
+    w, inp = _custom(cuda_device, dtype, lens, Hq, Hkv, D, 256, seed=77)
+    want, _, _ = compact_oracle_step(inp, np.arange(len(lens)))
+    out, _ = _run_step(inp, cuda_device)
+    assert pkv.pkv_device_status() == 0
+    assert_attention_close(bits(out), want, dtype_code(w), f"g={Hq // Hkv} D={D}")
+
+
+def test_length_one_returns_v_exactly(cuda_device):
+    w, inp = _custom(cuda_device, "bf16", [1, 1, 1], 8, 2, 128, 8, seed=5)
+    out, _ = _run_step(inp, cuda_device)
+    # out[s, i] == the new token's V row of KV head i // 4, bit for bit
+    want = inp["v_new"][0].repeat_interleave(4, dim=1)
+    assert torch.equal(out.view(torch.int16), want.view(torch.int16))
+
+
+def test_empty_context_gives_zeros(cuda_device):
+    w, inp = _custom(cuda_device, "f16", [5, 40, 7], 8, 4, 128, 16, seed=6)
+    inp["context_lens"][1] = 0           # a padding row
+    lens = inp["context_lens_host"].copy()
+    lens[1] = 0
+    inp["context_lens_host"] = lens
+    keep = np.array([0, 2])
+    want, _, _ = compact_oracle_step(inp, keep)
+    out, slots = _run_step(inp, cuda_device)
+    assert pkv.pkv_device_status() == 0
+    assert int(slots[1]) == -1
+    assert torch.count_nonzero(out[1]) == 0
+    assert_attention_close(bits(out)[keep], want, oracle.F16, "non-empty rows")
+
+
+def test_bad_device_values_are_flagged_not_read(cuda_device):
+    """A table entry outside the pool and a length beyond the bound are skipped and
+    flagged in the device status word; the other rows stay correct."""
+    w, inp = _custom(cuda_device, "bf16", [40, 40, 40], 8, 4, 128, 16, seed=8)
+    want, _, _ = compact_oracle_step(inp, np.array([0]))
+    q, kc, vc = inp["q"], inp["k_cache"][0], inp["v_cache"][0]
+    slots = pkv.paged_kv_slot_mapping(inp["block_tables"], inp["context_lens"], w.num_blocks)
+    pkv.reshape_and_cache(inp["k_new"][0], inp["v_new"][0], kc, vc, slots)
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_status() == 0
+    inp["block_tables"][1, 1] = 1 << 30          # out of range
+    inp["context_lens"][2] = 999                 # beyond max_context_len and the table
+    max_len = 40
+    out = torch.empty_like(q)
+    ws = pkv.new_workspace(3, 8, 128, max_len, cuda_device)
+    pkv.paged_attention_decode(q, kc, vc, inp["block_tables"], inp["context_lens"], max_len,
+                               w.scale, out, ws)
+    torch.cuda.synchronize()
+    flags = pkv.pkv_device_status(reset=True)
+    assert flags & pkv.DEV_BAD_BLOCK_ID and flags & pkv.DEV_BAD_LENGTH
+    assert torch.isfinite(out.float()).all()
+    assert torch.count_nonzero(out[2]) == 0      # an invalid length gives a zero row
+    assert_attention_close(bits(out)[:1], want, oracle.BF16, "row without bad values")
+    assert pkv.pkv_device_status() == 0
+
+
+def test_reshape_and_cache_padding_and_bad_slots(cuda_device):
+    NB, Hkv, D = 12, 8, 128
+    g = torch.Generator(device=cuda_device).manual_seed(3)
+    kc = torch.randn(NB, 16, Hkv, D, generator=g, device=cuda_device).to(torch.float16)
+    vc = torch.randn(NB, 16, Hkv, D, generator=g, device=cuda_device).to(torch.float16)
+    kn = torch.randn(5, Hkv, D, generator=g, device=cuda_device).to(torch.float16)
+    vn = torch.randn(5, Hkv, D, generator=g, device=cuda_device).to(torch.float16)
+    slots = torch.tensor([3, -1, 191, 17, NB * 16 + 5], dtype=torch.int64, device=cuda_device)
+    hk, hv = bits(kc), bits(vc)
+    wk, wv = oracle.reshape_and_cache(bits(kn)[[0, 2, 3]], bits(vn)[[0, 2, 3]], hk, hv,
+                                      np.array([3, 191, 17]))
+    pkv.reshape_and_cache(kn, vn, kc, vc, slots)
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_status(reset=True) == pkv.DEV_BAD_SLOT
+    assert np.array_equal(bits(kc), wk) and np.array_equal(bits(vc), wv)
+
+
+def test_maximum_batch_and_maximum_length(cuda_device):
+    """8192 sequences (lengths and offsets fill 64 KB of shared memory) and two
+    32768-token contexts (64 partitions of the minimum length)."""
+    rng = np.random.default_rng(9)
+    lens = [int(x) for x in rng.integers(1, 40, size=8192)]
+    w, inp = _custom(cuda_device, "f16", lens, 4, 2, 64, 8192 * 3 + 8, seed=10)
+    ids = sample_seqs(np.array(lens), 64, seed=1)
+    want, _, _ = compact_oracle_step(inp, ids)
+    out, _ = _run_step(inp, cuda_device)
+    assert pkv.pkv_device_status() == 0
+    assert_attention_close(bits(out)[ids], want, oracle.F16, "8192 seqs")
+
+    w, inp = _custom(cuda_device, "bf16", [32768, 32768], 32, 8, 128, 4100, seed=11)
+    want, _, _ = compact_oracle_step(inp, np.arange(2))
+    out, _ = _run_step(inp, cuda_device)
+    assert pkv.pkv_device_status() == 0
+    assert_attention_close(bits(out), want, oracle.BF16, "32768 tokens")
+
+
+def test_host_buffer_step(cuda_device):
+    """paged_kv_decode_step_host: inputs and output in pinned host memory."""
+    w = wl.WORKLOADS["tiny"]
+    inp = wl.make_inputs(w, device=cuda_device, num_layers=1)
+    want, _, _ = compact_oracle_step(inp, np.arange(w.num_seqs))
+    pin = lambda t: t.cpu().pin_memory()
+    qh, knh, vnh = pin(inp["q"]), pin(inp["k_new"][0]), pin(inp["v_new"][0])
+    bth, clh = pin(inp["block_tables"]), pin(inp["context_lens"])
+    outh = torch.empty_like(qh).pin_memory()
+    max_len = int(inp["context_lens_host"].max())
+    staging = torch.empty(pkv.paged_kv_decode_step_staging_bytes(w.num_seqs, w.num_q_heads,
+                                                                 w.num_kv_heads, w.head_dim,
+                                                                 w.max_blocks_per_seq),
+                          dtype=torch.uint8, device=cuda_device)
+    ws = pkv.new_workspace(w.num_seqs, w.num_q_heads, w.head_dim, max_len, cuda_device)
+    pkv.paged_kv_decode_step_host(qh, knh, vnh, bth, clh, outh, staging, inp["k_cache"][0],
+                                  inp["v_cache"][0], max_len, w.scale, ws)
+    torch.cuda.current_stream().synchronize()
+    assert pkv.pkv_device_status() == 0
+    assert_attention_close(bits(outh), want, oracle.F16, "host step")
+
+
+def test_layer_views_of_a_layer_major_pool(cuda_device):
+    """Each layer of a layer-major pool is addressed by its own base pointer (a view)."""
+    w = wl.WORKLOADS["tiny"]
+    inp = wl.make_inputs(w, device=cuda_device, num_layers=3)
+    max_len = int(inp["context_lens_host"].max())
+    ws = pkv.new_workspace(w.num_seqs, w.num_q_heads, w.head_dim, max_len, cuda_device)
+    for layer in (2, 0, 1):
+        want, _, _ = compact_oracle_step(inp, np.arange(w.num_seqs), layer=layer)
+        out = torch.empty_like(inp["q"])
+        pkv.paged_kv_decode_step(inp["q"], inp["k_new"][layer], inp["v_new"][layer],
+                                 inp["k_cache"][layer], inp["v_cache"][layer],
+                                 inp["block_tables"], inp["context_lens"], max_len, w.scale,
+                                 out, ws)
+        torch.cuda.synchronize()
+        assert_attention_close(bits(out), want, oracle.F16, f"layer {layer}")
+    assert pkv.pkv_device_status() == 0
