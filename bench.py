@@ -44,12 +44,14 @@ KERNEL_SOURCES = ["paged_kv_cache_211_gb300/csrc/pkv_decode.cu",
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama7b_long")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer loop")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pool-blocks", type=int, default=0,
+                    help="shrink the physical pool (for small profiler captures)")
     return ap.parse_args()
 
 
@@ -237,11 +239,13 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x: float, world: int, dev) -> float:
+def max_over_ranks(x: float, world: int, dev=None) -> float:
+    """The slowest rank's time (every rank gets it)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    on = dev if (dev is not None and dist.get_backend() == "nccl") else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=on)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -270,6 +274,8 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     pkv.lib()  # fail loudly if the library is missing
     w = wl.WORKLOADS[args.workload]
+    if args.pool_blocks:
+        w = w.with_(num_blocks=args.pool_blocks)
     inp = wl.make_inputs(w, device=dev, num_layers=1)
     lens = inp["context_lens_host"]
     B, Hq, Hkv, D = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim
@@ -281,55 +287,75 @@ def run_ours(args):
     ws = pkv.new_workspace(B, Hq, D, max_len, dev)
     step_bytes = wl.algorithmic_bytes(w, lens, with_write=True)
     blocks = int(((lens.astype(np.int64) + 15) // 16).sum())
-    part_bytes = wl.kv_bytes(w, lens) + B * Hq * D * 2 + blocks * 4 + B * 4
+    # the fused write + partition kernel: K/V of every valid token (the new row
+    # read from k_new/v_new instead of the cache), q, table entries, lengths,
+    # and the new rows written
+    part_bytes = (wl.kv_bytes(w, lens) + B * Hq * D * 2 + blocks * 4 + B * 4
+                  + 2 * B * Hkv * D * 2)
     need_flush = step_bytes <= 4 * L2_BYTES
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev) if need_flush else None
     stream = torch.cuda.current_stream()
     min_pb = pkv.paged_attention_min_partition_blocks(max_len)
     merges = int((max_len + 15) // 16 > max(min_pb, 8))
 
-    def step(evs=None):
-        if evs:
-            evs[0].record(stream)
-        pkv.paged_kv_write_new_tokens(kn, vn, kc, vc, bt, cl, stream=stream)
-        if evs:
-            evs[1].record(stream)
-        pkv.paged_attention_partition_pass(q, kc, vc, bt, cl, max_len, w.scale, out, ws,
-                                           stream=stream)
-        if evs:
-            evs[2].record(stream)
+    def step():
+        # the public one-call step: fused write + partition pass, then the merge
+        pkv.paged_kv_decode_step(q, kn, vn, kc, vc, bt, cl, max_len, w.scale, out, ws,
+                                 stream=stream)
+
+    def step_split(evs):
+        # the same two kernels through their own entry points, with events between
+        evs[0].record(stream)
+        pkv.paged_kv_decode_step_partition_pass(q, kn, vn, kc, vc, bt, cl, max_len, w.scale,
+                                                out, ws, stream=stream)
+        evs[1].record(stream)
         pkv.paged_attention_merge_pass(q, kc, vc, bt, cl, max_len, w.scale, out, ws,
                                        stream=stream)
-        if evs:
-            evs[3].record(stream)
+        evs[2].record(stream)
 
+    K = args.steps
     for _ in range(max(args.warmup, 3)):
         if flush is not None:
             flush.zero_()
         step()
     torch.cuda.synchronize()
-    K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+
+    # timed region A: the step as a user calls it -> value, ms_per_step
+    step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     barrier(world)
     torch.cuda.synchronize()
     clocks = ClockSampler(dev.index) if rank == 0 else None
     for i in range(K):
         if flush is not None:
             flush.zero_()
-        step(evs[i])
+        if need_flush or i == 0:
+            step_ev[i][0].record(stream)
+        step()
+        if need_flush or i == K - 1:
+            step_ev[i][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop() if clocks else None
+    if need_flush:
+        ms = sum(e[0].elapsed_time(e[1]) for e in step_ev) / K
+    else:
+        ms = step_ev[0][0].elapsed_time(step_ev[-1][1]) / K
+    ms = max_over_ranks(ms, world, dev)
+
+    # timed region B: per-kernel durations (roofline of the dominant kernel)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(K):
+        if flush is not None:
+            flush.zero_()
+        step_split(evs[i])
+    torch.cuda.synchronize()
+    barrier(world)
     if pkv.pkv_device_status() != 0:
         raise SystemExit("device status flags set during the benchmark")
-    t_write = sum(e[0].elapsed_time(e[1]) for e in evs) / K
-    t_part = sum(e[1].elapsed_time(e[2]) for e in evs) / K
-    t_merge = sum(e[2].elapsed_time(e[3]) for e in evs) / K
-    if need_flush:
-        ms = sum(e[0].elapsed_time(e[3]) for e in evs) / K
-    else:
-        ms = evs[0][0].elapsed_time(evs[-1][3]) / K
-    ms = max_over_ranks(ms, world, dev)
+    t_part = sum(e[0].elapsed_time(e[1]) for e in evs) / K
+    t_merge = sum(e[1].elapsed_time(e[2]) for e in evs) / K
 
     # end to end through the host-buffer entry point: pinned inputs in, output out
     e2e = None
@@ -393,8 +419,8 @@ def run_ours(args):
         "pct_of_nominal_8tbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_hbm": round(100 * value / world / peak, 2),
         "algorithmic_bytes_per_step": int(step_bytes),
-        "kernels_ms": {"write_new_tokens": round(t_write, 5),
-                       "decode_partition": round(t_part, 5), "decode_merge": round(t_merge, 5)},
+        "kernels_ms": {"decode_partition_fused_write": round(t_part, 5),
+                       "decode_merge": round(t_merge, 5)},
         "roofline": {"bound": "hbm", "kernel": "decode_partition_kernel",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} hbm_gbs",
@@ -402,7 +428,7 @@ def run_ours(args):
                      "traffic": traffic},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": K * (2 + merges),
+        "gpu_launches": K * (1 + merges),
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

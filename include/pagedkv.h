@@ -224,7 +224,11 @@ pkv_status paged_kv_write_new_tokens(const void* k_new, const void* v_new, void*
                                      pkv_stream_t stream);
 
 /* One decode step of one layer ([P3] §2 and item 1: write, then attend):
- * paged_kv_write_new_tokens followed by paged_attention_decode.
+ * the result of paged_kv_write_new_tokens followed by paged_attention_decode.
+ * The write is fused into the partition pass: the warp that reads a
+ * sequence's last block takes the new token's row from k_new / v_new and
+ * stores it into its slot, so one kernel writes and attends, and the merge
+ * pass follows. Within the call, nothing reads the new rows back from the cache.
  * slot_mapping_out may be NULL; if not, it receives the slots ([num_seqs]
  * int64, device). */
 pkv_status paged_kv_decode_step(const void* q, const void* k_new, const void* v_new,
@@ -234,6 +238,16 @@ pkv_status paged_kv_decode_step(const void* q, const void* k_new, const void* v_
                                 int num_kv_heads, int head_dim, int num_blocks, float scale,
                                 void* out, int64_t* slot_mapping_out, void* workspace,
                                 size_t workspace_bytes, pkv_dtype dtype, pkv_stream_t stream);
+
+/* The first of the two kernels of paged_kv_decode_step: the fused write
+ * and partition pass.  paged_attention_merge_pass with partition_blocks = 0
+ * and the same arguments completes the step. */
+pkv_status paged_kv_decode_step_partition_pass(
+    const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+    int max_context_len, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int num_blocks, float scale, void* out, int64_t* slot_mapping_out, void* workspace,
+    size_t workspace_bytes, pkv_dtype dtype, pkv_stream_t stream);
 
 /* Device staging bytes paged_kv_decode_step_host needs: device copies of q,
  * k_new, v_new, block_tables, context_lens and out, each 256-byte aligned. */

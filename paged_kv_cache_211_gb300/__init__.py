@@ -21,6 +21,7 @@ __all__ = [
     "paged_attention_min_partition_blocks", "paged_attention_decode",
     "paged_attention_decode_partitioned", "paged_attention_partition_pass",
     "paged_attention_merge_pass", "paged_kv_write_new_tokens", "paged_kv_decode_step",
+    "paged_kv_decode_step_partition_pass",
     "paged_kv_decode_step_staging_bytes", "paged_kv_decode_step_host", "pkv_device_status",
     "BlockAllocator", "new_workspace",
 ]
@@ -72,6 +73,8 @@ _SIGS = {
                                     _vp, _vp, _sz, _i, _i, _vp], _i),
     "paged_kv_write_new_tokens": ([_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _vp, _i,
                                    _vp], _i),
+    "paged_kv_decode_step_partition_pass": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i,
+                                             _i, _i, _i, _f, _vp, _vp, _vp, _sz, _i, _vp], _i),
     "paged_kv_decode_step_staging_bytes": ([_i, _i, _i, _i, _i], _sz),
     "paged_kv_decode_step_host": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp, _i, _i,
                                    _i, _i, _i, _i, _i, _f, _vp, _sz, _i, _vp], _i),
@@ -260,15 +263,13 @@ def paged_kv_write_new_tokens(k_new, v_new, k_cache, v_cache, block_tables, cont
         _opt(slot_mapping_out, "slot_mapping_out"), _dtype_code(k_new), _stream(stream)))
 
 
-def paged_kv_decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
-                         max_context_len, scale, out, workspace, slot_mapping_out=None,
-                         stream=None):
-    """Write each sequence's new K/V at position len-1, then decode attention."""
+def _decode_step(fn_name, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
+                 max_context_len, scale, out, workspace, slot_mapping_out, stream):
     B, Hq, Hkv, D, NB = _check_decode_shapes(q, k_cache, v_cache, block_tables, context_lens,
                                              out)
     if tuple(k_new.shape) != (B, Hkv, D) or v_new.shape != k_new.shape:
         raise ValueError("k_new/v_new must be [num_seqs, num_kv_heads, head_dim]")
-    _check("paged_kv_decode_step", lib().paged_kv_decode_step(
+    _check(fn_name, getattr(lib(), fn_name)(
         _dev(q, "q"), _dev(k_new, "k_new"), _dev(v_new, "v_new"), _dev(k_cache, "k_cache"),
         _dev(v_cache, "v_cache"), _dev(block_tables, "block_tables"), block_tables.shape[1],
         _dev(context_lens, "context_lens"), int(max_context_len), B, Hq, Hkv, D, NB,
@@ -276,6 +277,24 @@ def paged_kv_decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, contex
         _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _dtype_code(q), _stream(stream)))
     return out
+
+
+def paged_kv_decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
+                         max_context_len, scale, out, workspace, slot_mapping_out=None,
+                         stream=None):
+    """Write each sequence's new K/V at position len-1, then decode attention."""
+    return _decode_step("paged_kv_decode_step", q, k_new, v_new, k_cache, v_cache, block_tables,
+                        context_lens, max_context_len, scale, out, workspace, slot_mapping_out,
+                        stream)
+
+
+def paged_kv_decode_step_partition_pass(q, k_new, v_new, k_cache, v_cache, block_tables,
+                                        context_lens, max_context_len, scale, out, workspace,
+                                        slot_mapping_out=None, stream=None):
+    """The first kernel of paged_kv_decode_step (fused write + partition pass)."""
+    return _decode_step("paged_kv_decode_step_partition_pass", q, k_new, v_new, k_cache,
+                        v_cache, block_tables, context_lens, max_context_len, scale, out,
+                        workspace, slot_mapping_out, stream)
 
 
 def paged_kv_decode_step_staging_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,

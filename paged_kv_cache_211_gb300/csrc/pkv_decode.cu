@@ -97,6 +97,12 @@ struct DecodeParams {
     float* ws_l;
     float* ws_o;
     unsigned int* status;
+    // optional fused KV write of the step's token (all null for plain decode)
+    const void* k_new;          // [num_seqs][num_kv_heads][D]
+    const void* v_new;
+    void* k_cache_w;            // the same pools, written through these
+    void* v_cache_w;
+    int64_t* slot_out;          // [num_seqs] or null
     int num_seqs, num_q_heads, num_kv_heads, group;
     int max_blocks_per_seq, num_blocks, len_bound;
     int partition_blocks;      // > 0: fixed partition length (blocks)
@@ -152,15 +158,23 @@ struct BlockFrag {
     uint4 k[2][KC];
     uint4 v[VC][4];
     bool bad;
+    int rnew;     // row of this step's new token in this block, or -1
+    size_t blk;   // first row of the physical block
 };
 
+// Loads one block's K/V fragments.  With rnew >= 0 the block holds this
+// step's token at row rnew, which is not in the cache yet: that row is taken
+// from knew / vnew ([D] each, this KV head) instead.
 template <typename T, int D>
 __device__ __forceinline__ void fetch_block(BlockFrag<D>& f, const T* kbase, const T* vbase,
-                                            int id, size_t row_stride, int gid, int tig) {
+                                            int id, size_t row_stride, int gid, int tig,
+                                            int rnew, const T* knew, const T* vnew) {
     f.bad = id < 0;
+    f.rnew = f.bad ? -1 : rnew;
     const size_t blk = (size_t)(f.bad ? 0 : id) * PKV_BLOCK_SIZE;
-    const T* kr0 = kbase + (blk + gid) * row_stride;
-    const T* kr1 = kr0 + 8 * row_stride;
+    f.blk = blk;
+    const T* kr0 = gid == f.rnew ? knew : kbase + (blk + gid) * row_stride;
+    const T* kr1 = gid + 8 == f.rnew ? knew : kbase + (blk + gid + 8) * row_stride;
 #pragma unroll
     for (int j = 0; j < BlockFrag<D>::KC; ++j) {
         f.k[0][j] = ld_stream(kr0 + (4 * j + tig) * 8);
@@ -171,7 +185,35 @@ __device__ __forceinline__ void fetch_block(BlockFrag<D>& f, const T* kbase, con
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
             const int tok = 2 * tig + (t & 1) + (t >> 1) * 8;
-            f.v[c][t] = ld_stream(vbase + (blk + tok) * row_stride + (gid + 8 * c) * 8);
+            const T* src = tok == f.rnew ? vnew : vbase + (blk + tok) * row_stride;
+            f.v[c][t] = ld_stream(src + (gid + 8 * c) * 8);
+        }
+    }
+}
+
+// The KV write fused into the decode step: the lanes that hold the new row
+// (taken from k_new / v_new by fetch_block) store it into its cache slot.
+template <typename T, int D>
+__device__ __forceinline__ void store_new_row(const BlockFrag<D>& f, T* kbase_w, T* vbase_w,
+                                              size_t row_stride, int gid, int tig) {
+    const int r = f.rnew;
+#pragma unroll
+    for (int j = 0; j < BlockFrag<D>::KC; ++j) {
+        if (gid == r)
+            *reinterpret_cast<uint4*>(kbase_w + (f.blk + r) * row_stride + (4 * j + tig) * 8) =
+                f.k[0][j];
+        if (gid + 8 == r)
+            *reinterpret_cast<uint4*>(kbase_w + (f.blk + r) * row_stride + (4 * j + tig) * 8) =
+                f.k[1][j];
+    }
+#pragma unroll
+    for (int c = 0; c < BlockFrag<D>::VC; ++c) {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int tok = 2 * tig + (t & 1) + (t >> 1) * 8;
+            if (tok == r)
+                *reinterpret_cast<uint4*>(vbase_w + (f.blk + r) * row_stride +
+                                          (gid + 8 * c) * 8) = f.v[c][t];
         }
     }
 }
@@ -277,9 +319,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
             n = 0;  // the row is written as zeros
         }
         sm_len[s] = n;
+        if (n == 0 && p.slot_out && blockIdx.x == 0) p.slot_out[s] = -1;  // nothing written
         my_blocks += (n + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
     }
     const int total_blocks = cta_sum(my_blocks, red);
+    // the merge kernel may be launched now; it waits for this grid's results
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
     // (2) partition length: fixed, or enough items for every CTA
     int PB = p.partition_blocks;
@@ -350,6 +395,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
 
         const T* kbase = kc + (size_t)h * D;
         const T* vbase = vc + (size_t)h * D;
+        // this step's token (position n-1) lives in the sequence's last block
+        const bool writes = p.k_new != nullptr && n > 0;
+        const int last_blk = writes ? nblk - 1 : -1;
+        const int rnew = (n - 1) & (PKV_BLOCK_SIZE - 1);
+        const T* knew = writes ? static_cast<const T*>(p.k_new) + ((size_t)s * Hkv + h) * D : kbase;
+        const T* vnew = writes ? static_cast<const T*>(p.v_new) + ((size_t)s * Hkv + h) * D : vbase;
         const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
         // physical ids of this warp's blocks, 32 at a time (lane l: block j0 + l*kWarps)
         auto load_ids = [&](int j0) {
@@ -368,18 +419,27 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
         int k = 0;  // index of block j among this warp's blocks
         int ids = 0;
         BlockFrag<D> fa, fb;
+        T* kbase_w = static_cast<T*>(p.k_cache_w) + (size_t)h * D;
+        T* vbase_w = static_cast<T*>(p.v_cache_w) + (size_t)h * D;
+        // the step's token: write it (lanes holding it) and record its slot (head 0)
+        auto finish_new_row = [&](const BlockFrag<D>& f) {
+            if (f.rnew >= 0) store_new_row<T, D>(f, kbase_w, vbase_w, row_stride, gid, tig);
+            if (p.slot_out && h == 0 && lane == 0)
+                p.slot_out[s] = f.bad ? -1 : (int64_t)f.blk + rnew;
+        };
         if (j < blk_hi) {
             ids = load_ids(j);
             fetch_block<T, D>(fa, kbase, vbase, __shfl_sync(0xffffffffu, ids, 0), row_stride,
-                              gid, tig);
+                              gid, tig, j == last_blk ? rnew : -1, knew, vnew);
         }
         while (j < blk_hi) {
             int jn = j + kWarps;
             if (jn < blk_hi) {
                 if (((k + 1) & 31) == 0) ids = load_ids(jn);
                 fetch_block<T, D>(fb, kbase, vbase, __shfl_sync(0xffffffffu, ids, (k + 1) & 31),
-                                  row_stride, gid, tig);
+                                  row_stride, gid, tig, jn == last_blk ? rnew : -1, knew, vnew);
             }
+            if (j == last_blk) finish_new_row(fa);
             compute_block<T, D>(st, fa, qf, fa.bad ? 0 : min(PKV_BLOCK_SIZE, n - j * 16),
                                 p.scale_log2, gid, tig);
             j = jn;
@@ -389,8 +449,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
             if (jn < blk_hi) {
                 if (((k + 1) & 31) == 0) ids = load_ids(jn);
                 fetch_block<T, D>(fa, kbase, vbase, __shfl_sync(0xffffffffu, ids, (k + 1) & 31),
-                                  row_stride, gid, tig);
+                                  row_stride, gid, tig, jn == last_blk ? rnew : -1, knew, vnew);
             }
+            if (j == last_blk) finish_new_row(fb);
             compute_block<T, D>(st, fb, qf, fb.bad ? 0 : min(PKV_BLOCK_SIZE, n - j * 16),
                                 p.scale_log2, gid, tig);
             j = jn;
@@ -487,6 +548,8 @@ struct MergeParams {
 template <typename T, int D>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const MergeParams p) {
     constexpr int PER = D / 32;
+    // launched early (programmatic dependent launch): wait for the partition pass
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int wg = blockIdx.x * 4 + (threadIdx.x >> 5);
     if (wg >= p.num_seqs * p.num_q_heads) return;
@@ -563,9 +626,21 @@ pkv_status launch_decode(const DecodeParams& prm_in, const MergeParams& mp, int 
         if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
     }
     if ((passes & kPassMerge) && need_merge) {
+        // programmatic dependent launch: the merge grid is scheduled while the
+        // partition grid drains and waits (griddepcontrol.wait) for its results
         const int warps = prm.num_seqs * prm.num_q_heads;
-        decode_merge_kernel<T, D><<<(warps + 3) / 4, 128, 0, stream>>>(mp);
-        if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)((warps + 3) / 4));
+        cfg.blockDim = dim3(128);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, decode_merge_kernel<T, D>, mp) != cudaSuccess)
+            return PKV_ERR_CUDA;
     }
     return PKV_OK;
 }
@@ -576,7 +651,8 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
                        int num_q_heads, int num_kv_heads, int head_dim, int num_blocks,
                        float scale, void* out, void* workspace, size_t workspace_bytes,
                        int partition_blocks, pkv_dtype dtype, int passes,
-                       cudaStream_t stream) {
+                       cudaStream_t stream, const void* k_new = nullptr,
+                       const void* v_new = nullptr, int64_t* slot_out = nullptr) {
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
         max_blocks_per_seq <= 0 || num_blocks <= 0 || max_context_len < 0 ||
         partition_blocks < 0)
@@ -621,6 +697,11 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
     prm.ws_l = reinterpret_cast<float*>(wsb + ws.l);
     prm.ws_o = reinterpret_cast<float*>(wsb + ws.o);
     prm.status = status;
+    prm.k_new = k_new;
+    prm.v_new = v_new;
+    prm.k_cache_w = const_cast<void*>(k_cache);
+    prm.v_cache_w = const_cast<void*>(v_cache);
+    prm.slot_out = k_new ? slot_out : nullptr;
     prm.num_seqs = num_seqs;
     prm.num_q_heads = num_q_heads;
     prm.num_kv_heads = num_kv_heads;
@@ -743,6 +824,34 @@ pkv_status paged_kv_write_new_tokens(const void* k_new, const void* v_new, void*
                                          reinterpret_cast<cudaStream_t>(stream));
 }
 
+}  // extern "C"
+
+namespace pkv {
+namespace {
+
+pkv_status decode_step_impl(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                            void* v_cache, const int32_t* block_tables, int max_blocks_per_seq,
+                            const int32_t* context_lens, int max_context_len, int num_seqs,
+                            int num_q_heads, int num_kv_heads, int head_dim, int num_blocks,
+                            float scale, void* out, int64_t* slot_mapping_out, void* workspace,
+                            size_t workspace_bytes, pkv_dtype dtype, int passes,
+                            cudaStream_t stream) {
+    if (num_seqs < 0 || num_kv_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0 ||
+        num_blocks <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PKV_OK;
+    if (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return PKV_ERR_INVALID_ARG;
+    return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                       max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                       num_blocks, scale, out, workspace, workspace_bytes, 0, dtype, passes,
+                       stream, k_new, v_new, slot_mapping_out);
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" {
+
 pkv_status paged_kv_decode_step(const void* q, const void* k_new, const void* v_new,
                                 void* k_cache, void* v_cache, const int32_t* block_tables,
                                 int max_blocks_per_seq, const int32_t* context_lens,
@@ -750,37 +859,25 @@ pkv_status paged_kv_decode_step(const void* q, const void* k_new, const void* v_
                                 int num_kv_heads, int head_dim, int num_blocks, float scale,
                                 void* out, int64_t* slot_mapping_out, void* workspace,
                                 size_t workspace_bytes, pkv_dtype dtype, pkv_stream_t stream) {
-    if (num_seqs < 0 || num_kv_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0 ||
-        num_blocks <= 0)
-        return PKV_ERR_INVALID_ARG;
-    if (num_seqs == 0) return PKV_OK;
-    if (!k_new || !v_new || !pkv::aligned16(k_new) || !pkv::aligned16(v_new))
-        return PKV_ERR_INVALID_ARG;
-    // validate the attention arguments before anything is enqueued
-    if (num_q_heads <= 0 || num_q_heads % num_kv_heads) return PKV_ERR_INVALID_ARG;
-    if (num_q_heads / num_kv_heads > pkv::kMaxGroup || (head_dim != 64 && head_dim != 128) ||
-        num_seqs > pkv::kMaxSeqs)
-        return PKV_ERR_UNSUPPORTED;
-    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
-        return PKV_ERR_INVALID_ARG;
-    if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
-    if (!pkv::aligned16(q) || !pkv::aligned16(k_cache) || !pkv::aligned16(v_cache) ||
-        !pkv::aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-        return PKV_ERR_INVALID_ARG;
-    if (!workspace ||
-        workspace_bytes < paged_attention_workspace_bytes(num_seqs, num_q_heads, head_dim,
-                                                          max_context_len))
-        return PKV_ERR_WORKSPACE;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    pkv_status rc = pkv::launch_decode_step_write(k_new, v_new, k_cache, v_cache, block_tables,
-                                                  max_blocks_per_seq, context_lens, num_seqs,
-                                                  num_blocks, num_kv_heads, head_dim,
-                                                  slot_mapping_out, st);
-    if (rc != PKV_OK) return rc;
-    return pkv::decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-                            max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
-                            num_blocks, scale, out, workspace, workspace_bytes, 0, dtype,
-                            pkv::kPassPartition | pkv::kPassMerge, st);
+    return pkv::decode_step_impl(q, k_new, v_new, k_cache, v_cache, block_tables,
+                                 max_blocks_per_seq, context_lens, max_context_len, num_seqs,
+                                 num_q_heads, num_kv_heads, head_dim, num_blocks, scale, out,
+                                 slot_mapping_out, workspace, workspace_bytes, dtype,
+                                 pkv::kPassPartition | pkv::kPassMerge,
+                                 reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status paged_kv_decode_step_partition_pass(
+    const void* q, const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+    const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+    int max_context_len, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int num_blocks, float scale, void* out, int64_t* slot_mapping_out, void* workspace,
+    size_t workspace_bytes, pkv_dtype dtype, pkv_stream_t stream) {
+    return pkv::decode_step_impl(q, k_new, v_new, k_cache, v_cache, block_tables,
+                                 max_blocks_per_seq, context_lens, max_context_len, num_seqs,
+                                 num_q_heads, num_kv_heads, head_dim, num_blocks, scale, out,
+                                 slot_mapping_out, workspace, workspace_bytes, dtype,
+                                 pkv::kPassPartition, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"
