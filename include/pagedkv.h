@@ -273,6 +273,38 @@ pkv_status paged_kv_decode_step_host(const void* q_host, const void* k_new_host,
                                      size_t workspace_bytes, pkv_dtype dtype,
                                      pkv_stream_t stream);
 
+/* Size of the static scratch used by paged_attention_decode_noalloc (32 MiB
+ * per GPU that loads the library, held until the process exits). */
+#define PKV_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/* paged_attention_decode for callers that cannot allocate device memory (a
+ * plug-in inside a framework that owns all device memory; a runtime whose
+ * memory plan is fixed at start-up and that must not call cudaMalloc, which
+ * synchronises the device and can fail mid-request).  There is no workspace
+ * argument: the split-context partials go to a static device array of
+ * PKV_NOALLOC_SCRATCH_BYTES inside the library.  The caller still passes all
+ * inputs and the output, as for paged_attention_decode.
+ *  - No cudaMalloc, cudaFree or other allocating call is made.
+ *  - The first call on a device performs a one-time set-up there (it looks up
+ *    the array's device address); make that first call before any stream
+ *    capture.
+ *  - A problem whose paged_attention_workspace_bytes(num_seqs, num_q_heads,
+ *    head_dim, max_context_len) exceeds PKV_NOALLOC_SCRATCH_BYTES is rejected
+ *    with PKV_ERR_WORKSPACE and nothing is enqueued.
+ *  - Every call shares the one array and leaves its partials there; nothing in
+ *    it needs to start at zero.  Calls that overlap on the GPU (other streams,
+ *    other threads) race on it: serialise them.
+ * The pages have no counterpart to this entry point; it exists for the callers
+ * above.  Same semantics, shapes and errors as paged_attention_decode
+ * otherwise. */
+pkv_status paged_attention_decode_noalloc(const void* q, const void* k_cache,
+                                          const void* v_cache, const int32_t* block_tables,
+                                          int max_blocks_per_seq, const int32_t* context_lens,
+                                          int max_context_len, int num_seqs, int num_q_heads,
+                                          int num_kv_heads, int head_dim, int num_blocks,
+                                          float scale, void* out, pkv_dtype dtype,
+                                          pkv_stream_t stream);
+
 /* Device status word of the current device: returns (in *flags) the
  * PKV_DEV_* bits set by kernels since the last reset, and clears them if
  * `reset` is non-zero.  Synchronises the device. */

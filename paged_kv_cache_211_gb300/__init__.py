@@ -23,7 +23,8 @@ __all__ = [
     "paged_attention_merge_pass", "paged_kv_write_new_tokens", "paged_kv_decode_step",
     "paged_kv_decode_step_partition_pass",
     "paged_kv_decode_step_staging_bytes", "paged_kv_decode_step_host", "pkv_device_status",
-    "BlockAllocator", "new_workspace",
+    "BlockAllocator", "new_workspace", "paged_attention_decode_noalloc",
+    "NOALLOC_SCRATCH_BYTES",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -79,6 +80,8 @@ _SIGS = {
     "paged_kv_decode_step_host": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp, _i, _i,
                                    _i, _i, _i, _i, _i, _f, _vp, _sz, _i, _vp], _i),
     "pkv_device_status": ([ctypes.POINTER(ctypes.c_uint), _i], _i),
+    "paged_attention_decode_noalloc": ([_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i, _f,
+                                        _vp, _i, _vp], _i),
 }
 
 
@@ -327,6 +330,25 @@ def paged_kv_decode_step_host(q_host, k_new_host, v_new_host, block_tables_host,
         _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), block_tables_host.shape[1],
         int(max_context_len), B, Hq, Hkv, D, NB, float(scale), _dev(workspace, "workspace"),
         workspace.numel() * workspace.element_size(), _dtype_code(q_host), _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def paged_attention_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens,
+                                   max_context_len, scale, out, stream=None):
+    """paged_attention_decode without a workspace argument, for callers that cannot
+    allocate device memory: the partials go to a static 32 MiB array inside the
+    library.  Calls share that array, so calls overlapping on the GPU must not be
+    issued; problems needing more scratch raise (status 6)."""
+    B, Hq, Hkv, D, NB = _check_decode_shapes(q, k_cache, v_cache, block_tables, context_lens,
+                                             out)
+    _check("paged_attention_decode_noalloc", lib().paged_attention_decode_noalloc(
+        _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_tables, "block_tables"), block_tables.shape[1],
+        _dev(context_lens, "context_lens"), int(max_context_len), B, Hq, Hkv, D, NB,
+        float(scale), _dev(out, "out"), _dtype_code(q), _stream(stream)))
+    return out
 
 
 def pkv_device_status(reset: bool = True) -> int:
