@@ -251,12 +251,14 @@ def max_over_ranks(x: float, world: int, dev=None) -> float:
 
 
 def workload_config(w, lens, per_step_bytes):
+    layers = w.num_layers
     return {
         "workload": w.name, "description": w.description, "num_seqs": w.num_seqs,
         "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
         "block_size": 16, "num_blocks": w.num_blocks, "context_tokens": int(lens.sum()),
-        "max_context_len": int(lens.max()), "layers_per_step": 1,
-        "step": "write 1 new token/seq + partition pass + LSE merge, one layer",
+        "max_context_len": int(lens.max()), "layers_per_step": layers,
+        "step": ("write 1 new token/seq + partition pass + LSE merge, one layer" if layers == 1
+                 else f"{layers} layers x (write + partition pass + LSE merge), one CUDA graph"),
         "l2": ("inputs larger than L2: %.2f GB touched per step vs 129 MB L2, no flush"
                % (per_step_bytes / 1e9)) if per_step_bytes > 4 * L2_BYTES else
               "L2 flushed (256 MB write) before every timed step",
@@ -276,7 +278,8 @@ def run_ours(args):
     w = wl.WORKLOADS[args.workload]
     if args.pool_blocks:
         w = w.with_(num_blocks=args.pool_blocks)
-    inp = wl.make_inputs(w, device=dev, num_layers=1)
+    L = w.num_layers
+    inp = wl.make_inputs(w, device=dev, num_layers=L)
     lens = inp["context_lens_host"]
     B, Hq, Hkv, D = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim
     max_len = int(lens.max())
@@ -285,7 +288,7 @@ def run_ours(args):
     bt, cl = inp["block_tables"], inp["context_lens"]
     out = torch.empty_like(q)
     ws = pkv.new_workspace(B, Hq, D, max_len, dev)
-    step_bytes = wl.algorithmic_bytes(w, lens, with_write=True)
+    step_bytes = L * wl.algorithmic_bytes(w, lens, with_write=True)
     blocks = int(((lens.astype(np.int64) + 15) // 16).sum())
     # the fused write + partition kernel: K/V of every valid token (the new row
     # read from k_new/v_new instead of the cache), q, table entries, lengths,
@@ -302,6 +305,35 @@ def run_ours(args):
         # the public one-call step: fused write + partition pass, then the merge
         pkv.paged_kv_decode_step(q, kn, vn, kc, vc, bt, cl, max_len, w.scale, out, ws,
                                  stream=stream)
+
+    eager_ms = None
+    if L > 1:
+        # every layer in one call, captured once into a CUDA graph and replayed
+        q_all = inp["q_layers"].contiguous()
+        out_all = torch.empty_like(q_all)
+        lay_args = (q_all, inp["k_new"], inp["v_new"], inp["k_cache"], inp["v_cache"], bt, cl,
+                    max_len, w.scale, out_all, ws)
+        for _ in range(3):
+            pkv.paged_kv_decode_step_layers(*lay_args, stream=stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(20):
+            pkv.paged_kv_decode_step_layers(*lay_args, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        eager_ms = e0.elapsed_time(e1) / 20
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph, stream=cap, capture_error_mode="relaxed"):
+                pkv.paged_kv_decode_step_layers(*lay_args, stream=cap)
+        stream.wait_stream(cap)
+        torch.cuda.synchronize()
+
+        def step():  # noqa: F811 - the layered step replaces the one-layer step
+            graph.replay()
 
     def step_split(evs):
         # the same two kernels through their own entry points, with events between
@@ -359,7 +391,7 @@ def run_ours(args):
 
     # end to end through the host-buffer entry point: pinned inputs in, output out
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and L == 1:
         pin = lambda t: t.cpu().pin_memory()
         qh, knh, vnh, bth, clh = pin(q), pin(kn), pin(vn), pin(bt), pin(cl)
         outh = torch.empty_like(qh).pin_memory()
@@ -428,7 +460,8 @@ def run_ours(args):
                      "traffic": traffic},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": K * (1 + merges),
+        "gpu_launches": K * L * (1 + merges),
+        "eager_ms_per_step": None if eager_ms is None else round(eager_ms, 5),
         "clocks": clk,
     }
     print(json.dumps(line), flush=True)

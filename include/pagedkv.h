@@ -72,6 +72,7 @@ typedef enum { PKV_F16 = 0, PKV_BF16 = 1 } pkv_dtype;
 #define PKV_DEV_BAD_BLOCK_ID 0x1u   /* a table entry outside [0, num_blocks) was skipped */
 #define PKV_DEV_BAD_LENGTH   0x2u   /* a context length < 0 or beyond the table / bound */
 #define PKV_DEV_BAD_SLOT     0x4u   /* a slot >= num_blocks * 16 was skipped by the write */
+#define PKV_DEV_TIMEOUT      0x8u   /* a kernel gave up an internal wait (~2 s) and returned */
 
 /* Library version (major * 10000 + minor * 100 + patch). */
 int pkv_version(void);
@@ -112,8 +113,61 @@ pkv_status paged_kv_free(pkv_allocator* a, int n, const int32_t* block_ids);
 
 int paged_kv_num_free(const pkv_allocator* a);
 
-/* Reference count of one block (0 = free), or -1 for an id out of range. */
+/* Reference count of one block (0 = free or cached), or -1 for an id out of range. */
 int paged_kv_refcount(const pkv_allocator* a, int32_t block_id);
+
+/* ---------------------------------------------------------------------------
+ * Prefix cache, copy-on-write and rollback ([P1] KVCacheManager: prefix
+ * cache; [P3] §2: blocks shared by sequences with a common prefix; [P3]
+ * §工程启示: KV rollback for speculative decoding).
+ *
+ * A full block can be registered under a 64-bit hash of its content and of
+ * everything before it (paged_kv_block_hash chains a parent hash with the
+ * block's 16 token ids).  When its count drops to 0 a registered block is
+ * not freed but kept as "cached": paged_kv_prefix_lookup can revive it for a
+ * new sequence with the same prefix, and paged_kv_alloc evicts cached blocks
+ * (least recently released first) only once the free blocks run out.
+ * paged_kv_num_free counts free and cached blocks alike (both can be taken).
+ * ------------------------------------------------------------------------- */
+
+/* Hash of one block: chains `parent_hash` (0 for the first block of a
+ * sequence) with the block's token ids (splitmix64 mixing; deterministic
+ * across runs and machines). */
+uint64_t paged_kv_block_hash(uint64_t parent_hash, const int32_t* tokens, int num_tokens);
+
+/* Registers live block `block_id` as holding the content named by `hash`.
+ * If another block already holds that hash, nothing changes (PKV_OK). A
+ * block that already carries a different hash gives PKV_ERR_INVALID_ARG; a
+ * block that is not live gives PKV_ERR_BAD_BLOCK_ID. */
+pkv_status paged_kv_prefix_insert(pkv_allocator* a, int32_t block_id, uint64_t hash);
+
+/* Looks up hashes[0..n) in order and stops at the first miss.  Every hit
+ * gains one reference (a cached block becomes live again) and its id goes to
+ * out_block_ids[i]; *num_hits receives the number of leading hits. */
+pkv_status paged_kv_prefix_lookup(pkv_allocator* a, int n, const uint64_t* hashes,
+                                  int32_t* out_block_ids, int* num_hits);
+
+/* Number of blocks registered in the prefix cache (live or cached). */
+int paged_kv_num_cached(const pkv_allocator* a);
+
+/* Copy-on-write before writing into live block `block_id`.  If the caller
+ * holds the only reference, the block keeps its id (*needs_copy = 0) and
+ * leaves the prefix cache (its content is about to change).  Otherwise a new
+ * block is taken (*out_block_id, *needs_copy = 1), the caller's reference
+ * moves to it, and the caller must copy the block's contents on the device
+ * (paged_kv_copy_blocks) before writing.  PKV_ERR_NO_BLOCKS if none can be
+ * taken (nothing changes). */
+pkv_status paged_kv_cow(pkv_allocator* a, int32_t block_id, int32_t* out_block_id,
+                        int* needs_copy);
+
+/* Rollback of a sequence to new_len tokens (e.g. rejected speculative
+ * tokens): drops the references of block_table[ceil(new_len/16) ..
+ * num_table_blocks) (host table; those entries become -1) and returns the
+ * kept block count.  A kept last block that becomes partial leaves the
+ * prefix cache when the caller holds its only reference; if it is shared the
+ * caller must copy-on-write before writing into it. */
+pkv_status paged_kv_rollback(pkv_allocator* a, int32_t* block_table, int num_table_blocks,
+                             int new_len, int* new_num_blocks);
 
 /* ---------------------------------------------------------------------------
  * Device operations
@@ -140,6 +194,17 @@ pkv_status reshape_and_cache(const void* k_new, const void* v_new, void* k_cache
                              void* v_cache, const int64_t* slot_mapping, int num_tokens,
                              int num_blocks, int num_kv_heads, int head_dim, pkv_dtype dtype,
                              pkv_stream_t stream);
+
+/* Whole-block copies in both pools of one layer (the device half of
+ * copy-on-write): block dst_block_ids[i] receives block src_block_ids[i]
+ * ([16][num_kv_heads][head_dim] of K and of V), for i < num_pairs.  Both id
+ * arrays are device int32; an id outside [0, num_blocks) skips that pair and
+ * sets PKV_DEV_BAD_BLOCK_ID.  No dst block may appear among the src blocks of
+ * the same call.  Bit-exact copy. */
+pkv_status paged_kv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src_block_ids,
+                                const int32_t* dst_block_ids, int num_pairs, int num_blocks,
+                                int num_kv_heads, int head_dim, pkv_dtype dtype,
+                                pkv_stream_t stream);
 
 /* Workspace (bytes) paged_attention_decode needs for these sizes: the
  * split-context partials (running max, running sum and unnormalised output
@@ -248,6 +313,23 @@ pkv_status paged_kv_decode_step_partition_pass(
     int max_context_len, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
     int num_blocks, float scale, void* out, int64_t* slot_mapping_out, void* workspace,
     size_t workspace_bytes, pkv_dtype dtype, pkv_stream_t stream);
+
+/* One decode step of every layer of a layer-major stack ([P3] item 3: pools
+ * are layer-major; item 1: every layer reads its cache through the same
+ * per-sequence lengths here): for l < num_layers, paged_kv_decode_step on
+ *   q + l*[B][Hq][D], k_new / v_new + l*[B][Hkv][D], the pools' layer l
+ *   (k_cache / v_cache + l*[num_blocks][16][Hkv][D]) and out + l*[B][Hq][D],
+ * in order on `stream`, sharing block_tables, context_lens and the workspace.
+ * The call neither allocates nor synchronises, so a caller may capture it
+ * into a CUDA graph (stream capture) and replay the whole step. */
+pkv_status paged_kv_decode_step_layers(const void* q, const void* k_new, const void* v_new,
+                                       void* k_cache, void* v_cache, const int32_t* block_tables,
+                                       int max_blocks_per_seq, const int32_t* context_lens,
+                                       int max_context_len, int num_seqs, int num_q_heads,
+                                       int num_kv_heads, int head_dim, int num_blocks,
+                                       int num_layers, float scale, void* out, void* workspace,
+                                       size_t workspace_bytes, pkv_dtype dtype,
+                                       pkv_stream_t stream);
 
 /* Device staging bytes paged_kv_decode_step_host needs: device copies of q,
  * k_new, v_new, block_tables, context_lens and out, each 256-byte aligned. */

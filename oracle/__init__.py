@@ -17,6 +17,10 @@ Functions and the passages they follow (page title, section):
   decode stage) over the cache above; plain softmax attention in fp64.
 * ``decode_f16`` / ``decode_bf16`` -- the IEEE binary16 and bfloat16 format
   definitions.
+* ``copy_blocks`` -- the device half of copy-on-write (whole-block copies).
+* ``prefix_cache_model.PrefixCacheModel`` -- the allocator's policy (free
+  stack, prefix cache by hash, LRU of released cached blocks, copy-on-write,
+  rollback) in plain Python.
 
 Every function is pinned by ``tests/test_oracle_pins.py`` against something
 other than itself (library routines, brute force, closed forms, invariants).
@@ -89,6 +93,9 @@ class Oracle:
                                              ctypes.c_int, ctypes.c_double, c_f64p, c_f64p,
                                              ctypes.c_int64]
         lib.pko_decode_attention.restype = ctypes.c_int
+        lib.pko_copy_blocks.argtypes = [c_u16p, c_u16p, c_i32p, c_i32p, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        lib.pko_copy_blocks.restype = ctypes.c_int
         self.lib = lib
         self.path = so_path
 
@@ -133,6 +140,19 @@ class Oracle:
                                             _ptr(sl, ctypes.c_int64), sl.shape[0], nb, bs, hkv, d)
         if rc != 0:
             raise ValueError(f"oracle reshape_and_cache failed with code {rc}")
+        return kc, vc
+
+    def copy_blocks(self, k_cache, v_cache, src, dst):
+        """Copies of the pools after block dst[i] receives block src[i] (K and V)."""
+        kc, vc = _bits(k_cache).copy(), _bits(v_cache).copy()
+        s = np.ascontiguousarray(src, dtype=np.int32)
+        d = np.ascontiguousarray(dst, dtype=np.int32)
+        nb, bs, hkv, hd = kc.shape
+        rc = self.lib.pko_copy_blocks(_ptr(kc, ctypes.c_uint16), _ptr(vc, ctypes.c_uint16),
+                                      _ptr(s, ctypes.c_int32), _ptr(d, ctypes.c_int32), s.shape[0],
+                                      nb, bs, hkv, hd)
+        if rc != 0:
+            raise ValueError(f"oracle copy_blocks failed with code {rc}")
         return kc, vc
 
     def decode_attention(self, dtype: int, q, k_cache, v_cache, block_tables, context_lens,
@@ -202,6 +222,10 @@ def slot_mapping(block_tables, context_lens, block_size: int, num_blocks: int):
 
 def reshape_and_cache(k_new, v_new, k_cache, v_cache, slots):
     return default().reshape_and_cache(k_new, v_new, k_cache, v_cache, slots)
+
+
+def copy_blocks(k_cache, v_cache, src, dst):
+    return default().copy_blocks(k_cache, v_cache, src, dst)
 
 
 def decode_attention(dtype: int, q, k_cache, v_cache, block_tables, context_lens, scale: float,

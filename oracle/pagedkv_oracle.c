@@ -219,3 +219,20 @@ int pko_decode_attention(int dtype, const uint16_t* q, const uint16_t* k_cache,
     free(qd);
     return rc;
 }
+
+/* Whole-block copy of one layer's pools (the device half of copy-on-write):
+ * block dst[i] receives block src[i] ([block_size][num_kv_heads][head_dim]
+ * of K and of V).  A pure byte copy, pair by pair in order. */
+int pko_copy_blocks(uint16_t* k_cache, uint16_t* v_cache, const int32_t* src,
+                    const int32_t* dst, int num_pairs, int num_blocks, int block_size,
+                    int num_kv_heads, int head_dim) {
+    if (!k_cache || !v_cache || !src || !dst) return PKO_ERR_ARG;
+    int64_t blk = (int64_t)block_size * num_kv_heads * head_dim;
+    for (int i = 0; i < num_pairs; ++i) {
+        if (src[i] < 0 || src[i] >= num_blocks || dst[i] < 0 || dst[i] >= num_blocks)
+            return PKO_ERR_BLOCK_ID;
+        memcpy(k_cache + dst[i] * blk, k_cache + src[i] * blk, (size_t)blk * 2);
+        memcpy(v_cache + dst[i] * blk, v_cache + src[i] * blk, (size_t)blk * 2);
+    }
+    return PKO_OK;
+}

@@ -21,9 +21,9 @@ __all__ = [
     "paged_attention_min_partition_blocks", "paged_attention_decode",
     "paged_attention_decode_partitioned", "paged_attention_partition_pass",
     "paged_attention_merge_pass", "paged_kv_write_new_tokens", "paged_kv_decode_step",
-    "paged_kv_decode_step_partition_pass",
+    "paged_kv_decode_step_partition_pass", "paged_kv_decode_step_layers",
     "paged_kv_decode_step_staging_bytes", "paged_kv_decode_step_host", "pkv_device_status",
-    "BlockAllocator", "new_workspace", "paged_attention_decode_noalloc",
+    "BlockAllocator", "new_workspace", "paged_kv_block_hash", "paged_kv_copy_blocks", "paged_attention_decode_noalloc",
     "NOALLOC_SCRATCH_BYTES",
 ]
 
@@ -76,10 +76,20 @@ _SIGS = {
                                    _vp], _i),
     "paged_kv_decode_step_partition_pass": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i,
                                              _i, _i, _i, _f, _vp, _vp, _vp, _sz, _i, _vp], _i),
+    "paged_kv_decode_step_layers": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i,
+                                     _i, _i, _f, _vp, _vp, _sz, _i, _vp], _i),
     "paged_kv_decode_step_staging_bytes": ([_i, _i, _i, _i, _i], _sz),
     "paged_kv_decode_step_host": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp, _i, _i,
                                    _i, _i, _i, _i, _i, _f, _vp, _sz, _i, _vp], _i),
     "pkv_device_status": ([ctypes.POINTER(ctypes.c_uint), _i], _i),
+    "paged_kv_num_cached": ([_vp], _i),
+    "paged_kv_block_hash": ([ctypes.c_uint64, _vp, _i], ctypes.c_uint64),
+    "paged_kv_prefix_insert": ([_vp, ctypes.c_int32, ctypes.c_uint64], _i),
+    "paged_kv_prefix_lookup": ([_vp, _i, _vp, _vp, ctypes.POINTER(_i)], _i),
+    "paged_kv_cow": ([_vp, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(_i)],
+                     _i),
+    "paged_kv_rollback": ([_vp, _vp, _i, _i, ctypes.POINTER(_i)], _i),
+    "paged_kv_copy_blocks": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp], _i),
     "paged_attention_decode_noalloc": ([_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i, _f,
                                         _vp, _i, _vp], _i),
 }
@@ -300,6 +310,29 @@ def paged_kv_decode_step_partition_pass(q, k_new, v_new, k_cache, v_cache, block
                         workspace, slot_mapping_out, stream)
 
 
+def paged_kv_decode_step_layers(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
+                                max_context_len, scale, out, workspace, stream=None):
+    """One decode step of every layer: q/out [L,B,Hq,D], k_new/v_new [L,B,Hkv,D],
+    pools [L,NB,16,Hkv,D] (layer-major); tables, lengths and workspace shared."""
+    L, B, Hq, D = q.shape
+    L2, NB, bs, Hkv, D2 = k_cache.shape
+    if L2 != L or bs != BLOCK_SIZE or D2 != D or v_cache.shape != k_cache.shape:
+        raise ValueError("pools must be [layers, num_blocks, 16, num_kv_heads, head_dim]")
+    if tuple(k_new.shape) != (L, B, Hkv, D) or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new must be [layers, num_seqs, num_kv_heads, head_dim]")
+    if out.shape != q.shape or out.dtype != q.dtype or k_cache.dtype != q.dtype:
+        raise ValueError("q, out and the pools must share one dtype; out shaped like q")
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise ValueError("block tables and lengths must be int32")
+    _check("paged_kv_decode_step_layers", lib().paged_kv_decode_step_layers(
+        _dev(q, "q"), _dev(k_new, "k_new"), _dev(v_new, "v_new"), _dev(k_cache, "k_cache"),
+        _dev(v_cache, "v_cache"), _dev(block_tables, "block_tables"), block_tables.shape[1],
+        _dev(context_lens, "context_lens"), int(max_context_len), B, Hq, Hkv, D, NB, L,
+        float(scale), _dev(out, "out"), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _dtype_code(q), _stream(stream)))
+    return out
+
+
 def paged_kv_decode_step_staging_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
                                        max_blocks_per_seq) -> int:
     return lib().paged_kv_decode_step_staging_bytes(num_seqs, num_q_heads, num_kv_heads,
@@ -349,6 +382,26 @@ def paged_attention_decode_noalloc(q, k_cache, v_cache, block_tables, context_le
         _dev(context_lens, "context_lens"), int(max_context_len), B, Hq, Hkv, D, NB,
         float(scale), _dev(out, "out"), _dtype_code(q), _stream(stream)))
     return out
+
+
+def paged_kv_block_hash(parent_hash: int, tokens) -> int:
+    """64-bit hash of one block's token ids chained with its parent block's hash."""
+    arr = (ctypes.c_int32 * max(len(tokens), 1))(*[int(t) for t in tokens])
+    return lib().paged_kv_block_hash(ctypes.c_uint64(parent_hash),
+                                     ctypes.cast(arr, ctypes.c_void_p), len(tokens))
+
+
+def paged_kv_copy_blocks(k_cache, v_cache, src_block_ids, dst_block_ids, stream=None):
+    """Copy whole blocks src -> dst in both pools of one layer (device int32 id lists)."""
+    NB, bs, Hkv, D = k_cache.shape
+    if v_cache.shape != k_cache.shape or bs != BLOCK_SIZE:
+        raise ValueError("pool shape must be [num_blocks, 16, num_kv_heads, head_dim]")
+    if src_block_ids.dtype != torch.int32 or dst_block_ids.shape != src_block_ids.shape:
+        raise ValueError("block id lists must be int32 and of equal length")
+    _check("paged_kv_copy_blocks", lib().paged_kv_copy_blocks(
+        _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), _dev(src_block_ids, "src"),
+        _dev(dst_block_ids, "dst"), src_block_ids.numel(), NB, Hkv, D, _dtype_code(k_cache),
+        _stream(stream)))
 
 
 def pkv_device_status(reset: bool = True) -> int:
@@ -401,3 +454,37 @@ class BlockAllocator:
 
     def refcount(self, block_id: int) -> int:
         return lib().paged_kv_refcount(self._h, block_id)
+
+    def num_cached(self) -> int:
+        return lib().paged_kv_num_cached(self._h)
+
+    def prefix_insert(self, block_id: int, block_hash: int):
+        _check("paged_kv_prefix_insert",
+               lib().paged_kv_prefix_insert(self._h, block_id, ctypes.c_uint64(block_hash)))
+
+    def prefix_lookup(self, hashes) -> list:
+        """Ids of the leading cached blocks (each gains a reference); stops at a miss."""
+        n = len(hashes)
+        harr = (ctypes.c_uint64 * max(n, 1))(*[int(h) for h in hashes])
+        out = (ctypes.c_int32 * max(n, 1))()
+        hits = ctypes.c_int(0)
+        _check("paged_kv_prefix_lookup", lib().paged_kv_prefix_lookup(
+            self._h, n, ctypes.cast(harr, ctypes.c_void_p), ctypes.cast(out, ctypes.c_void_p),
+            ctypes.byref(hits)))
+        return list(out[:hits.value])
+
+    def cow(self, block_id: int):
+        """(block to write into, whether the caller must copy the old block's content)."""
+        new_id = ctypes.c_int32(0)
+        copy = ctypes.c_int(0)
+        _check("paged_kv_cow", lib().paged_kv_cow(self._h, block_id, ctypes.byref(new_id),
+                                                  ctypes.byref(copy)))
+        return new_id.value, bool(copy.value)
+
+    def rollback(self, table, new_len: int):
+        """Drop the blocks past new_len tokens; returns the kept table."""
+        arr = (ctypes.c_int32 * max(len(table), 1))(*[int(b) for b in table])
+        keep = ctypes.c_int(0)
+        _check("paged_kv_rollback", lib().paged_kv_rollback(
+            self._h, ctypes.cast(arr, ctypes.c_void_p), len(table), new_len, ctypes.byref(keep)))
+        return list(arr[:keep.value])

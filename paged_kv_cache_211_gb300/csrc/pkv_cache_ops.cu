@@ -101,6 +101,28 @@ __global__ void decode_step_write_kernel(const uint4* __restrict__ k_new,
     (is_v ? v_cache : k_cache)[slot * row_vecs + c] = v;
 }
 
+// Whole-block copies for copy-on-write: block dst[i] of both pools receives
+// block src[i] ([16][Hkv][D] each).  One thread per 16-byte vector.
+__global__ void copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                                   const int32_t* __restrict__ src,
+                                   const int32_t* __restrict__ dst, int num_pairs,
+                                   int num_blocks, int block_vecs, unsigned int* status) {
+    const int64_t per_pair = 2ll * block_vecs;
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= per_pair * num_pairs) return;
+    const int i = (int)(idx / per_pair);
+    const int r = (int)(idx - (int64_t)i * per_pair);
+    const bool is_v = r >= block_vecs;
+    const int c = is_v ? r - block_vecs : r;
+    const int32_t s = src[i], d = dst[i];
+    if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
+        if (r == 0) atomicOr(status, PKV_DEV_BAD_BLOCK_ID);
+        return;
+    }
+    uint4* pool = is_v ? v_cache : k_cache;
+    pool[(int64_t)d * block_vecs + c] = pool[(int64_t)s * block_vecs + c];
+}
+
 }  // namespace
 
 // Launches the decode-step write (used by paged_kv_decode_step).
@@ -164,6 +186,28 @@ pkv_status reshape_and_cache(const void* k_new, const void* v_new, void* k_cache
         static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
         static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), slot_mapping, num_tokens,
         (int64_t)num_blocks * PKV_BLOCK_SIZE, row_vecs, status);
+    return pkv::cuda_status(cudaGetLastError());
+}
+
+pkv_status paged_kv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src_block_ids,
+                                const int32_t* dst_block_ids, int num_pairs, int num_blocks,
+                                int num_kv_heads, int head_dim, pkv_dtype dtype,
+                                pkv_stream_t stream) {
+    if (num_pairs < 0 || num_blocks <= 0 || num_kv_heads <= 0 || head_dim <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (dtype != PKV_F16 && dtype != PKV_BF16) return PKV_ERR_INVALID_ARG;
+    if ((head_dim * 2) % 16 != 0) return PKV_ERR_UNSUPPORTED;
+    if (num_pairs == 0) return PKV_OK;
+    if (!k_cache || !v_cache || !src_block_ids || !dst_block_ids) return PKV_ERR_INVALID_ARG;
+    if (!pkv::aligned16(k_cache) || !pkv::aligned16(v_cache)) return PKV_ERR_INVALID_ARG;
+    unsigned int* status = pkv::status_word();
+    if (!status) return PKV_ERR_CUDA;
+    const int block_vecs = PKV_BLOCK_SIZE * num_kv_heads * head_dim / 8;
+    const int64_t total = 2ll * block_vecs * num_pairs;
+    const int grid = (int)((total + pkv::kThreads - 1) / pkv::kThreads);
+    pkv::copy_blocks_kernel<<<grid, pkv::kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), src_block_ids,
+        dst_block_ids, num_pairs, num_blocks, block_vecs, status);
     return pkv::cuda_status(cudaGetLastError());
 }
 

@@ -35,8 +35,14 @@
 // layout of the second MMA with two 8x8 movmatrix transposes.  Loads of the
 // next block are issued before the current block is computed (two register
 // stages).
+#include <cuda.h>  // CUtensorMap and its enums (the encoder is fetched at run time)
+
 #include <algorithm>
 #include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <type_traits>
 
 #include "pkv_internal.cuh"
 
@@ -111,7 +117,8 @@ struct DecodeParams {
     float scale_log2;          // scale * log2(e): scores live in base 2
 };
 
-// Sum over the CTA; every thread gets the result.
+// Sum over the CTA of NW warps; every thread gets the result.
+template <int NW = kWarps>
 __device__ __forceinline__ int cta_sum(int v, int* red) {
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -120,11 +127,12 @@ __device__ __forceinline__ int cta_sum(int v, int* red) {
     __syncthreads();
     int t = 0;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) t += red[w];
+    for (int w = 0; w < NW; ++w) t += red[w];
     return t;
 }
 
-// Exclusive prefix sum over the CTA (thread order); *total gets the sum.
+// Exclusive prefix sum over the CTA of NW warps (thread order); *total gets the sum.
+template <int NW = kWarps>
 __device__ __forceinline__ int cta_exclusive_scan(int v, int* red, int* total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int incl = v;
@@ -137,7 +145,7 @@ __device__ __forceinline__ int cta_exclusive_scan(int v, int* red, int* total) {
     __syncthreads();
     int before = 0, all = 0;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
+    for (int w = 0; w < NW; ++w) {
         if (w < warp) before += red[w];
         all += red[w];
     }
@@ -534,6 +542,476 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
     }
 }
 
+
+// ============================================================================
+// Partition pass, TMA version (the default).
+//
+// One persistent CTA per SM: four consumer warps do exactly the arithmetic of
+// the kernel above, and one producer warp feeds them.  The producer walks the
+// same items and blocks, reads the block table 32 entries at a time, and for
+// each block issues cp.async.bulk.tensor copies of the 16 rows x D K and V
+// tiles of its KV head (boxes of 16 rows x 64 elements, 128-byte swizzle)
+// into a ring of shared-memory stages, one ring per consumer warp, tracked
+// by "full" / "empty" mbarriers.  The producer runs ahead across item
+// boundaries, so up to (ring size) blocks per consumer are in flight
+// regardless of registers.  Consumers read their operands with ldmatrix
+// (.trans for V), which the swizzle makes conflict-free, and release each
+// stage as soon as its fragments are in registers.  Every mbarrier wait is
+// bounded: on a time-out the kernel sets PKV_DEV_TIMEOUT, stops issuing and
+// waiting, lets every copy it issued land, and returns.
+// ============================================================================
+constexpr int kTmaConsumers = 4;
+constexpr int kTmaThreads = (kTmaConsumers + 1) * 32;
+constexpr int kTmaItemsPerCta = 8;
+constexpr int kTmaMaxStages = 8;
+constexpr long long kWaitCycles = 4000000000ll;  // ~2 s at 2 GHz
+
+__device__ __forceinline__ uint32_t smem_addr(const void* ptr) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Waits for the phase of `bar` with parity `parity`.  Returns false without
+// waiting once *abort is set, and sets *abort and the status bit when the
+// wait exceeds kWaitCycles.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          unsigned int* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!*abort) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (clock64() - t0 > kWaitCycles) {
+            *abort = 1;
+            atomicOr(status, PKV_DEV_TIMEOUT);
+            return false;
+        }
+    }
+    return false;
+}
+
+// A bounded wait that ignores the abort flag (used to let issued copies land).
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, unsigned int* status) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > kWaitCycles) {
+            atomicOr(status, PKV_DEV_TIMEOUT);
+            return;
+        }
+    }
+}
+
+// 16 rows x 64 elements of one KV head: tensor coordinates (element x, head, row).
+__device__ __forceinline__ void tma_load_rows(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                              int x, int head, int row) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];\n" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(head), "r"(row)
+        : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
+// Byte offset of 16-byte chunk c (of D/8) of row `row` in a swizzled tile of
+// 64-element boxes: box c/8 (2 KB each), 128-byte row, chunk (c%8) ^ (row%8).
+__device__ __forceinline__ uint32_t swz(int row, int c) {
+    return (uint32_t)((c >> 3) * 2048 + row * 128 + (((c & 7) ^ (row & 7)) << 4));
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+    decode_partition_tma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
+                                const __grid_constant__ CUtensorMap tmap_v, int nstages) {
+    using E = Elem<T>;
+    constexpr int NC = kTmaConsumers;
+    constexpr int HALVES = D / 64;
+    constexpr int TILE = 16 * D * 2;   // one K or V tile: 16 rows x D
+    constexpr int STAGE = 2 * TILE;    // K tile, then V tile
+    constexpr int KS = D / 16;         // k-steps of the score MMA = row tiles of O^T
+    constexpr int DP = D + 4;          // padded rows of the merge buffer
+    extern __shared__ unsigned char smem_raw[];
+    const int B = p.num_seqs;
+    const uint32_t raw = smem_addr(smem_raw);
+    unsigned char* ring = smem_raw + (((raw + 1023u) & ~1023u) - raw);  // 1024-B aligned
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)NC * nstages * STAGE);
+    uint64_t* empty = full + NC * nstages;
+    int* stage_id = reinterpret_cast<int*>(empty + NC * nstages);     // block id per slot
+    int* last_use = stage_id + NC * nstages;                           // last use issued per slot
+    float* sm_o = reinterpret_cast<float*>(last_use + NC * nstages);   // [NC][8][DP]
+    float* sm_m = sm_o + NC * kMaxGroup * DP;                          // [NC][8]
+    float* sm_l = sm_m + NC * kMaxGroup;                               // [NC][8]
+    int* red = reinterpret_cast<int*>(sm_l + NC * kMaxGroup);          // [NC + 1]
+    volatile int* abort_flag = red + NC + 1;
+    int* sm_len = red + NC + 2 + NC;                                   // [B]
+    int* sm_off = sm_len + B;                                          // [B + 1]
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) {
+        for (int i = 0; i < NC * nstages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+            last_use[i] = -1;
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+
+    // validated lengths, partition length, partitions per sequence (all warps)
+    int my_blocks = 0;
+    for (int s = tid; s < B; s += kTmaThreads) {
+        int n = p.context_lens[s];
+        if (n < 0 || n > p.len_bound) {
+            if (blockIdx.x == 0) atomicOr(p.status, PKV_DEV_BAD_LENGTH);
+            n = 0;
+        }
+        sm_len[s] = n;
+        if (n == 0 && p.slot_out && blockIdx.x == 0) p.slot_out[s] = -1;
+        my_blocks += (n + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
+    }
+    const int total_blocks = cta_sum<NC + 1>(my_blocks, red);
+    int PB = p.partition_blocks;
+    if (PB <= 0) {
+        const long long want =
+            ((long long)total_blocks * p.num_kv_heads + p.target_items - 1) / p.target_items;
+        const long long lo = p.min_partition_blocks;
+        const long long hi = kAdaptiveMaxBlocks > lo ? kAdaptiveMaxBlocks : lo;
+        PB = (int)(want < lo ? lo : (want > hi ? hi : want));
+    }
+    const int chunk = (B + kTmaThreads - 1) / kTmaThreads;
+    const int s_lo = min(B, tid * chunk), s_hi = min(B, s_lo + chunk);
+    int mine = 0;
+    for (int s = s_lo; s < s_hi; ++s) mine += parts_of(sm_len[s], PB);
+    int total_parts = 0;
+    int run = cta_exclusive_scan<NC + 1>(mine, red, &total_parts);
+    for (int s = s_lo; s < s_hi; ++s) {
+        sm_off[s] = run;
+        run += parts_of(sm_len[s], PB);
+    }
+    if (tid == 0) sm_off[B] = total_parts;
+    __syncthreads();
+    if (blockIdx.x == 0) {
+        for (int s = tid; s <= B; s += kTmaThreads) p.ws_offsets[s] = sm_off[s];
+    }
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+
+    const int Hq = p.num_q_heads, Hkv = p.num_kv_heads, g = p.group;
+    const size_t row_stride = (size_t)Hkv * D;
+    const int total_items = total_parts * Hkv;
+    struct Item {
+        int s, h, gp, nparts, n, nblk, lo, hi;
+    };
+    auto item_of = [&](int item) {
+        Item it;
+        it.gp = item / Hkv;
+        it.h = item - it.gp * Hkv;
+        int a = 0, b = B - 1;
+        while (a < b) {
+            const int mid = (a + b + 1) >> 1;
+            if (sm_off[mid] <= it.gp) a = mid; else b = mid - 1;
+        }
+        it.s = a;
+        it.nparts = sm_off[a + 1] - sm_off[a];
+        it.n = sm_len[a];
+        it.nblk = (it.n + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
+        it.lo = (it.gp - sm_off[a]) * PB;
+        it.hi = min(it.nblk, it.lo + PB);
+        return it;
+    };
+
+    if (warp == NC) {
+        // ------------------------------------------------------------ producer
+        // Blocks come in batches from the start of the item, lane t issuing
+        // block jb + t.  Block i of an item belongs to consumer i % NC; its
+        // position in that consumer's ring is the consumer's running count
+        // plus t / NC (batches hold a multiple of NC blocks).  A batch gives
+        // each consumer at most `nstages` blocks, so no lane ever waits for a
+        // slot that another lane of this warp has yet to fill: every wait is
+        // on a consumer warp, never on a diverged lane of this one.
+        static_assert(32 % NC == 0, "consumers must divide the warp");
+        const int batch = min(32, NC * nstages);
+        int pc[NC];  // stages issued so far per consumer (same in every lane)
+#pragma unroll
+        for (int v = 0; v < NC; ++v) pc[v] = 0;
+        for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
+            const Item it = item_of(item);
+            const int32_t* table = p.block_tables + (size_t)it.s * p.max_blocks_per_seq;
+            for (int jb = it.lo; jb < it.hi; jb += batch) {
+                const int cnt = min(batch, it.hi - jb);
+                if (lane < cnt && !*abort_flag) {
+                    int id = table[jb + lane];
+                    if (id < 0 || id >= p.num_blocks) {
+                        atomicOr(p.status, PKV_DEV_BAD_BLOCK_ID);
+                        id = -1;  // never read: block 0 is fetched and fully masked
+                    }
+                    const int w = lane % NC;
+                    int base = 0;
+#pragma unroll
+                    for (int v = 0; v < NC; ++v)
+                        if (v == w) base = pc[v];
+                    const int use = base + lane / NC;
+                    const int k = w * nstages + use % nstages;
+                    if (mbar_wait(&empty[k], ((use / nstages) & 1) ^ 1, abort_flag, p.status)) {
+                        stage_id[k] = id;
+                        last_use[k] = use;
+                        mbar_arrive_expect_tx(&full[k], STAGE);
+                        unsigned char* st = ring + (size_t)k * STAGE;
+                        const int row = (id < 0 ? 0 : id) * PKV_BLOCK_SIZE;
+#pragma unroll
+                        for (int hh = 0; hh < HALVES; ++hh) {
+                            tma_load_rows(st + hh * 2048, &tmap_k, &full[k], hh * 64, it.h, row);
+                            tma_load_rows(st + TILE + hh * 2048, &tmap_v, &full[k], hh * 64,
+                                          it.h, row);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int v = 0; v < NC; ++v) pc[v] += (cnt - v + NC - 1) / NC;
+                __syncwarp();
+            }
+        }
+        // every copy issued must land before the CTA may exit: wait for the
+        // last use issued into each slot (earlier uses completed before reuse)
+        __syncwarp();
+        for (int k = lane; k < NC * nstages; k += 32) {
+            const int use = last_use[k];
+            if (use >= 0) mbar_drain(&full[k], (use / nstages) & 1, p.status);
+        }
+        return;
+    }
+
+    // -------------------------------------------------------------- consumers
+    const int w = warp;
+    const int gid = lane >> 2, tig = lane & 3;
+    const T* __restrict__ q = static_cast<const T*>(p.q);
+    int ncons = 0;  // stages this warp has consumed
+    for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
+        const Item it = item_of(item);
+        const int s = it.s, h = it.h, n = it.n;
+        // q fragment: column gid of the score MMA is query head h*g + gid
+        uint32_t qf[KS][2];
+        {
+            const bool live = gid < g;
+            const T* qrow = q + ((size_t)s * Hq + (size_t)h * g + (live ? gid : 0)) * D;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+                qf[ks][0] = live ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * tig) : 0u;
+                qf[ks][1] =
+                    live ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * tig) : 0u;
+            }
+        }
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        float o[KS][4];
+#pragma unroll
+        for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+        const bool writes = p.k_new != nullptr && n > 0;
+        const int last_blk = writes ? it.nblk - 1 : -1;
+        const int rnew = (n - 1) & (PKV_BLOCK_SIZE - 1);
+        T* kbase_w = static_cast<T*>(p.k_cache_w) + (size_t)h * D;
+        T* vbase_w = static_cast<T*>(p.v_cache_w) + (size_t)h * D;
+
+        for (int j = it.lo + w; j < it.hi; j += NC, ++ncons) {
+            const int k = w * nstages + ncons % nstages;
+            const bool ok = mbar_wait(&full[k], (ncons / nstages) & 1, abort_flag, p.status);
+            unsigned char* st = ring + (size_t)k * STAGE;
+            const int id = ok ? stage_id[k] : -1;
+            const int nv = id < 0 ? 0 : min(PKV_BLOCK_SIZE, n - j * PKV_BLOCK_SIZE);
+            if (j == last_blk) {
+                // this step's token: not in the cache yet; patch it into the
+                // stage from k_new / v_new and store it into its slot
+                if (id >= 0) {
+                    constexpr int CH = D / 8;
+                    if (lane < 2 * CH) {
+                        const bool isv = lane >= CH;
+                        const int c = isv ? lane - CH : lane;
+                        const T* src = static_cast<const T*>(isv ? p.v_new : p.k_new) +
+                                       ((size_t)s * Hkv + h) * D + c * 8;
+                        const uint4 v = *reinterpret_cast<const uint4*>(src);
+                        *reinterpret_cast<uint4*>(st + (isv ? TILE : 0) + swz(rnew, c)) = v;
+                        T* dst = (isv ? vbase_w : kbase_w) +
+                                 ((size_t)id * PKV_BLOCK_SIZE + rnew) * row_stride + c * 8;
+                        *reinterpret_cast<uint4*>(dst) = v;
+                    }
+                    // the stage is refilled by the async proxy after release
+                    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+                    __syncwarp();
+                }
+                if (p.slot_out && h == 0 && lane == 0)
+                    p.slot_out[s] = id >= 0 ? (int64_t)id * PKV_BLOCK_SIZE + rnew : -1;
+            }
+            uint32_t kf[KS][4], vf[KS][4];
+            if (ok) {
+                const uint32_t kt = smem_addr(st), vt = kt + TILE;
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    const int row = lane & 15;
+                    ldsm_x4(kf[ks], kt + swz(row, 2 * ks + (lane >> 4)));
+                    const int mi = lane >> 3;
+                    const int tok = (lane & 7) + 8 * (mi >> 1);
+                    ldsm_x4_trans(vf[ks], vt + swz(tok, 2 * ks + (mi & 1)));
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[k]);  // fragments are in registers
+            if (!ok || nv == 0) continue;
+
+            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < KS; ks += 2) {
+                E::mma(sa, kf[ks][0], kf[ks][1], kf[ks][2], kf[ks][3], qf[ks][0], qf[ks][1]);
+                E::mma(sb, kf[ks + 1][0], kf[ks + 1][1], kf[ks + 1][2], kf[ks + 1][3],
+                       qf[ks + 1][0], qf[ks + 1][1]);
+            }
+            float s0 = (sa[0] + sb[0]) * p.scale_log2, s1 = (sa[1] + sb[1]) * p.scale_log2;
+            float s2 = (sa[2] + sb[2]) * p.scale_log2, s3 = (sa[3] + sb[3]) * p.scale_log2;
+            if (nv < PKV_BLOCK_SIZE) {  // partial last block: select, never weight
+                if (gid >= nv) s0 = s1 = -INFINITY;
+                if (gid + 8 >= nv) s2 = s3 = -INFINITY;
+                const uint32_t mlo = (2 * tig < nv ? 0x0000ffffu : 0u) |
+                                     (2 * tig + 1 < nv ? 0xffff0000u : 0u);
+                const uint32_t mhi = (2 * tig + 8 < nv ? 0x0000ffffu : 0u) |
+                                     (2 * tig + 9 < nv ? 0xffff0000u : 0u);
+#pragma unroll
+                for (int i = 0; i < KS; ++i) {
+                    vf[i][0] &= mlo;
+                    vf[i][1] &= mlo;
+                    vf[i][2] &= mhi;
+                    vf[i][3] &= mhi;
+                }
+            }
+            float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float ms0 = mn0 == -INFINITY ? 0.f : mn0;
+            const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
+            const float c0 = fast_exp2(m0 - ms0), c1 = fast_exp2(m1 - ms1);
+            const float p0 = fast_exp2(s0 - ms0), p1 = fast_exp2(s1 - ms1);
+            const float p2 = fast_exp2(s2 - ms0), p3 = fast_exp2(s3 - ms1);
+            l0 = l0 * c0 + p0 + p2;
+            l1 = l1 * c1 + p1 + p3;
+            m0 = mn0;
+            m1 = mn1;
+#pragma unroll
+            for (int i = 0; i < KS; ++i) {
+                o[i][0] *= c0;
+                o[i][1] *= c1;
+                o[i][2] *= c0;
+                o[i][3] *= c1;
+            }
+            const uint32_t pt = movmatrix_trans(E::pack(p0, p1));
+            const uint32_t pbt = movmatrix_trans(E::pack(p2, p3));
+#pragma unroll
+            for (int i = 0; i < KS; ++i)
+                E::mma(o[i], vf[i][0], vf[i][1], vf[i][2], vf[i][3], pt, pbt);
+        }
+
+        // combine the consumer warps of this item (named barrier: consumers only)
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+        }
+        float* mo = sm_o + w * kMaxGroup * DP;
+#pragma unroll
+        for (int i = 0; i < KS; ++i) {
+            mo[(2 * tig) * DP + 16 * i + gid] = o[i][0];
+            mo[(2 * tig + 1) * DP + 16 * i + gid] = o[i][1];
+            mo[(2 * tig) * DP + 16 * i + 8 + gid] = o[i][2];
+            mo[(2 * tig + 1) * DP + 16 * i + 8 + gid] = o[i][3];
+        }
+        if (gid == 0) {
+            sm_m[w * kMaxGroup + 2 * tig] = m0;
+            sm_m[w * kMaxGroup + 2 * tig + 1] = m1;
+            sm_l[w * kMaxGroup + 2 * tig] = l0;
+            sm_l[w * kMaxGroup + 2 * tig + 1] = l1;
+        }
+        asm volatile("bar.sync 1, %0;\n" ::"r"(NC * 32) : "memory");
+        constexpr int SL = D / 8;
+        for (int x = tid; x < g * SL; x += NC * 32) {
+            const int hh = x / SL, d0 = (x - hh * SL) * 8;
+            float M = -INFINITY;
+#pragma unroll
+            for (int v = 0; v < NC; ++v) M = fmaxf(M, sm_m[v * kMaxGroup + hh]);
+            const float Ms = M == -INFINITY ? 0.f : M;
+            float L = 0.f;
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int v = 0; v < NC; ++v) {
+                const float e = fast_exp2(sm_m[v * kMaxGroup + hh] - Ms);
+                L += e * sm_l[v * kMaxGroup + hh];
+                const float* src = sm_o + (v * kMaxGroup + hh) * DP + d0;
+                const float4 u = *reinterpret_cast<const float4*>(src);
+                const float4 u2 = *reinterpret_cast<const float4*>(src + 4);
+                acc[0] += e * u.x; acc[1] += e * u.y; acc[2] += e * u.z; acc[3] += e * u.w;
+                acc[4] += e * u2.x; acc[5] += e * u2.y; acc[6] += e * u2.z; acc[7] += e * u2.w;
+            }
+            const int qh = h * g + hh;
+            if (it.nparts == 1) {
+                const float inv = L > 0.f ? 1.f / L : 0.f;
+                uint4 packed;
+                packed.x = E::pack(acc[0] * inv, acc[1] * inv);
+                packed.y = E::pack(acc[2] * inv, acc[3] * inv);
+                packed.z = E::pack(acc[4] * inv, acc[5] * inv);
+                packed.w = E::pack(acc[6] * inv, acc[7] * inv);
+                *reinterpret_cast<uint4*>(static_cast<T*>(p.out) + ((size_t)s * Hq + qh) * D +
+                                          d0) = packed;
+            } else {
+                const size_t row = (size_t)it.gp * Hq + qh;
+                float* dst = p.ws_o + row * D + d0;
+                *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+                if (d0 == 0) {
+                    p.ws_m[row] = M;
+                    p.ws_l[row] = L;
+                }
+            }
+        }
+        asm volatile("bar.sync 1, %0;\n" ::"r"(NC * 32) : "memory");
+    }
+}
+
 struct MergeParams {
     const int* ws_offsets;
     const float* ws_m;
@@ -645,6 +1123,131 @@ pkv_status launch_decode(const DecodeParams& prm_in, const MergeParams& mp, int 
     return PKV_OK;
 }
 
+
+// ---------------------------------------------------------------------------
+// Host side of the TMA partition pass.
+// ---------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled, fetched through the runtime (no link against the
+// driver library).  nullptr if unavailable.
+EncodeTiledFn encode_tiled() {
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// A pool [NB][16][Hkv][D] viewed as (element, head, row) with boxes of
+// 64 elements x 1 head x 16 rows and the 128-byte swizzle.
+bool make_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int num_kv_heads,
+                   int head_dim, pkv_dtype dtype) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads,
+                                (cuuint64_t)num_blocks * PKV_BLOCK_SIZE};
+    const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2,
+                                   (cuuint64_t)num_kv_heads * head_dim * 2};
+    const cuuint32_t box[3] = {64, 1, PKV_BLOCK_SIZE};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType dt =
+        dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    return enc(map, dt, 3, const_cast<void*>(pool), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+int smem_optin_bytes() {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        return 0;
+    return v;
+}
+
+size_t tma_fixed_smem(int head_dim, int num_seqs) {
+    return 1024 + (size_t)kTmaConsumers * kMaxGroup * (head_dim + 4) * 4 +
+           2 * kTmaConsumers * kMaxGroup * 4 + (2 * kTmaConsumers + 2) * 4 +
+           (size_t)(2 * num_seqs + 1) * 4;
+}
+
+size_t tma_stage_smem(int head_dim) {
+    // one K and one V tile, two mbarriers, a block id and a use count, per consumer
+    return (size_t)kTmaConsumers * (2 * 16 * head_dim * 2 + 2 * 8 + 4 + 4);
+}
+
+// Stages per consumer ring that fit in the opt-in shared memory (0 if < 2).
+int tma_stages(int head_dim, int num_seqs) {
+    const long long room = (long long)smem_optin_bytes() - (long long)tma_fixed_smem(head_dim, num_seqs);
+    const long long ns = room / (long long)tma_stage_smem(head_dim);
+    return ns < 2 ? 0 : (int)std::min<long long>(ns, kTmaMaxStages);
+}
+
+template <typename T, int D>
+pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp, int pb_lower,
+                             int max_blocks, bool need_merge, int passes, int nstages,
+                             cudaStream_t stream) {
+    DecodeParams prm = prm_in;
+    if (passes & kPassPartition) {
+        CUtensorMap tmk, tmv;
+        const pkv_dtype dt = std::is_same<T, __nv_bfloat16>::value ? PKV_BF16 : PKV_F16;
+        if (!make_pool_map(&tmk, prm.k_cache, prm.num_blocks, prm.num_kv_heads, D, dt) ||
+            !make_pool_map(&tmv, prm.v_cache, prm.num_blocks, prm.num_kv_heads, D, dt))
+            return PKV_ERR_CUDA;
+        auto kern = decode_partition_tma_kernel<T, D>;
+        const size_t smem = tma_fixed_smem(D, prm.num_seqs) + (size_t)nstages * tma_stage_smem(D);
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return PKV_ERR_CUDA;
+        const int sms = sm_count();
+        if (sms <= 0) return PKV_ERR_CUDA;
+        const long long parts_upper =
+            (long long)prm.num_seqs * std::max(1, ceil_div(max_blocks, pb_lower));
+        const long long items_upper = parts_upper * prm.num_kv_heads;
+        const int grid = (int)std::max<long long>(1, std::min<long long>(items_upper, sms));
+        prm.target_items = grid * kTmaItemsPerCta;
+        kern<<<grid, kTmaThreads, smem, stream>>>(prm, tmk, tmv, nstages);
+        if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    }
+    if ((passes & kPassMerge) && need_merge) {
+        const int warps = prm.num_seqs * prm.num_q_heads;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)((warps + 3) / 4));
+        cfg.blockDim = dim3(128);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, decode_merge_kernel<T, D>, mp) != cudaSuccess)
+            return PKV_ERR_CUDA;
+    }
+    return PKV_OK;
+}
+
+// Which partition kernel runs: the TMA pipeline unless PKV_DECODE_KERNEL=ldg
+// selects the register-pipelined kernel (kept for comparison).
+bool use_tma_kernel() {
+    static const bool tma = [] {
+        const char* v = std::getenv("PKV_DECODE_KERNEL");
+        return !(v && std::strcmp(v, "ldg") == 0);
+    }();
+    return tma;
+}
+
 pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
                        const int32_t* block_tables, int max_blocks_per_seq,
                        const int32_t* context_lens, int max_context_len, int num_seqs,
@@ -723,6 +1326,21 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
     mp.num_seqs = num_seqs;
     mp.num_q_heads = num_q_heads;
 
+    // the merge kernel is shared; the mode does not change the workspace layout
+    const int nstages = use_tma_kernel() ? tma_stages(head_dim, num_seqs) : 0;
+    if (nstages > 0) {
+        if (dtype == PKV_BF16)
+            return head_dim == 128
+                       ? launch_decode_tma<__nv_bfloat16, 128>(prm, mp, pb_lower, max_blocks,
+                                                               need_merge, passes, nstages, stream)
+                       : launch_decode_tma<__nv_bfloat16, 64>(prm, mp, pb_lower, max_blocks,
+                                                              need_merge, passes, nstages, stream);
+        return head_dim == 128
+                   ? launch_decode_tma<__half, 128>(prm, mp, pb_lower, max_blocks, need_merge,
+                                                    passes, nstages, stream)
+                   : launch_decode_tma<__half, 64>(prm, mp, pb_lower, max_blocks, need_merge,
+                                                   passes, nstages, stream);
+    }
     if (dtype == PKV_BF16) {
         return head_dim == 128 ? launch_decode<__nv_bfloat16, 128>(prm, mp, pb_lower, max_blocks,
                                                                    need_merge, passes, stream)
@@ -865,6 +1483,36 @@ pkv_status paged_kv_decode_step(const void* q, const void* k_new, const void* v_
                                  slot_mapping_out, workspace, workspace_bytes, dtype,
                                  pkv::kPassPartition | pkv::kPassMerge,
                                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status paged_kv_decode_step_layers(const void* q, const void* k_new, const void* v_new,
+                                       void* k_cache, void* v_cache, const int32_t* block_tables,
+                                       int max_blocks_per_seq, const int32_t* context_lens,
+                                       int max_context_len, int num_seqs, int num_q_heads,
+                                       int num_kv_heads, int head_dim, int num_blocks,
+                                       int num_layers, float scale, void* out, void* workspace,
+                                       size_t workspace_bytes, pkv_dtype dtype,
+                                       pkv_stream_t stream) {
+    if (num_layers < 0 || num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        head_dim <= 0 || num_blocks <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (num_layers == 0 || num_seqs == 0) return PKV_OK;
+    if (!q || !k_new || !v_new || !k_cache || !v_cache || !out) return PKV_ERR_INVALID_ARG;
+    const size_t q_layer = (size_t)num_seqs * num_q_heads * head_dim * 2;
+    const size_t new_layer = (size_t)num_seqs * num_kv_heads * head_dim * 2;
+    const size_t pool_layer = (size_t)num_blocks * PKV_BLOCK_SIZE * num_kv_heads * head_dim * 2;
+    for (int l = 0; l < num_layers; ++l) {
+        const pkv_status rc = pkv::decode_step_impl(
+            static_cast<const char*>(q) + l * q_layer, static_cast<const char*>(k_new) + l * new_layer,
+            static_cast<const char*>(v_new) + l * new_layer, static_cast<char*>(k_cache) + l * pool_layer,
+            static_cast<char*>(v_cache) + l * pool_layer, block_tables, max_blocks_per_seq,
+            context_lens, max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
+            num_blocks, scale, static_cast<char*>(out) + l * q_layer, nullptr, workspace,
+            workspace_bytes, dtype, pkv::kPassPartition | pkv::kPassMerge,
+            reinterpret_cast<cudaStream_t>(stream));
+        if (rc != PKV_OK) return rc;
+    }
+    return PKV_OK;
 }
 
 pkv_status paged_kv_decode_step_partition_pass(

@@ -162,8 +162,9 @@ def make_inputs(w: Workload, device="cpu", poison: bool = True,
                 num_layers: Optional[int] = None) -> dict:
     """All inputs of one decode step of ``w`` as torch tensors on ``device``.
 
-    Keys: q [B,Hq,D], k_cache/v_cache [L,NB,16,Hkv,D] (layer-major; L=1 unless
-    ``num_layers``), block_tables [B,MB] int32, context_lens [B] int32,
+    Keys: q [B,Hq,D] (and q_layers [L,B,Hq,D], q_layers[0] = q), k_cache/v_cache
+    [L,NB,16,Hkv,D] (layer-major; L=1 unless ``num_layers``), block_tables [B,MB]
+    int32, context_lens [B] int32,
     k_new/v_new [L,B,Hkv,D] (the token at position len-1), plus host copies of
     lengths and tables and the poison bookkeeping.
     """
@@ -180,6 +181,9 @@ def make_inputs(w: Workload, device="cpu", poison: bool = True,
     v_cache = _randn((L, NB, BLOCK_SIZE, Hkv, D), dt, dev, gen)
     k_new = _randn((L, B, Hkv, D), dt, dev, gen)
     v_new = _randn((L, B, Hkv, D), dt, dev, gen)
+    # per-layer queries for multi-layer steps (layer 0 is q itself)
+    q_layers = torch.cat([q.unsqueeze(0), _randn((L - 1, B, Hq, D), dt, dev, gen)]) if L > 1 \
+        else q.unsqueeze(0)
     if poison:
         nan = float("nan")
         unused_ids = torch.from_numpy(np.flatnonzero(~used)).to(dev)
@@ -202,6 +206,7 @@ def make_inputs(w: Workload, device="cpu", poison: bool = True,
     return {
         "workload": w,
         "q": q,
+        "q_layers": q_layers,
         "k_cache": k_cache,
         "v_cache": v_cache,
         "k_new": k_new,
