@@ -304,6 +304,44 @@ pkv_status paged_kv_decode_step(const void* q, const void* k_new, const void* v_
                                 void* out, int64_t* slot_mapping_out, void* workspace,
                                 size_t workspace_bytes, pkv_dtype dtype, pkv_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * Cascade decode for a shared prefix ([P3] §2: blocks shared between
+ * sequences, prefix cache / parallel sampling).  Precondition: the first
+ * num_prefix_blocks entries of EVERY sequence's block table name the same
+ * physical blocks, and those blocks are full (16 tokens each).  Then the
+ * prefix is attended once for all sharers: a prefix pass puts query vectors
+ * of several sequences side by side against each prefix K/V row, the
+ * partition pass covers each sequence's own blocks after the prefix, and the
+ * merge combines them by log-sum-exp.  A sequence shorter than the prefix
+ * sees only its own length of it.  The result is that of
+ * paged_attention_decode (up to fp32 rounding); only the reads change.
+ * ------------------------------------------------------------------------- */
+size_t paged_attention_cascade_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
+                                               int max_context_len, int num_prefix_blocks);
+
+pkv_status paged_attention_decode_cascade(const void* q, const void* k_cache,
+                                          const void* v_cache, const int32_t* block_tables,
+                                          int max_blocks_per_seq, const int32_t* context_lens,
+                                          int max_context_len, int num_seqs, int num_q_heads,
+                                          int num_kv_heads, int head_dim, int num_blocks,
+                                          int num_prefix_blocks, float scale, void* out,
+                                          void* workspace, size_t workspace_bytes,
+                                          pkv_dtype dtype, pkv_stream_t stream);
+
+/* paged_kv_decode_step with the cascade: every sequence's new token must lie
+ * past the shared prefix (context_len - 1 >= 16 * num_prefix_blocks); a
+ * sequence whose token would land in a shared block is flagged
+ * (PKV_DEV_BAD_LENGTH) and its token is not written. */
+pkv_status paged_kv_decode_step_cascade(const void* q, const void* k_new, const void* v_new,
+                                        void* k_cache, void* v_cache,
+                                        const int32_t* block_tables, int max_blocks_per_seq,
+                                        const int32_t* context_lens, int max_context_len,
+                                        int num_seqs, int num_q_heads, int num_kv_heads,
+                                        int head_dim, int num_blocks, int num_prefix_blocks,
+                                        float scale, void* out, int64_t* slot_mapping_out,
+                                        void* workspace, size_t workspace_bytes, pkv_dtype dtype,
+                                        pkv_stream_t stream);
+
 /* The first of the two kernels of paged_kv_decode_step: the fused write
  * and partition pass.  paged_attention_merge_pass with partition_blocks = 0
  * and the same arguments completes the step. */

@@ -22,6 +22,8 @@ __all__ = [
     "paged_attention_decode_partitioned", "paged_attention_partition_pass",
     "paged_attention_merge_pass", "paged_kv_write_new_tokens", "paged_kv_decode_step",
     "paged_kv_decode_step_partition_pass", "paged_kv_decode_step_layers",
+    "paged_attention_cascade_workspace_bytes", "paged_attention_decode_cascade",
+    "paged_kv_decode_step_cascade", "new_cascade_workspace",
     "paged_kv_decode_step_staging_bytes", "paged_kv_decode_step_host", "pkv_device_status",
     "BlockAllocator", "new_workspace", "paged_kv_block_hash", "paged_kv_copy_blocks", "paged_attention_decode_noalloc",
     "NOALLOC_SCRATCH_BYTES",
@@ -32,7 +34,7 @@ LIB_PATH = os.path.join(_PKG, "libpagedkv.so")
 BLOCK_SIZE = 16
 
 PKV_F16, PKV_BF16 = 0, 1
-DEV_BAD_BLOCK_ID, DEV_BAD_LENGTH, DEV_BAD_SLOT = 0x1, 0x2, 0x4
+DEV_BAD_BLOCK_ID, DEV_BAD_LENGTH, DEV_BAD_SLOT, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "not enough free blocks",
            4: "bad block id", 5: "CUDA error", 6: "workspace missing or too small"}
@@ -78,6 +80,11 @@ _SIGS = {
                                              _i, _i, _i, _f, _vp, _vp, _vp, _sz, _i, _vp], _i),
     "paged_kv_decode_step_layers": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i,
                                      _i, _i, _f, _vp, _vp, _sz, _i, _vp], _i),
+    "paged_attention_cascade_workspace_bytes": ([_i, _i, _i, _i, _i], _sz),
+    "paged_attention_decode_cascade": ([_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i, _i,
+                                        _f, _vp, _vp, _sz, _i, _vp], _i),
+    "paged_kv_decode_step_cascade": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i,
+                                      _i, _i, _f, _vp, _vp, _vp, _sz, _i, _vp], _i),
     "paged_kv_decode_step_staging_bytes": ([_i, _i, _i, _i, _i], _sz),
     "paged_kv_decode_step_host": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp, _i, _i,
                                    _i, _i, _i, _i, _i, _f, _vp, _sz, _i, _vp], _i),
@@ -308,6 +315,47 @@ def paged_kv_decode_step_partition_pass(q, k_new, v_new, k_cache, v_cache, block
     return _decode_step("paged_kv_decode_step_partition_pass", q, k_new, v_new, k_cache,
                         v_cache, block_tables, context_lens, max_context_len, scale, out,
                         workspace, slot_mapping_out, stream)
+
+
+def new_cascade_workspace(num_seqs, num_q_heads, head_dim, max_context_len, num_prefix_blocks,
+                          device) -> torch.Tensor:
+    n = lib().paged_attention_cascade_workspace_bytes(num_seqs, num_q_heads, head_dim,
+                                                      max_context_len, num_prefix_blocks)
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def paged_attention_decode_cascade(q, k_cache, v_cache, block_tables, context_lens,
+                                   max_context_len, num_prefix_blocks, scale, out, workspace,
+                                   stream=None):
+    """Decode attention when every sequence's table starts with the same
+    num_prefix_blocks full blocks: the shared prefix is read once for all."""
+    B, Hq, Hkv, D, NB = _check_decode_shapes(q, k_cache, v_cache, block_tables, context_lens,
+                                             out)
+    _check("paged_attention_decode_cascade", lib().paged_attention_decode_cascade(
+        _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_tables, "block_tables"), block_tables.shape[1],
+        _dev(context_lens, "context_lens"), int(max_context_len), B, Hq, Hkv, D, NB,
+        int(num_prefix_blocks), float(scale), _dev(out, "out"), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _dtype_code(q), _stream(stream)))
+    return out
+
+
+def paged_kv_decode_step_cascade(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,
+                                 max_context_len, num_prefix_blocks, scale, out, workspace,
+                                 slot_mapping_out=None, stream=None):
+    """paged_kv_decode_step with the shared-prefix cascade."""
+    B, Hq, Hkv, D, NB = _check_decode_shapes(q, k_cache, v_cache, block_tables, context_lens,
+                                             out)
+    if tuple(k_new.shape) != (B, Hkv, D) or v_new.shape != k_new.shape:
+        raise ValueError("k_new/v_new must be [num_seqs, num_kv_heads, head_dim]")
+    _check("paged_kv_decode_step_cascade", lib().paged_kv_decode_step_cascade(
+        _dev(q, "q"), _dev(k_new, "k_new"), _dev(v_new, "v_new"), _dev(k_cache, "k_cache"),
+        _dev(v_cache, "v_cache"), _dev(block_tables, "block_tables"), block_tables.shape[1],
+        _dev(context_lens, "context_lens"), int(max_context_len), B, Hq, Hkv, D, NB,
+        int(num_prefix_blocks), float(scale), _dev(out, "out"),
+        _opt(slot_mapping_out, "slot_mapping_out"), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _dtype_code(q), _stream(stream)))
+    return out
 
 
 def paged_kv_decode_step_layers(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens,

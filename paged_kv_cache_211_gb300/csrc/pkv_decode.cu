@@ -78,9 +78,11 @@ struct WsLayout {
     size_t offsets, m, l, o, total;
 };
 
-WsLayout ws_layout(int num_seqs, int num_q_heads, int head_dim, int max_context_len) {
+WsLayout ws_layout(int num_seqs, int num_q_heads, int head_dim, int max_context_len,
+                   int extra_rows_per_seq = 0) {
     const int mb = ceil_div(std::max(max_context_len, 0), PKV_BLOCK_SIZE);
-    const int parts = std::max(1, ceil_div(mb, min_partition_blocks(max_context_len)));
+    const int parts =
+        std::max(1, ceil_div(mb, min_partition_blocks(max_context_len))) + extra_rows_per_seq;
     const size_t rows = (size_t)num_seqs * parts * num_q_heads;
     WsLayout w;
     w.offsets = 0;
@@ -112,6 +114,8 @@ struct DecodeParams {
     int num_seqs, num_q_heads, num_kv_heads, group;
     int max_blocks_per_seq, num_blocks, len_bound;
     int partition_blocks;      // > 0: fixed partition length (blocks)
+    int skip_blocks;           // cascade: leading shared blocks handled by the prefix pass
+    int prefix_parts;          // cascade: workspace rows per sequence written by the prefix pass
     int min_partition_blocks;  // lower bound of the adaptive choice
     int target_items;
     float scale_log2;          // scale * log2(e): scores live in base 2
@@ -153,9 +157,16 @@ __device__ __forceinline__ int cta_exclusive_scan(int v, int* red, int* total) {
     return before + incl - v;
 }
 
-__device__ __forceinline__ int parts_of(int n, int pb) {
+// Partition-pass items of one sequence.  Normally its blocks in partitions
+// of pb (an empty sequence keeps one empty partition, which writes zeros).
+// In cascade mode the first `skip` blocks belong to the prefix pass, which
+// writes the sequence's first prefix_parts workspace rows; the items cover
+// the remaining blocks only, and may be none.
+__device__ __forceinline__ int item_parts(int n, int pb, int skip, int prefix_parts) {
     const int nblk = (n + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
-    return nblk == 0 ? 1 : (nblk + pb - 1) / pb;  // an empty sequence keeps one (empty) partition
+    if (prefix_parts == 0) return nblk == 0 ? 1 : (nblk + pb - 1) / pb;
+    const int rest = nblk > skip ? nblk - skip : 0;
+    return (rest + pb - 1) / pb;
 }
 
 // Operand registers of one 16-token block for one lane (see the file comment).
@@ -326,6 +337,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
             if (blockIdx.x == 0) atomicOr(p.status, PKV_DEV_BAD_LENGTH);
             n = 0;  // the row is written as zeros
         }
+        // cascade: the step's token must land past the shared prefix
+        if (n > 0 && p.prefix_parts && p.k_new && (n - 1) / PKV_BLOCK_SIZE < p.skip_blocks) {
+            if (blockIdx.x == 0) atomicOr(p.status, PKV_DEV_BAD_LENGTH);
+            if (p.slot_out && blockIdx.x == 0) p.slot_out[s] = -1;
+        }
         sm_len[s] = n;
         if (n == 0 && p.slot_out && blockIdx.x == 0) p.slot_out[s] = -1;  // nothing written
         my_blocks += (n + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
@@ -348,17 +364,18 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
     const int chunk = (B + kThreads - 1) / kThreads;
     const int s_lo = min(B, tid * chunk), s_hi = min(B, s_lo + chunk);
     int mine = 0;
-    for (int s = s_lo; s < s_hi; ++s) mine += parts_of(sm_len[s], PB);
+    for (int s = s_lo; s < s_hi; ++s) mine += item_parts(sm_len[s], PB, p.skip_blocks, p.prefix_parts);
     int total_parts = 0;
     int run = cta_exclusive_scan(mine, red, &total_parts);
     for (int s = s_lo; s < s_hi; ++s) {
         sm_off[s] = run;
-        run += parts_of(sm_len[s], PB);
+        run += item_parts(sm_len[s], PB, p.skip_blocks, p.prefix_parts);
     }
     if (tid == 0) sm_off[B] = total_parts;
     __syncthreads();
     if (blockIdx.x == 0) {
-        for (int s = tid; s <= B; s += kThreads) p.ws_offsets[s] = sm_off[s];
+        // workspace rows of sequence s: its prefix rows, then one per item
+        for (int s = tid; s <= B; s += kThreads) p.ws_offsets[s] = sm_off[s] + p.prefix_parts * s;
     }
 
     const T* __restrict__ q = static_cast<const T*>(p.q);
@@ -378,10 +395,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
         }
         const int s = a;
         const int part = gp - sm_off[s];
-        const int nparts = sm_off[s + 1] - sm_off[s];
+        const int nparts = sm_off[s + 1] - sm_off[s] + p.prefix_parts;  // workspace rows of s
+        const int ws_row = gp + p.prefix_parts * (s + 1);               // this item's row
         const int n = sm_len[s];
         const int nblk = (n + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
-        const int blk_lo = part * PB;
+        const int blk_lo = p.skip_blocks + part * PB;
         const int blk_hi = min(nblk, blk_lo + PB);
 
         // query fragment: column gid of the score MMA is query head h*g + gid
@@ -528,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
                 *reinterpret_cast<uint4*>(static_cast<T*>(p.out) + ((size_t)s * Hq + qh) * D +
                                           d0) = packed;
             } else {
-                const size_t row = (size_t)gp * Hq + qh;
+                const size_t row = (size_t)ws_row * Hq + qh;
                 float* dst = p.ws_o + row * D + d0;
                 *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
                 *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
@@ -560,9 +578,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
 // bounded: on a time-out the kernel sets PKV_DEV_TIMEOUT, stops issuing and
 // waiting, lets every copy it issued land, and returns.
 // ============================================================================
-constexpr int kTmaConsumers = 4;
+constexpr int kTmaConsumers = 8;
 constexpr int kTmaThreads = (kTmaConsumers + 1) * 32;
-constexpr int kTmaItemsPerCta = 8;
+constexpr int kTmaItemsPerCta = 4;
 constexpr int kTmaMaxStages = 8;
 constexpr long long kWaitCycles = 4000000000ll;  // ~2 s at 2 GHz
 
@@ -675,8 +693,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     uint64_t* empty = full + NC * nstages;
     int* stage_id = reinterpret_cast<int*>(empty + NC * nstages);     // block id per slot
     int* last_use = stage_id + NC * nstages;                           // last use issued per slot
-    float* sm_o = reinterpret_cast<float*>(last_use + NC * nstages);   // [NC][8][DP]
-    float* sm_m = sm_o + NC * kMaxGroup * DP;                          // [NC][8]
+    const int g = p.group;
+    float* sm_o = reinterpret_cast<float*>(last_use + NC * nstages);   // [NC][g][DP]
+    float* sm_m = sm_o + NC * g * DP;                                  // [NC][8]
     float* sm_l = sm_m + NC * kMaxGroup;                               // [NC][8]
     int* red = reinterpret_cast<int*>(sm_l + NC * kMaxGroup);          // [NC + 1]
     volatile int* abort_flag = red + NC + 1;
@@ -702,6 +721,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             if (blockIdx.x == 0) atomicOr(p.status, PKV_DEV_BAD_LENGTH);
             n = 0;
         }
+        if (n > 0 && p.prefix_parts && p.k_new && (n - 1) / PKV_BLOCK_SIZE < p.skip_blocks) {
+            if (blockIdx.x == 0) atomicOr(p.status, PKV_DEV_BAD_LENGTH);
+            if (p.slot_out && blockIdx.x == 0) p.slot_out[s] = -1;
+        }
         sm_len[s] = n;
         if (n == 0 && p.slot_out && blockIdx.x == 0) p.slot_out[s] = -1;
         my_blocks += (n + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
@@ -709,8 +732,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     const int total_blocks = cta_sum<NC + 1>(my_blocks, red);
     int PB = p.partition_blocks;
     if (PB <= 0) {
-        const long long want =
-            ((long long)total_blocks * p.num_kv_heads + p.target_items - 1) / p.target_items;
+        // an item covers every KV head of its blocks
+        const long long want = ((long long)total_blocks + p.target_items - 1) / p.target_items;
         const long long lo = p.min_partition_blocks;
         const long long hi = kAdaptiveMaxBlocks > lo ? kAdaptiveMaxBlocks : lo;
         PB = (int)(want < lo ? lo : (want > hi ? hi : want));
@@ -718,75 +741,81 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     const int chunk = (B + kTmaThreads - 1) / kTmaThreads;
     const int s_lo = min(B, tid * chunk), s_hi = min(B, s_lo + chunk);
     int mine = 0;
-    for (int s = s_lo; s < s_hi; ++s) mine += parts_of(sm_len[s], PB);
+    for (int s = s_lo; s < s_hi; ++s) mine += item_parts(sm_len[s], PB, p.skip_blocks, p.prefix_parts);
     int total_parts = 0;
     int run = cta_exclusive_scan<NC + 1>(mine, red, &total_parts);
     for (int s = s_lo; s < s_hi; ++s) {
         sm_off[s] = run;
-        run += parts_of(sm_len[s], PB);
+        run += item_parts(sm_len[s], PB, p.skip_blocks, p.prefix_parts);
     }
     if (tid == 0) sm_off[B] = total_parts;
     __syncthreads();
     if (blockIdx.x == 0) {
-        for (int s = tid; s <= B; s += kTmaThreads) p.ws_offsets[s] = sm_off[s];
+        for (int s = tid; s <= B; s += kTmaThreads)
+            p.ws_offsets[s] = sm_off[s] + p.prefix_parts * s;
     }
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
-    const int Hq = p.num_q_heads, Hkv = p.num_kv_heads, g = p.group;
+    const int Hq = p.num_q_heads, Hkv = p.num_kv_heads;
     const size_t row_stride = (size_t)Hkv * D;
-    const int total_items = total_parts * Hkv;
+    // An item is one partition of one sequence across all KV heads, so a
+    // block's heads (one contiguous run of the pool) are fetched together.
+    // Consumer warp w serves KV head w % Hkv and every CPH-th block of the
+    // item, CPH = NC / Hkv consumers per head.
+    const int total_items = total_parts;
+    const int CPH = NC / Hkv;
     struct Item {
-        int s, h, gp, nparts, n, nblk, lo, hi;
+        int s, gp, nparts, ws_row, n, nblk, lo, hi;
     };
     auto item_of = [&](int item) {
         Item it;
-        it.gp = item / Hkv;
-        it.h = item - it.gp * Hkv;
+        it.gp = item;
         int a = 0, b = B - 1;
         while (a < b) {
             const int mid = (a + b + 1) >> 1;
             if (sm_off[mid] <= it.gp) a = mid; else b = mid - 1;
         }
         it.s = a;
-        it.nparts = sm_off[a + 1] - sm_off[a];
+        it.nparts = sm_off[a + 1] - sm_off[a] + p.prefix_parts;  // workspace rows of s
+        it.ws_row = it.gp + p.prefix_parts * (a + 1);            // this item's row
         it.n = sm_len[a];
         it.nblk = (it.n + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
-        it.lo = (it.gp - sm_off[a]) * PB;
+        it.lo = p.skip_blocks + (it.gp - sm_off[a]) * PB;
         it.hi = min(it.nblk, it.lo + PB);
         return it;
     };
 
     if (warp == NC) {
         // ------------------------------------------------------------ producer
-        // Blocks come in batches from the start of the item, lane t issuing
-        // block jb + t.  Block i of an item belongs to consumer i % NC; its
-        // position in that consumer's ring is the consumer's running count
-        // plus t / NC (batches hold a multiple of NC blocks).  A batch gives
-        // each consumer at most `nstages` blocks, so no lane ever waits for a
-        // slot that another lane of this warp has yet to fill: every wait is
-        // on a consumer warp, never on a diverged lane of this one.
-        static_assert(32 % NC == 0, "consumers must divide the warp");
-        const int batch = min(32, NC * nstages);
+        // Batches of BB blocks x Hkv heads, lane t issuing (block jb + t / Hkv,
+        // head t % Hkv) for consumer h + Hkv * ((block - lo) % CPH).  A batch
+        // gives each consumer at most min(4, nstages) blocks, so no lane ever
+        // waits for a slot another lane of this warp has yet to fill: every
+        // wait is on a consumer warp, never on a diverged lane of this one.
+        const int per = min(4, nstages);
+        const int BB = CPH * per;               // blocks per batch (a multiple of CPH)
         int pc[NC];  // stages issued so far per consumer (same in every lane)
 #pragma unroll
         for (int v = 0; v < NC; ++v) pc[v] = 0;
         for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
             const Item it = item_of(item);
             const int32_t* table = p.block_tables + (size_t)it.s * p.max_blocks_per_seq;
-            for (int jb = it.lo; jb < it.hi; jb += batch) {
-                const int cnt = min(batch, it.hi - jb);
-                if (lane < cnt && !*abort_flag) {
-                    int id = table[jb + lane];
+            for (int jb = it.lo; jb < it.hi; jb += BB) {
+                const int cnt = min(BB, it.hi - jb);   // blocks in this batch
+                const int bi = lane / Hkv;             // this lane's block in the batch
+                const int h = lane - bi * Hkv;         // and KV head
+                if (bi < cnt && !*abort_flag) {
+                    int id = table[jb + bi];
                     if (id < 0 || id >= p.num_blocks) {
-                        atomicOr(p.status, PKV_DEV_BAD_BLOCK_ID);
+                        if (h == 0) atomicOr(p.status, PKV_DEV_BAD_BLOCK_ID);
                         id = -1;  // never read: block 0 is fetched and fully masked
                     }
-                    const int w = lane % NC;
+                    const int w = h + Hkv * (bi % CPH);
                     int base = 0;
 #pragma unroll
                     for (int v = 0; v < NC; ++v)
                         if (v == w) base = pc[v];
-                    const int use = base + lane / NC;
+                    const int use = base + bi / CPH;
                     const int k = w * nstages + use % nstages;
                     if (mbar_wait(&empty[k], ((use / nstages) & 1) ^ 1, abort_flag, p.status)) {
                         stage_id[k] = id;
@@ -796,14 +825,17 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                         const int row = (id < 0 ? 0 : id) * PKV_BLOCK_SIZE;
 #pragma unroll
                         for (int hh = 0; hh < HALVES; ++hh) {
-                            tma_load_rows(st + hh * 2048, &tmap_k, &full[k], hh * 64, it.h, row);
-                            tma_load_rows(st + TILE + hh * 2048, &tmap_v, &full[k], hh * 64,
-                                          it.h, row);
+                            tma_load_rows(st + hh * 2048, &tmap_k, &full[k], hh * 64, h, row);
+                            tma_load_rows(st + TILE + hh * 2048, &tmap_v, &full[k], hh * 64, h,
+                                          row);
                         }
                     }
                 }
 #pragma unroll
-                for (int v = 0; v < NC; ++v) pc[v] += (cnt - v + NC - 1) / NC;
+                for (int v = 0; v < NC; ++v) {
+                    const int sub = v / Hkv;  // blocks of this batch with bi % CPH == sub
+                    pc[v] += cnt > sub ? (cnt - sub + CPH - 1) / CPH : 0;
+                }
                 __syncwarp();
             }
         }
@@ -819,12 +851,13 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 
     // -------------------------------------------------------------- consumers
     const int w = warp;
+    const int h = w % Hkv, sub = w / Hkv;  // this consumer's KV head and block phase
     const int gid = lane >> 2, tig = lane & 3;
     const T* __restrict__ q = static_cast<const T*>(p.q);
     int ncons = 0;  // stages this warp has consumed
     for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
         const Item it = item_of(item);
-        const int s = it.s, h = it.h, n = it.n;
+        const int s = it.s, n = it.n;
         // q fragment: column gid of the score MMA is query head h*g + gid
         uint32_t qf[KS][2];
         {
@@ -848,7 +881,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         T* kbase_w = static_cast<T*>(p.k_cache_w) + (size_t)h * D;
         T* vbase_w = static_cast<T*>(p.v_cache_w) + (size_t)h * D;
 
-        for (int j = it.lo + w; j < it.hi; j += NC, ++ncons) {
+        for (int j = it.lo + sub; j < it.hi; j += CPH, ++ncons) {
             const int k = w * nstages + ncons % nstages;
             const bool ok = mbar_wait(&full[k], (ncons / nstages) & 1, abort_flag, p.status);
             unsigned char* st = ring + (size_t)k * STAGE;
@@ -953,13 +986,18 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             l0 += __shfl_xor_sync(0xffffffffu, l0, off);
             l1 += __shfl_xor_sync(0xffffffffu, l1, off);
         }
-        float* mo = sm_o + w * kMaxGroup * DP;
+        float* mo = sm_o + w * g * DP;  // rows of the g live query heads only
+        const bool live0 = 2 * tig < g, live1 = 2 * tig + 1 < g;
 #pragma unroll
         for (int i = 0; i < KS; ++i) {
-            mo[(2 * tig) * DP + 16 * i + gid] = o[i][0];
-            mo[(2 * tig + 1) * DP + 16 * i + gid] = o[i][1];
-            mo[(2 * tig) * DP + 16 * i + 8 + gid] = o[i][2];
-            mo[(2 * tig + 1) * DP + 16 * i + 8 + gid] = o[i][3];
+            if (live0) {
+                mo[(2 * tig) * DP + 16 * i + gid] = o[i][0];
+                mo[(2 * tig) * DP + 16 * i + 8 + gid] = o[i][2];
+            }
+            if (live1) {
+                mo[(2 * tig + 1) * DP + 16 * i + gid] = o[i][1];
+                mo[(2 * tig + 1) * DP + 16 * i + 8 + gid] = o[i][3];
+            }
         }
         if (gid == 0) {
             sm_m[w * kMaxGroup + 2 * tig] = m0;
@@ -969,25 +1007,27 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         }
         asm volatile("bar.sync 1, %0;\n" ::"r"(NC * 32) : "memory");
         constexpr int SL = D / 8;
-        for (int x = tid; x < g * SL; x += NC * 32) {
-            const int hh = x / SL, d0 = (x - hh * SL) * 8;
+        // one thread per (KV head, query head of its group, 8-wide slice of D),
+        // merging the CPH consumers of that KV head
+        for (int x = tid; x < Hkv * g * SL; x += NC * 32) {
+            const int hk = x / (g * SL);
+            const int hh = (x / SL) % g, d0 = (x % SL) * 8;
             float M = -INFINITY;
-#pragma unroll
-            for (int v = 0; v < NC; ++v) M = fmaxf(M, sm_m[v * kMaxGroup + hh]);
+            for (int c = 0; c < CPH; ++c) M = fmaxf(M, sm_m[(hk + Hkv * c) * kMaxGroup + hh]);
             const float Ms = M == -INFINITY ? 0.f : M;
             float L = 0.f;
             float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int v = 0; v < NC; ++v) {
+            for (int c = 0; c < CPH; ++c) {
+                const int v = hk + Hkv * c;
                 const float e = fast_exp2(sm_m[v * kMaxGroup + hh] - Ms);
                 L += e * sm_l[v * kMaxGroup + hh];
-                const float* src = sm_o + (v * kMaxGroup + hh) * DP + d0;
+                const float* src = sm_o + (v * g + hh) * DP + d0;
                 const float4 u = *reinterpret_cast<const float4*>(src);
                 const float4 u2 = *reinterpret_cast<const float4*>(src + 4);
                 acc[0] += e * u.x; acc[1] += e * u.y; acc[2] += e * u.z; acc[3] += e * u.w;
                 acc[4] += e * u2.x; acc[5] += e * u2.y; acc[6] += e * u2.z; acc[7] += e * u2.w;
             }
-            const int qh = h * g + hh;
+            const int qh = hk * g + hh;
             if (it.nparts == 1) {
                 const float inv = L > 0.f ? 1.f / L : 0.f;
                 uint4 packed;
@@ -998,7 +1038,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                 *reinterpret_cast<uint4*>(static_cast<T*>(p.out) + ((size_t)s * Hq + qh) * D +
                                           d0) = packed;
             } else {
-                const size_t row = (size_t)it.gp * Hq + qh;
+                const size_t row = (size_t)it.ws_row * Hq + qh;
                 float* dst = p.ws_o + row * D + d0;
                 *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
                 *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
@@ -1012,6 +1052,172 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     }
 }
 
+
+// ============================================================================
+// Cascade decode: the prefix pass.
+//
+// When every sequence's first P table entries are the same P full blocks (a
+// shared prompt prefix, "从零手写 vLLM 核心：mini-vllm 项目深度解析" §2: prefix
+// cache / parallel sampling share blocks), the prefix is attended once for
+// all sharers instead of once per sequence.  A warp takes one KV head, one
+// chunk of the prefix and a tile of 8 query vectors of that KV head taken
+// across sequences (column c of the tile is query head c % g of sequence
+// c / g), and runs the same block loop as the partition pass with the 8
+// vectors as the n = 8 side of the MMA: each K/V row read serves 8 query
+// vectors of (for g < 8) several sequences.  Each column is masked by its own
+// sequence's length.  The warp leaves (m, l, o) for its columns in the
+// sequence's workspace row for the chunk; the suffix partitions and the merge
+// pass do the rest.
+// ============================================================================
+constexpr int kPrefixChunkBlocks = 8;
+
+struct PrefixParams {
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* block_tables;  // the prefix is row 0's first prefix_blocks entries
+    const int32_t* context_lens;
+    const int* ws_offsets;        // written by the partition pass before this kernel
+    float* ws_m;
+    float* ws_l;
+    float* ws_o;
+    unsigned int* status;
+    int num_seqs, num_q_heads, num_kv_heads, group, num_blocks, len_bound;
+    int prefix_blocks, prefix_parts;
+    float scale_log2;
+};
+
+template <typename T, int D>
+__global__ void __launch_bounds__(128) decode_prefix_kernel(const PrefixParams p) {
+    using E = Elem<T>;
+    constexpr int KC = BlockFrag<D>::KC;
+    constexpr int VC = BlockFrag<D>::VC;
+    constexpr int NT = D / 16;
+    const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+    const int g = p.group, Hq = p.num_q_heads, Hkv = p.num_kv_heads;
+    const int cols = p.num_seqs * g;
+    const int tiles = (cols + 7) / 8;
+    const int unit = blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (unit >= Hkv * tiles * p.prefix_parts) return;
+    const int chunk = unit % p.prefix_parts;
+    const int tile = (unit / p.prefix_parts) % tiles;
+    const int h = unit / (p.prefix_parts * tiles);
+    const int prefix_tokens = p.prefix_blocks * PKV_BLOCK_SIZE;
+
+    // query fragment: column gid is query vector tile*8 + gid
+    uint4 qf[KC];
+    {
+        const int c = tile * 8 + gid;
+        const bool live = c < cols;
+        const T* qrow = static_cast<const T*>(p.q) +
+                        ((size_t)(live ? c / g : 0) * Hq + (size_t)h * g + (live ? c % g : 0)) * D;
+#pragma unroll
+        for (int j = 0; j < KC; ++j)
+            qf[j] = live ? *reinterpret_cast<const uint4*>(qrow + (4 * j + tig) * 8)
+                         : make_uint4(0u, 0u, 0u, 0u);
+    }
+    // prefix tokens visible to this lane's two score columns 2tig, 2tig+1
+    auto visible = [&](int c) {
+        if (c >= cols) return 0;
+        int n = p.context_lens[c / g];
+        if (n < 0 || n > p.len_bound) n = 0;  // flagged by the partition pass
+        return min(n, prefix_tokens);
+    };
+    const int len0 = visible(tile * 8 + 2 * tig), len1 = visible(tile * 8 + 2 * tig + 1);
+
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float o[NT][4];
+#pragma unroll
+    for (int i = 0; i < NT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    const size_t row_stride = (size_t)Hkv * D;
+    const T* kbase = static_cast<const T*>(p.k_cache) + (size_t)h * D;
+    const T* vbase = static_cast<const T*>(p.v_cache) + (size_t)h * D;
+    const int b_lo = chunk * kPrefixChunkBlocks;
+    const int b_hi = min(p.prefix_blocks, b_lo + kPrefixChunkBlocks);
+    for (int j = b_lo; j < b_hi; ++j) {
+        int id = p.block_tables[j];
+        if (id < 0 || id >= p.num_blocks) {
+            atomicOr(p.status, PKV_DEV_BAD_BLOCK_ID);
+            continue;  // never read
+        }
+        BlockFrag<D> f;
+        fetch_block<T, D>(f, kbase, vbase, id, row_stride, gid, tig, -1, nullptr, nullptr);
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < KC; ++k) {
+            E::mma(sa, f.k[0][k].x, f.k[1][k].x, f.k[0][k].y, f.k[1][k].y, qf[k].x, qf[k].y);
+            E::mma(sb, f.k[0][k].z, f.k[1][k].z, f.k[0][k].w, f.k[1][k].w, qf[k].z, qf[k].w);
+        }
+        float s0 = (sa[0] + sb[0]) * p.scale_log2, s1 = (sa[1] + sb[1]) * p.scale_log2;
+        float s2 = (sa[2] + sb[2]) * p.scale_log2, s3 = (sa[3] + sb[3]) * p.scale_log2;
+        // per-column masks (prefix blocks are full, so V rows are finite data)
+        const int t0 = len0 - j * PKV_BLOCK_SIZE, t1 = len1 - j * PKV_BLOCK_SIZE;
+        if (gid >= t0) s0 = -INFINITY;
+        if (gid >= t1) s1 = -INFINITY;
+        if (gid + 8 >= t0) s2 = -INFINITY;
+        if (gid + 8 >= t1) s3 = -INFINITY;
+        float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float ms0 = mn0 == -INFINITY ? 0.f : mn0;
+        const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float c0 = fast_exp2(m0 - ms0), c1 = fast_exp2(m1 - ms1);
+        const float p0 = fast_exp2(s0 - ms0), p1 = fast_exp2(s1 - ms1);
+        const float p2 = fast_exp2(s2 - ms0), p3 = fast_exp2(s3 - ms1);
+        l0 = l0 * c0 + p0 + p2;
+        l1 = l1 * c1 + p1 + p3;
+        m0 = mn0;
+        m1 = mn1;
+#pragma unroll
+        for (int i = 0; i < NT; ++i) {
+            o[i][0] *= c0;
+            o[i][1] *= c1;
+            o[i][2] *= c0;
+            o[i][3] *= c1;
+        }
+        const uint32_t pt = movmatrix_trans(E::pack(p0, p1));
+        const uint32_t pbt = movmatrix_trans(E::pack(p2, p3));
+#pragma unroll
+        for (int i = 0; i < NT; ++i) {
+            const int c = i >> 2, w = i & 3;
+            const uint32_t x0 = word_of(f.v[c][0], w), x1 = word_of(f.v[c][1], w);
+            const uint32_t x2 = word_of(f.v[c][2], w), x3 = word_of(f.v[c][3], w);
+            E::mma(o[i], __byte_perm(x0, x1, 0x5410), __byte_perm(x0, x1, 0x7632),
+                   __byte_perm(x2, x3, 0x5410), __byte_perm(x2, x3, 0x7632), pt, pbt);
+        }
+    }
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+    // this lane holds columns 2tig, 2tig+1 at d = 8*(gid + 8c) + e
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const int c = tile * 8 + 2 * tig + half;
+        if (c >= cols) continue;
+        const int sq = c / g, qh = h * g + c % g;
+        const size_t row = (size_t)(p.ws_offsets[sq] + chunk) * Hq + qh;
+#pragma unroll
+        for (int cc = 0; cc < VC; ++cc) {
+            float* dst = p.ws_o + row * D + 8 * (gid + 8 * cc);
+            const int e = half;
+            *reinterpret_cast<float4*>(dst) = make_float4(
+                o[4 * cc][e], o[4 * cc][e + 2], o[4 * cc + 1][e], o[4 * cc + 1][e + 2]);
+            *reinterpret_cast<float4*>(dst + 4) = make_float4(
+                o[4 * cc + 2][e], o[4 * cc + 2][e + 2], o[4 * cc + 3][e], o[4 * cc + 3][e + 2]);
+        }
+        if (gid == 0) {
+            p.ws_m[row] = half ? m1 : m0;
+            p.ws_l[row] = half ? l1 : l0;
+        }
+    }
+}
+
 struct MergeParams {
     const int* ws_offsets;
     const float* ws_m;
@@ -1019,6 +1225,7 @@ struct MergeParams {
     const float* ws_o;
     void* out;
     int num_seqs, num_q_heads;
+    int min_rows;  // merge sequences with at least this many workspace rows
 };
 
 // Log-sum-exp merge of a sequence's partitions, one warp per (sequence, query head):
@@ -1035,7 +1242,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const MergeParams p) 
     const int s = wg / Hq, qh = wg - s * Hq;
     const int off = p.ws_offsets[s];
     const int np = p.ws_offsets[s + 1] - off;
-    if (np <= 1) return;  // written by the partition kernel
+    if (np < p.min_rows) return;  // a one-row sequence was written by the partition pass
     float M = -INFINITY;
     for (int i = lane; i < np; i += 32) M = fmaxf(M, p.ws_m[(size_t)(off + i) * Hq + qh]);
 #pragma unroll
@@ -1176,8 +1383,8 @@ int smem_optin_bytes() {
     return v;
 }
 
-size_t tma_fixed_smem(int head_dim, int num_seqs) {
-    return 1024 + (size_t)kTmaConsumers * kMaxGroup * (head_dim + 4) * 4 +
+size_t tma_fixed_smem(int head_dim, int num_seqs, int group) {
+    return 1024 + (size_t)kTmaConsumers * group * (head_dim + 4) * 4 +
            2 * kTmaConsumers * kMaxGroup * 4 + (2 * kTmaConsumers + 2) * 4 +
            (size_t)(2 * num_seqs + 1) * 4;
 }
@@ -1188,8 +1395,9 @@ size_t tma_stage_smem(int head_dim) {
 }
 
 // Stages per consumer ring that fit in the opt-in shared memory (0 if < 2).
-int tma_stages(int head_dim, int num_seqs) {
-    const long long room = (long long)smem_optin_bytes() - (long long)tma_fixed_smem(head_dim, num_seqs);
+int tma_stages(int head_dim, int num_seqs, int group) {
+    const long long room =
+        (long long)smem_optin_bytes() - (long long)tma_fixed_smem(head_dim, num_seqs, group);
     const long long ns = room / (long long)tma_stage_smem(head_dim);
     return ns < 2 ? 0 : (int)std::min<long long>(ns, kTmaMaxStages);
 }
@@ -1206,15 +1414,16 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp, 
             !make_pool_map(&tmv, prm.v_cache, prm.num_blocks, prm.num_kv_heads, D, dt))
             return PKV_ERR_CUDA;
         auto kern = decode_partition_tma_kernel<T, D>;
-        const size_t smem = tma_fixed_smem(D, prm.num_seqs) + (size_t)nstages * tma_stage_smem(D);
+        const size_t smem =
+            tma_fixed_smem(D, prm.num_seqs, prm.group) + (size_t)nstages * tma_stage_smem(D);
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
             return PKV_ERR_CUDA;
         const int sms = sm_count();
         if (sms <= 0) return PKV_ERR_CUDA;
-        const long long parts_upper =
+        // one item per partition, covering every KV head
+        const long long items_upper =
             (long long)prm.num_seqs * std::max(1, ceil_div(max_blocks, pb_lower));
-        const long long items_upper = parts_upper * prm.num_kv_heads;
         const int grid = (int)std::max<long long>(1, std::min<long long>(items_upper, sms));
         prm.target_items = grid * kTmaItemsPerCta;
         kern<<<grid, kTmaThreads, smem, stream>>>(prm, tmk, tmv, nstages);
@@ -1255,7 +1464,8 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
                        float scale, void* out, void* workspace, size_t workspace_bytes,
                        int partition_blocks, pkv_dtype dtype, int passes,
                        cudaStream_t stream, const void* k_new = nullptr,
-                       const void* v_new = nullptr, int64_t* slot_out = nullptr) {
+                       const void* v_new = nullptr, int64_t* slot_out = nullptr,
+                       int prefix_blocks = 0) {
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
         max_blocks_per_seq <= 0 || num_blocks <= 0 || max_context_len < 0 ||
         partition_blocks < 0)
@@ -1271,7 +1481,10 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
         return PKV_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
         return PKV_ERR_INVALID_ARG;
-    const WsLayout ws = ws_layout(num_seqs, num_q_heads, head_dim, max_context_len);
+    if (prefix_blocks < 0 || prefix_blocks > max_blocks_per_seq) return PKV_ERR_INVALID_ARG;
+    const int prefix_parts = ceil_div(prefix_blocks, kPrefixChunkBlocks);  // 0 unless cascade
+    const WsLayout ws =
+        ws_layout(num_seqs, num_q_heads, head_dim, max_context_len, prefix_parts);
     if (!workspace || workspace_bytes < ws.total ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return PKV_ERR_WORKSPACE;
@@ -1285,7 +1498,8 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
     const int max_blocks = ceil_div(len_bound, PKV_BLOCK_SIZE);
     const int pb_lower =
         partition_blocks > 0 ? partition_blocks : std::max(min_pb, kAdaptiveMinBlocks);
-    const bool need_merge = max_blocks > pb_lower;
+    // a cascade merges every sequence (its prefix rows plus its suffix items)
+    const bool need_merge = prefix_parts > 0 || max_blocks > pb_lower;
 
     char* wsb = static_cast<char*>(workspace);
     DecodeParams prm;
@@ -1313,6 +1527,8 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
     prm.num_blocks = num_blocks;
     prm.len_bound = len_bound;
     prm.partition_blocks = partition_blocks;
+    prm.skip_blocks = prefix_blocks;
+    prm.prefix_parts = prefix_parts;
     prm.min_partition_blocks = pb_lower;
     prm.target_items = 0;
     prm.scale_log2 = scale * kLog2e;
@@ -1325,33 +1541,79 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
     mp.out = out;
     mp.num_seqs = num_seqs;
     mp.num_q_heads = num_q_heads;
+    mp.min_rows = prefix_parts > 0 ? 1 : 2;
 
-    // the merge kernel is shared; the mode does not change the workspace layout
-    const int nstages = use_tma_kernel() ? tma_stages(head_dim, num_seqs) : 0;
-    if (nstages > 0) {
-        if (dtype == PKV_BF16)
+    // partition kernel (TMA pipeline or register pipeline) and merge kernel
+    // the TMA kernel maps its 8 consumer warps onto the KV heads (Hkv must divide 8)
+    const int nstages = use_tma_kernel() && kTmaConsumers % num_kv_heads == 0
+                            ? tma_stages(head_dim, num_seqs, g)
+                            : 0;
+    const int grid_blocks = std::max(1, max_blocks - prefix_blocks);  // blocks items can cover
+    auto run = [&](int pass_mask) -> pkv_status {
+        if (nstages > 0) {
+            if (dtype == PKV_BF16)
+                return head_dim == 128
+                           ? launch_decode_tma<__nv_bfloat16, 128>(prm, mp, pb_lower, grid_blocks,
+                                                                   need_merge, pass_mask, nstages,
+                                                                   stream)
+                           : launch_decode_tma<__nv_bfloat16, 64>(prm, mp, pb_lower, grid_blocks,
+                                                                  need_merge, pass_mask, nstages,
+                                                                  stream);
             return head_dim == 128
-                       ? launch_decode_tma<__nv_bfloat16, 128>(prm, mp, pb_lower, max_blocks,
-                                                               need_merge, passes, nstages, stream)
-                       : launch_decode_tma<__nv_bfloat16, 64>(prm, mp, pb_lower, max_blocks,
-                                                              need_merge, passes, nstages, stream);
-        return head_dim == 128
-                   ? launch_decode_tma<__half, 128>(prm, mp, pb_lower, max_blocks, need_merge,
-                                                    passes, nstages, stream)
-                   : launch_decode_tma<__half, 64>(prm, mp, pb_lower, max_blocks, need_merge,
-                                                   passes, nstages, stream);
+                       ? launch_decode_tma<__half, 128>(prm, mp, pb_lower, grid_blocks, need_merge,
+                                                        pass_mask, nstages, stream)
+                       : launch_decode_tma<__half, 64>(prm, mp, pb_lower, grid_blocks, need_merge,
+                                                       pass_mask, nstages, stream);
+        }
+        if (dtype == PKV_BF16)
+            return head_dim == 128 ? launch_decode<__nv_bfloat16, 128>(
+                                         prm, mp, pb_lower, grid_blocks, need_merge, pass_mask, stream)
+                                   : launch_decode<__nv_bfloat16, 64>(
+                                         prm, mp, pb_lower, grid_blocks, need_merge, pass_mask, stream);
+        return head_dim == 128 ? launch_decode<__half, 128>(prm, mp, pb_lower, grid_blocks,
+                                                            need_merge, pass_mask, stream)
+                               : launch_decode<__half, 64>(prm, mp, pb_lower, grid_blocks,
+                                                           need_merge, pass_mask, stream);
+    };
+    if (prefix_parts == 0) return run(passes);
+
+    // cascade: suffix partitions, then the shared prefix for all sharers, then the merge
+    if (passes & kPassPartition) {
+        pkv_status rc = run(kPassPartition);
+        if (rc != PKV_OK) return rc;
+        PrefixParams pp;
+        pp.q = q;
+        pp.k_cache = k_cache;
+        pp.v_cache = v_cache;
+        pp.block_tables = block_tables;
+        pp.context_lens = context_lens;
+        pp.ws_offsets = prm.ws_offsets;
+        pp.ws_m = prm.ws_m;
+        pp.ws_l = prm.ws_l;
+        pp.ws_o = prm.ws_o;
+        pp.status = status;
+        pp.num_seqs = num_seqs;
+        pp.num_q_heads = num_q_heads;
+        pp.num_kv_heads = num_kv_heads;
+        pp.group = g;
+        pp.num_blocks = num_blocks;
+        pp.len_bound = len_bound;
+        pp.prefix_blocks = prefix_blocks;
+        pp.prefix_parts = prefix_parts;
+        pp.scale_log2 = prm.scale_log2;
+        const long long units =
+            (long long)num_kv_heads * ((num_seqs * g + 7) / 8) * prefix_parts;
+        const unsigned grid = (unsigned)((units + 3) / 4);
+        if (dtype == PKV_BF16) {
+            if (head_dim == 128) decode_prefix_kernel<__nv_bfloat16, 128><<<grid, 128, 0, stream>>>(pp);
+            else decode_prefix_kernel<__nv_bfloat16, 64><<<grid, 128, 0, stream>>>(pp);
+        } else {
+            if (head_dim == 128) decode_prefix_kernel<__half, 128><<<grid, 128, 0, stream>>>(pp);
+            else decode_prefix_kernel<__half, 64><<<grid, 128, 0, stream>>>(pp);
+        }
+        if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
     }
-    if (dtype == PKV_BF16) {
-        return head_dim == 128 ? launch_decode<__nv_bfloat16, 128>(prm, mp, pb_lower, max_blocks,
-                                                                   need_merge, passes, stream)
-                               : launch_decode<__nv_bfloat16, 64>(prm, mp, pb_lower, max_blocks,
-                                                                  need_merge, passes, stream);
-    }
-    return head_dim == 128
-               ? launch_decode<__half, 128>(prm, mp, pb_lower, max_blocks, need_merge, passes,
-                                            stream)
-               : launch_decode<__half, 64>(prm, mp, pb_lower, max_blocks, need_merge, passes,
-                                           stream);
+    return (passes & kPassMerge) ? run(kPassMerge) : PKV_OK;
 }
 
 }  // namespace
@@ -1367,6 +1629,33 @@ size_t paged_attention_workspace_bytes(int num_seqs, int num_q_heads, int head_d
                                        int max_context_len) {
     if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len < 0) return 0;
     return pkv::ws_layout(num_seqs, num_q_heads, head_dim, max_context_len).total;
+}
+
+size_t paged_attention_cascade_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
+                                               int max_context_len, int num_prefix_blocks) {
+    if (num_seqs <= 0 || num_q_heads <= 0 || head_dim <= 0 || max_context_len < 0 ||
+        num_prefix_blocks < 0)
+        return 0;
+    return pkv::ws_layout(num_seqs, num_q_heads, head_dim, max_context_len,
+                          pkv::ceil_div(num_prefix_blocks, pkv::kPrefixChunkBlocks))
+        .total;
+}
+
+pkv_status paged_attention_decode_cascade(const void* q, const void* k_cache,
+                                          const void* v_cache, const int32_t* block_tables,
+                                          int max_blocks_per_seq, const int32_t* context_lens,
+                                          int max_context_len, int num_seqs, int num_q_heads,
+                                          int num_kv_heads, int head_dim, int num_blocks,
+                                          int num_prefix_blocks, float scale, void* out,
+                                          void* workspace, size_t workspace_bytes,
+                                          pkv_dtype dtype, pkv_stream_t stream) {
+    if (num_prefix_blocks <= 0) return PKV_ERR_INVALID_ARG;
+    return pkv::decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                            max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                            num_blocks, scale, out, workspace, workspace_bytes, 0, dtype,
+                            pkv::kPassPartition | pkv::kPassMerge,
+                            reinterpret_cast<cudaStream_t>(stream), nullptr, nullptr, nullptr,
+                            num_prefix_blocks);
 }
 
 pkv_status paged_attention_decode(const void* q, const void* k_cache, const void* v_cache,
@@ -1453,7 +1742,7 @@ pkv_status decode_step_impl(const void* q, const void* k_new, const void* v_new,
                             int num_q_heads, int num_kv_heads, int head_dim, int num_blocks,
                             float scale, void* out, int64_t* slot_mapping_out, void* workspace,
                             size_t workspace_bytes, pkv_dtype dtype, int passes,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, int prefix_blocks = 0) {
     if (num_seqs < 0 || num_kv_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0 ||
         num_blocks <= 0)
         return PKV_ERR_INVALID_ARG;
@@ -1462,7 +1751,7 @@ pkv_status decode_step_impl(const void* q, const void* k_new, const void* v_new,
     return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                        max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
                        num_blocks, scale, out, workspace, workspace_bytes, 0, dtype, passes,
-                       stream, k_new, v_new, slot_mapping_out);
+                       stream, k_new, v_new, slot_mapping_out, prefix_blocks);
 }
 
 }  // namespace
@@ -1513,6 +1802,24 @@ pkv_status paged_kv_decode_step_layers(const void* q, const void* k_new, const v
         if (rc != PKV_OK) return rc;
     }
     return PKV_OK;
+}
+
+pkv_status paged_kv_decode_step_cascade(const void* q, const void* k_new, const void* v_new,
+                                        void* k_cache, void* v_cache,
+                                        const int32_t* block_tables, int max_blocks_per_seq,
+                                        const int32_t* context_lens, int max_context_len,
+                                        int num_seqs, int num_q_heads, int num_kv_heads,
+                                        int head_dim, int num_blocks, int num_prefix_blocks,
+                                        float scale, void* out, int64_t* slot_mapping_out,
+                                        void* workspace, size_t workspace_bytes, pkv_dtype dtype,
+                                        pkv_stream_t stream) {
+    if (num_prefix_blocks <= 0) return PKV_ERR_INVALID_ARG;
+    return pkv::decode_step_impl(q, k_new, v_new, k_cache, v_cache, block_tables,
+                                 max_blocks_per_seq, context_lens, max_context_len, num_seqs,
+                                 num_q_heads, num_kv_heads, head_dim, num_blocks, scale, out,
+                                 slot_mapping_out, workspace, workspace_bytes, dtype,
+                                 pkv::kPassPartition | pkv::kPassMerge,
+                                 reinterpret_cast<cudaStream_t>(stream), num_prefix_blocks);
 }
 
 pkv_status paged_kv_decode_step_partition_pass(
