@@ -38,7 +38,8 @@ FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_partition_llama7b_long.md")
 KERNEL_SOURCES = ["paged_kv_cache_211_gb300/csrc/pkv_decode.cu",
-                  "paged_kv_cache_211_gb300/csrc/pkv_internal.cuh"]
+                  "paged_kv_cache_211_gb300/csrc/pkv_internal.cuh",
+                  "paged_kv_cache_211_gb300/csrc/pkv_tma.cuh"]
 
 
 def parse_args():
@@ -50,6 +51,8 @@ def parse_args():
     ap.add_argument("--workload", default="llama7b_long")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer loop")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill", action="store_true",
+                    help="time chunked-prefill attention instead of the decode step")
     ap.add_argument("--pool-blocks", type=int, default=0,
                     help="shrink the physical pool (for small profiler captures)")
     return ap.parse_args()
@@ -480,6 +483,56 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
+def run_prefill(args):
+    """Chunked-prefill attention on the Llama-7B-shaped prompt batch: TFLOP/s."""
+    import paged_kv_cache_211_gb300 as pkv
+    from paged_kv_cache_211_gb300 import workloads as wl
+
+    dev = torch.device("cuda", 0)
+    w = wl.WORKLOADS["llama7b_prefill"]
+    inp = wl.make_prefill_inputs(w, chunk=2048, device=dev)
+    kc, vc = inp["k_cache"][0], inp["v_cache"][0]
+    pkv.reshape_and_cache(inp["k_rows"], inp["v_rows"], kc, vc, inp["row_slots"])
+    q, out = inp["q_rows"], torch.empty_like(inp["q_rows"])
+    lens = inp["context_lens_host"]
+    qlens = np.diff(inp["cu_q_lens_host"])
+    flops = wl.prefill_flops(lens, qlens, w.num_q_heads, w.head_dim)
+
+    def step():
+        pkv.paged_attention_prefill(q, kc, vc, inp["block_tables"], inp["context_lens"],
+                                    inp["cu_q_lens"], inp["max_q_len"], w.scale, out)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    K = max(1, min(args.steps, 200))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    if pkv.pkv_device_status() != 0:
+        raise SystemExit("device status flags set during the benchmark")
+    ms = e0.elapsed_time(e1) / K
+    peak = None
+    try:
+        peak = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"])
+    except Exception:
+        pass
+    tf = flops / (ms / 1e3) / 1e12
+    print(json.dumps({
+        "metric": "chunked-prefill attention TFLOP/s (causal, paged cache)", "value": round(tf, 2),
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "dtype": w.dtype,
+        "data": "synthetic", "config": {"workload": w.name, "description": w.description,
+                                        "query_rows": int(qlens.sum()), "flops": flops},
+        "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(tf / peak, 4) if peak else None,
+                     "note": "mma.sync m16n8k16 against the measured cuBLAS bf16 peak"},
+        "gpu_launches": K}), flush=True)
+
+
 def run_reference(args):
     """The CPU oracle, as it stands, on a bounded sample of the same workload per step."""
     from paged_kv_cache_211_gb300 import workloads as wl
@@ -550,6 +603,8 @@ def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.prefill:
+        run_prefill(args)
     else:
         run_ours(args)
 

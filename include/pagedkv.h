@@ -342,6 +342,26 @@ pkv_status paged_kv_decode_step_cascade(const void* q, const void* k_new, const 
                                         void* workspace, size_t workspace_bytes, pkv_dtype dtype,
                                         pkv_stream_t stream);
 
+/* Chunked-prefill attention over the paged cache ([P2] 使用教程 step 4 and
+ * 核心亮点: a self-written FlashAttention serves the prefill stage; [P3]
+ * §关键工程决策 item 2: prefill chunks are batched with decode).  Sequence s
+ * contributes q_len[s] = cu_q_lens[s+1] - cu_q_lens[s] query rows (packed:
+ * rows cu_q_lens[s] .. cu_q_lens[s+1] of q and out, [rows][num_q_heads]
+ * [head_dim]) at positions context_lens[s] - q_len[s] .. context_lens[s] - 1.
+ * Their K/V must already be in the cache (reshape_and_cache with their
+ * slots).  The query at position p attends to tokens 0..p of its sequence
+ * (causal), query head i reading KV head i / (num_q_heads / num_kv_heads).
+ * cu_q_lens: [num_seqs + 1] int32, device; max_q_len: host bound on every
+ * q_len.  A sequence with q_len > context_len is flagged (PKV_DEV_BAD_LENGTH)
+ * and skipped.  Supported: head_dim 64 or 128, num_q_heads / num_kv_heads
+ * up to 16. */
+pkv_status paged_attention_prefill(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, int max_blocks_per_seq,
+                                   const int32_t* context_lens, const int32_t* cu_q_lens,
+                                   int num_seqs, int max_q_len, int num_q_heads,
+                                   int num_kv_heads, int head_dim, int num_blocks, float scale,
+                                   void* out, pkv_dtype dtype, pkv_stream_t stream);
+
 /* The first of the two kernels of paged_kv_decode_step: the fused write
  * and partition pass.  paged_attention_merge_pass with partition_blocks = 0
  * and the same arguments completes the step. */

@@ -18,6 +18,9 @@ Functions and the passages they follow (page title, section):
 * ``decode_f16`` / ``decode_bf16`` -- the IEEE binary16 and bfloat16 format
   definitions.
 * ``copy_blocks`` -- the device half of copy-on-write (whole-block copies).
+* ``prefill_attention`` -- "MinivLLM" 使用教程 step 4 / 核心亮点 (a self-written
+  FlashAttention for the prefill stage) over the paged cache: packed query
+  chunks, causal within each sequence.
 * ``prefix_cache_model.PrefixCacheModel`` -- the allocator's policy (free
   stack, prefix cache by hash, LRU of released cached blocks, copy-on-write,
   rollback) in plain Python.
@@ -96,6 +99,11 @@ class Oracle:
         lib.pko_copy_blocks.argtypes = [c_u16p, c_u16p, c_i32p, c_i32p, ctypes.c_int,
                                         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
         lib.pko_copy_blocks.restype = ctypes.c_int
+        lib.pko_prefill_attention.argtypes = [ctypes.c_int, c_u16p, c_u16p, c_u16p, c_i32p,
+                                              ctypes.c_int, c_i32p, c_i32p, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_int, ctypes.c_double, c_f64p]
+        lib.pko_prefill_attention.restype = ctypes.c_int
         self.lib = lib
         self.path = so_path
 
@@ -154,6 +162,25 @@ class Oracle:
         if rc != 0:
             raise ValueError(f"oracle copy_blocks failed with code {rc}")
         return kc, vc
+
+    def prefill_attention(self, dtype: int, q, k_cache, v_cache, block_tables, context_lens,
+                          cu_q_lens, scale: float):
+        """fp64 causal attention of packed query rows [R, Hq, D] over the paged cache."""
+        qb, kc, vc = _bits(q), _bits(k_cache), _bits(v_cache)
+        bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+        cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+        cu = np.ascontiguousarray(cu_q_lens, dtype=np.int32)
+        r, hq, d = qb.shape
+        nb, bs, hkv, _ = kc.shape
+        out = np.zeros((r, hq, d), np.float64)
+        rc = self.lib.pko_prefill_attention(
+            dtype, _ptr(qb, ctypes.c_uint16), _ptr(kc, ctypes.c_uint16),
+            _ptr(vc, ctypes.c_uint16), _ptr(bt, ctypes.c_int32), bt.shape[1],
+            _ptr(cl, ctypes.c_int32), _ptr(cu, ctypes.c_int32), cl.shape[0], hq, hkv, d, nb, bs,
+            float(scale), _ptr(out, ctypes.c_double))
+        if rc != 0:
+            raise ValueError(f"oracle prefill_attention failed with code {rc}")
+        return out
 
     def decode_attention(self, dtype: int, q, k_cache, v_cache, block_tables, context_lens,
                          scale: float, return_weights: bool = False):
@@ -226,6 +253,12 @@ def reshape_and_cache(k_new, v_new, k_cache, v_cache, slots):
 
 def copy_blocks(k_cache, v_cache, src, dst):
     return default().copy_blocks(k_cache, v_cache, src, dst)
+
+
+def prefill_attention(dtype: int, q, k_cache, v_cache, block_tables, context_lens, cu_q_lens,
+                      scale: float):
+    return default().prefill_attention(dtype, q, k_cache, v_cache, block_tables, context_lens,
+                                       cu_q_lens, scale)
 
 
 def decode_attention(dtype: int, q, k_cache, v_cache, block_tables, context_lens, scale: float,

@@ -236,3 +236,63 @@ int pko_copy_blocks(uint16_t* k_cache, uint16_t* v_cache, const int32_t* src,
     }
     return PKO_OK;
 }
+
+/* Chunked-prefill attention in fp64 (the prefill stage's attention, here over
+ * the paged cache): sequence s contributes q_len[s] query rows, packed from
+ * row cu_q_lens[s], at positions context_lens[s] - q_len[s] .. context_lens[s]
+ * - 1; their own K/V are already in the cache.  The query at position p
+ * attends to the tokens 0..p of its sequence (causal), each head as in
+ * decode attention.  q and out are [num_rows][num_q_heads][head_dim]. */
+int pko_prefill_attention(int dtype, const uint16_t* q, const uint16_t* k_cache,
+                          const uint16_t* v_cache, const int32_t* block_tables,
+                          int max_blocks_per_seq, const int32_t* context_lens,
+                          const int32_t* cu_q_lens, int num_seqs, int num_q_heads,
+                          int num_kv_heads, int head_dim, int num_blocks, int block_size,
+                          double scale, double* out) {
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !cu_q_lens || !out)
+        return PKO_ERR_ARG;
+    if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0) return PKO_ERR_ARG;
+    int group = num_q_heads / num_kv_heads;
+    int max_len = max_blocks_per_seq * block_size;
+    double* z = (double*)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+    double* qd = (double*)malloc(sizeof(double) * (size_t)head_dim);
+    if (!z || !qd) { free(z); free(qd); return PKO_ERR_NOMEM; }
+    int rc = PKO_OK;
+    for (int s = 0; s < num_seqs && rc == PKO_OK; ++s) {
+        int n = context_lens[s];
+        int rows = cu_q_lens[s + 1] - cu_q_lens[s];
+        if (n < rows || n > max_len || rows < 0) { rc = PKO_ERR_ARG; break; }
+        for (int r = 0; r < rows && rc == PKO_OK; ++r) {
+            int p = n - rows + r;           /* this query's position */
+            int64_t qrow = (int64_t)cu_q_lens[s] + r;
+            for (int i = 0; i < num_q_heads; ++i) {
+                double* o = out + (qrow * num_q_heads + i) * head_dim;
+                const uint16_t* qi = q + (qrow * num_q_heads + i) * head_dim;
+                int h = i / group;
+                for (int d = 0; d < head_dim; ++d) { qd[d] = decode(dtype, qi[d]); o[d] = 0.0; }
+                double zmax = -INFINITY;
+                for (int t = 0; t <= p; ++t) {
+                    int32_t b = block_tables[(int64_t)s * max_blocks_per_seq + t / block_size];
+                    if (b < 0 || b >= num_blocks) { rc = PKO_ERR_BLOCK_ID; break; }
+                    int64_t row = (((int64_t)b * block_size + t % block_size) * num_kv_heads + h) * head_dim;
+                    double acc = 0.0;
+                    for (int d = 0; d < head_dim; ++d) acc += qd[d] * decode(dtype, k_cache[row + d]);
+                    z[t] = scale * acc;
+                    if (z[t] > zmax) zmax = z[t];
+                }
+                if (rc != PKO_OK) break;
+                double denom = 0.0;
+                for (int t = 0; t <= p; ++t) { z[t] = exp(z[t] - zmax); denom += z[t]; }
+                for (int t = 0; t <= p; ++t) {
+                    int32_t b = block_tables[(int64_t)s * max_blocks_per_seq + t / block_size];
+                    int64_t row = (((int64_t)b * block_size + t % block_size) * num_kv_heads + h) * head_dim;
+                    double w = z[t] / denom;
+                    for (int d = 0; d < head_dim; ++d) o[d] += w * decode(dtype, v_cache[row + d]);
+                }
+            }
+        }
+    }
+    free(z);
+    free(qd);
+    return rc;
+}

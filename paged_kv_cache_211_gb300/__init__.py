@@ -23,7 +23,7 @@ __all__ = [
     "paged_attention_merge_pass", "paged_kv_write_new_tokens", "paged_kv_decode_step",
     "paged_kv_decode_step_partition_pass", "paged_kv_decode_step_layers",
     "paged_attention_cascade_workspace_bytes", "paged_attention_decode_cascade",
-    "paged_kv_decode_step_cascade", "new_cascade_workspace",
+    "paged_kv_decode_step_cascade", "new_cascade_workspace", "paged_attention_prefill",
     "paged_kv_decode_step_staging_bytes", "paged_kv_decode_step_host", "pkv_device_status",
     "BlockAllocator", "new_workspace", "paged_kv_block_hash", "paged_kv_copy_blocks", "paged_attention_decode_noalloc",
     "NOALLOC_SCRATCH_BYTES",
@@ -85,6 +85,8 @@ _SIGS = {
                                         _f, _vp, _vp, _sz, _i, _vp], _i),
     "paged_kv_decode_step_cascade": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i,
                                       _i, _i, _f, _vp, _vp, _vp, _sz, _i, _vp], _i),
+    "paged_attention_prefill": ([_vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _f,
+                                 _vp, _i, _vp], _i),
     "paged_kv_decode_step_staging_bytes": ([_i, _i, _i, _i, _i], _sz),
     "paged_kv_decode_step_host": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp, _i, _i,
                                    _i, _i, _i, _i, _i, _f, _vp, _sz, _i, _vp], _i),
@@ -355,6 +357,26 @@ def paged_kv_decode_step_cascade(q, k_new, v_new, k_cache, v_cache, block_tables
         int(num_prefix_blocks), float(scale), _dev(out, "out"),
         _opt(slot_mapping_out, "slot_mapping_out"), _dev(workspace, "workspace"),
         workspace.numel() * workspace.element_size(), _dtype_code(q), _stream(stream)))
+    return out
+
+
+def paged_attention_prefill(q, k_cache, v_cache, block_tables, context_lens, cu_q_lens,
+                            max_q_len, scale, out, stream=None):
+    """Causal attention of packed query chunks [rows, Hq, D] over the paged cache."""
+    R, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_cache.shape
+    if bs != BLOCK_SIZE or D2 != D or v_cache.shape != k_cache.shape:
+        raise ValueError("pool shape must be [num_blocks, 16, num_kv_heads, head_dim]")
+    B = context_lens.numel()
+    if cu_q_lens.dtype != torch.int32 or cu_q_lens.numel() != B + 1:
+        raise ValueError("cu_q_lens must be int32 [num_seqs + 1]")
+    if out.shape != q.shape or out.dtype != q.dtype or k_cache.dtype != q.dtype:
+        raise ValueError("q, out and the pools must share one dtype; out shaped like q")
+    _check("paged_attention_prefill", lib().paged_attention_prefill(
+        _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
+        _dev(block_tables, "block_tables"), block_tables.shape[1],
+        _dev(context_lens, "context_lens"), _dev(cu_q_lens, "cu_q_lens"), B, int(max_q_len), Hq,
+        Hkv, D, NB, float(scale), _dev(out, "out"), _dtype_code(q), _stream(stream)))
     return out
 
 

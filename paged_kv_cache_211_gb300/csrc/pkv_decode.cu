@@ -35,8 +35,6 @@
 // layout of the second MMA with two 8x8 movmatrix transposes.  Loads of the
 // next block are issued before the current block is computed (two register
 // stages).
-#include <cuda.h>  // CUtensorMap and its enums (the encoder is fetched at run time)
-
 #include <algorithm>
 #include <cmath>
 #include <cstdlib>
@@ -45,6 +43,7 @@
 #include <type_traits>
 
 #include "pkv_internal.cuh"
+#include "pkv_tma.cuh"
 
 namespace pkv {
 
@@ -115,6 +114,7 @@ struct DecodeParams {
     int max_blocks_per_seq, num_blocks, len_bound;
     int partition_blocks;      // > 0: fixed partition length (blocks)
     int skip_blocks;           // cascade: leading shared blocks handled by the prefix pass
+    int l2_prefetch;           // TMA pass: prefetch the next batch of blocks into L2
     int prefix_parts;          // cascade: workspace rows per sequence written by the prefix pass
     int min_partition_blocks;  // lower bound of the adaptive choice
     int target_items;
@@ -580,104 +580,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
 // ============================================================================
 constexpr int kTmaConsumers = 8;
 constexpr int kTmaThreads = (kTmaConsumers + 1) * 32;
-constexpr int kTmaItemsPerCta = 4;
+constexpr int kTmaItemsPerCta = 8;
 constexpr int kTmaMaxStages = 8;
-constexpr long long kWaitCycles = 4000000000ll;  // ~2 s at 2 GHz
-
-__device__ __forceinline__ uint32_t smem_addr(const void* ptr) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_addr(bar)), "r"(count)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_addr(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_addr(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n"
-        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-
-// Waits for the phase of `bar` with parity `parity`.  Returns false without
-// waiting once *abort is set, and sets *abort and the status bit when the
-// wait exceeds kWaitCycles.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          unsigned int* status) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (!*abort) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (clock64() - t0 > kWaitCycles) {
-            *abort = 1;
-            atomicOr(status, PKV_DEV_TIMEOUT);
-            return false;
-        }
-    }
-    return false;
-}
-
-// A bounded wait that ignores the abort flag (used to let issued copies land).
-__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, unsigned int* status) {
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > kWaitCycles) {
-            atomicOr(status, PKV_DEV_TIMEOUT);
-            return;
-        }
-    }
-}
-
-// 16 rows x 64 elements of one KV head: tensor coordinates (element x, head, row).
-__device__ __forceinline__ void tma_load_rows(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                              int x, int head, int row) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5}], [%2];\n" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(head), "r"(row)
-        : "memory");
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr)
-                 : "memory");
-}
-
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr)
-                 : "memory");
-}
-
-// Byte offset of 16-byte chunk c (of D/8) of row `row` in a swizzled tile of
-// 64-element boxes: box c/8 (2 KB each), 128-byte row, chunk (c%8) ^ (row%8).
-__device__ __forceinline__ uint32_t swz(int row, int c) {
-    return (uint32_t)((c >> 3) * 2048 + row * 128 + (((c & 7) ^ (row & 7)) << 4));
-}
-
 template <typename T, int D>
 __global__ void __launch_bounds__(kTmaThreads, 1)
     decode_partition_tma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
-                                const __grid_constant__ CUtensorMap tmap_v, int nstages) {
+                                const __grid_constant__ CUtensorMap tmap_v, int nstages,
+                                int heads_per_item) {
     using E = Elem<T>;
     constexpr int NC = kTmaConsumers;
     constexpr int HALVES = D / 64;
@@ -732,8 +641,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     const int total_blocks = cta_sum<NC + 1>(my_blocks, red);
     int PB = p.partition_blocks;
     if (PB <= 0) {
-        // an item covers every KV head of its blocks
-        const long long want = ((long long)total_blocks + p.target_items - 1) / p.target_items;
+        // items cover heads_per_item KV heads of their blocks
+        const long long want =
+            ((long long)total_blocks * (p.num_kv_heads / heads_per_item) + p.target_items - 1) /
+            p.target_items;
         const long long lo = p.min_partition_blocks;
         const long long hi = kAdaptiveMaxBlocks > lo ? kAdaptiveMaxBlocks : lo;
         PB = (int)(want < lo ? lo : (want > hi ? hi : want));
@@ -758,18 +669,22 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 
     const int Hq = p.num_q_heads, Hkv = p.num_kv_heads;
     const size_t row_stride = (size_t)Hkv * D;
-    // An item is one partition of one sequence across all KV heads, so a
-    // block's heads (one contiguous run of the pool) are fetched together.
-    // Consumer warp w serves KV head w % Hkv and every CPH-th block of the
-    // item, CPH = NC / Hkv consumers per head.
-    const int total_items = total_parts;
-    const int CPH = NC / Hkv;
+    // An item is one partition of one sequence and a group of HPI KV heads
+    // (HPI = 1: one head; HPI = Hkv: all heads, so a block's heads -- one
+    // contiguous run of the pool -- are fetched together).  Consumer warp w
+    // serves head hg*HPI + w % HPI of the item and every CPH-th block of it,
+    // CPH = NC / HPI consumers per head.
+    const int HPI = heads_per_item;
+    const int groups = Hkv / HPI;
+    const int total_items = total_parts * groups;
+    const int CPH = NC / HPI;
     struct Item {
-        int s, gp, nparts, ws_row, n, nblk, lo, hi;
+        int s, gp, hg, nparts, ws_row, n, nblk, lo, hi;
     };
     auto item_of = [&](int item) {
         Item it;
-        it.gp = item;
+        it.gp = item / groups;
+        it.hg = item - it.gp * groups;
         int a = 0, b = B - 1;
         while (a < b) {
             const int mid = (a + b + 1) >> 1;
@@ -787,35 +702,58 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 
     if (warp == NC) {
         // ------------------------------------------------------------ producer
-        // Batches of BB blocks x Hkv heads, lane t issuing (block jb + t / Hkv,
-        // head t % Hkv) for consumer h + Hkv * ((block - lo) % CPH).  A batch
+        // Batches of BB blocks x HPI heads, lane t issuing (block jb + t / HPI,
+        // head t % HPI of the group) for consumer t % HPI + HPI * ((block - lo) % CPH).  A batch
         // gives each consumer at most min(4, nstages) blocks, so no lane ever
         // waits for a slot another lane of this warp has yet to fill: every
         // wait is on a consumer warp, never on a diverged lane of this one.
         const int per = min(4, nstages);
         const int BB = CPH * per;               // blocks per batch (a multiple of CPH)
-        int pc[NC];  // stages issued so far per consumer (same in every lane)
+        // lane-constant roles (no division inside the loops)
+        const int bi = lane / HPI;              // this lane's block in a batch
+        const int hl = lane - bi * HPI;         // and head within the group
+        const int wl = hl + HPI * (bi % CPH);   // the consumer it feeds
+        const int uoff = bi / CPH;              // its stage offset within the batch
+        int pc[NC], subv[NC];  // stages issued so far per consumer; consumer's block phase
 #pragma unroll
-        for (int v = 0; v < NC; ++v) pc[v] = 0;
+        for (int v = 0; v < NC; ++v) {
+            pc[v] = 0;
+            subv[v] = v / HPI;
+        }
+        // table entry of this lane's block in the batch starting at jb (-1: none / bad)
+        auto lane_id = [&](const int32_t* table, int jb, int hi) {
+            if (jb + bi >= hi) return -1;
+            const int id = table[jb + bi];
+            if (id < 0 || id >= p.num_blocks) {
+                if (hl == 0) atomicOr(p.status, PKV_DEV_BAD_BLOCK_ID);
+                return -1;  // never read: block 0 is fetched and fully masked
+            }
+            return id;
+        };
         for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
             const Item it = item_of(item);
             const int32_t* table = p.block_tables + (size_t)it.s * p.max_blocks_per_seq;
+            const int h = it.hg * HPI + hl;
+            int id_cur = bi < BB ? lane_id(table, it.lo, it.hi) : -1;
             for (int jb = it.lo; jb < it.hi; jb += BB) {
                 const int cnt = min(BB, it.hi - jb);   // blocks in this batch
-                const int bi = lane / Hkv;             // this lane's block in the batch
-                const int h = lane - bi * Hkv;         // and KV head
-                if (bi < cnt && !*abort_flag) {
-                    int id = table[jb + bi];
-                    if (id < 0 || id >= p.num_blocks) {
-                        if (h == 0) atomicOr(p.status, PKV_DEV_BAD_BLOCK_ID);
-                        id = -1;  // never read: block 0 is fetched and fully masked
+                // the next batch's blocks: ids now, and into L2 ahead of their copies
+                const int id_next = bi < BB ? lane_id(table, jb + BB, it.hi) : -1;
+                if (p.l2_prefetch && id_next >= 0) {
+#pragma unroll
+                    for (int hh = 0; hh < HALVES; ++hh) {
+                        tma_prefetch_rows(&tmap_k, hh * 64, h, id_next * PKV_BLOCK_SIZE);
+                        tma_prefetch_rows(&tmap_v, hh * 64, h, id_next * PKV_BLOCK_SIZE);
                     }
-                    const int w = h + Hkv * (bi % CPH);
+                }
+                if (bi < cnt && !*abort_flag) {
+                    const int id = id_cur;
+                    const int w = wl;
                     int base = 0;
 #pragma unroll
                     for (int v = 0; v < NC; ++v)
                         if (v == w) base = pc[v];
-                    const int use = base + bi / CPH;
+                    const int use = base + uoff;
                     const int k = w * nstages + use % nstages;
                     if (mbar_wait(&empty[k], ((use / nstages) & 1) ^ 1, abort_flag, p.status)) {
                         stage_id[k] = id;
@@ -831,10 +769,14 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                         }
                     }
                 }
+                id_cur = id_next;
+                if (cnt == BB) {  // a full batch gives every consumer `per` stages
 #pragma unroll
-                for (int v = 0; v < NC; ++v) {
-                    const int sub = v / Hkv;  // blocks of this batch with bi % CPH == sub
-                    pc[v] += cnt > sub ? (cnt - sub + CPH - 1) / CPH : 0;
+                    for (int v = 0; v < NC; ++v) pc[v] += per;
+                } else {          // blocks of the batch with bi % CPH == subv[v]
+#pragma unroll
+                    for (int v = 0; v < NC; ++v)
+                        pc[v] += cnt > subv[v] ? (cnt - subv[v] + CPH - 1) / CPH : 0;
                 }
                 __syncwarp();
             }
@@ -851,13 +793,14 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 
     // -------------------------------------------------------------- consumers
     const int w = warp;
-    const int h = w % Hkv, sub = w / Hkv;  // this consumer's KV head and block phase
+    const int hl = w % HPI, sub = w / HPI;  // this consumer's head in the group, block phase
     const int gid = lane >> 2, tig = lane & 3;
     const T* __restrict__ q = static_cast<const T*>(p.q);
     int ncons = 0;  // stages this warp has consumed
     for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
         const Item it = item_of(item);
         const int s = it.s, n = it.n;
+        const int h = it.hg * HPI + hl;
         // q fragment: column gid of the score MMA is query head h*g + gid
         uint32_t qf[KS][2];
         {
@@ -1009,16 +952,16 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         constexpr int SL = D / 8;
         // one thread per (KV head, query head of its group, 8-wide slice of D),
         // merging the CPH consumers of that KV head
-        for (int x = tid; x < Hkv * g * SL; x += NC * 32) {
-            const int hk = x / (g * SL);
+        for (int x = tid; x < HPI * g * SL; x += NC * 32) {
+            const int hk = x / (g * SL);  // head within the group
             const int hh = (x / SL) % g, d0 = (x % SL) * 8;
             float M = -INFINITY;
-            for (int c = 0; c < CPH; ++c) M = fmaxf(M, sm_m[(hk + Hkv * c) * kMaxGroup + hh]);
+            for (int c = 0; c < CPH; ++c) M = fmaxf(M, sm_m[(hk + HPI * c) * kMaxGroup + hh]);
             const float Ms = M == -INFINITY ? 0.f : M;
             float L = 0.f;
             float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             for (int c = 0; c < CPH; ++c) {
-                const int v = hk + Hkv * c;
+                const int v = hk + HPI * c;
                 const float e = fast_exp2(sm_m[v * kMaxGroup + hh] - Ms);
                 L += e * sm_l[v * kMaxGroup + hh];
                 const float* src = sm_o + (v * g + hh) * DP + d0;
@@ -1027,7 +970,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                 acc[0] += e * u.x; acc[1] += e * u.y; acc[2] += e * u.z; acc[3] += e * u.w;
                 acc[4] += e * u2.x; acc[5] += e * u2.y; acc[6] += e * u2.z; acc[7] += e * u2.w;
             }
-            const int qh = hk * g + hh;
+            const int qh = (it.hg * HPI + hk) * g + hh;
             if (it.nparts == 1) {
                 const float inv = L > 0.f ? 1.f / L : 0.f;
                 uint4 packed;
@@ -1218,6 +1161,7 @@ __global__ void __launch_bounds__(128) decode_prefix_kernel(const PrefixParams p
     }
 }
 
+
 struct MergeParams {
     const int* ws_offsets;
     const float* ws_m;
@@ -1334,47 +1278,6 @@ pkv_status launch_decode(const DecodeParams& prm_in, const MergeParams& mp, int 
 // ---------------------------------------------------------------------------
 // Host side of the TMA partition pass.
 // ---------------------------------------------------------------------------
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// cuTensorMapEncodeTiled, fetched through the runtime (no link against the
-// driver library).  nullptr if unavailable.
-EncodeTiledFn encode_tiled() {
-    static std::once_flag once;
-    static EncodeTiledFn fn = nullptr;
-    std::call_once(once, [] {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    });
-    return fn;
-}
-
-// A pool [NB][16][Hkv][D] viewed as (element, head, row) with boxes of
-// 64 elements x 1 head x 16 rows and the 128-byte swizzle.
-bool make_pool_map(CUtensorMap* map, const void* pool, int num_blocks, int num_kv_heads,
-                   int head_dim, pkv_dtype dtype) {
-    EncodeTiledFn enc = encode_tiled();
-    if (!enc) return false;
-    const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_kv_heads,
-                                (cuuint64_t)num_blocks * PKV_BLOCK_SIZE};
-    const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2,
-                                   (cuuint64_t)num_kv_heads * head_dim * 2};
-    const cuuint32_t box[3] = {64, 1, PKV_BLOCK_SIZE};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    const CUtensorMapDataType dt =
-        dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    return enc(map, dt, 3, const_cast<void*>(pool), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-           CUDA_SUCCESS;
-}
-
 int smem_optin_bytes() {
     int dev = 0, v = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -1402,6 +1305,22 @@ int tma_stages(int head_dim, int num_seqs, int group) {
     return ns < 2 ? 0 : (int)std::min<long long>(ns, kTmaMaxStages);
 }
 
+// KV heads per TMA item.  All heads of a block together keep its contiguous
+// run in one place (measured best at head_dim 64, where one head's rows are
+// only 128 bytes); one head per item keeps partitions long and partials few
+// (measured best at head_dim 128 with long contexts).  PKV_HEADS_PER_ITEM=1 or
+// =all overrides.
+int tma_heads_per_item(int head_dim, int num_kv_heads) {
+    static const int mode = [] {
+        const char* v = std::getenv("PKV_HEADS_PER_ITEM");
+        if (!v) return 0;
+        return std::strcmp(v, "all") == 0 ? 2 : (std::strcmp(v, "1") == 0 ? 1 : 0);
+    }();
+    if (mode == 1) return 1;
+    if (mode == 2) return num_kv_heads;
+    return head_dim == 64 ? num_kv_heads : 1;
+}
+
 template <typename T, int D>
 pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp, int pb_lower,
                              int max_blocks, bool need_merge, int passes, int nstages,
@@ -1421,12 +1340,15 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp, 
             return PKV_ERR_CUDA;
         const int sms = sm_count();
         if (sms <= 0) return PKV_ERR_CUDA;
-        // one item per partition, covering every KV head
-        const long long items_upper =
-            (long long)prm.num_seqs * std::max(1, ceil_div(max_blocks, pb_lower));
+        // items cover `hpi` KV heads of one partition
+        const int hpi = tma_heads_per_item(D, prm.num_kv_heads);
+        const long long items_upper = (long long)prm.num_seqs *
+                                      std::max(1, ceil_div(max_blocks, pb_lower)) *
+                                      (prm.num_kv_heads / hpi);
         const int grid = (int)std::max<long long>(1, std::min<long long>(items_upper, sms));
-        prm.target_items = grid * kTmaItemsPerCta;
-        kern<<<grid, kTmaThreads, smem, stream>>>(prm, tmk, tmv, nstages);
+        // per-head items: 8 per CTA; all-heads items carry Hkv heads each: 4 per CTA
+        prm.target_items = grid * (hpi == 1 ? kTmaItemsPerCta : kTmaItemsPerCta / 2);
+        kern<<<grid, kTmaThreads, smem, stream>>>(prm, tmk, tmv, nstages, hpi);
         if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
     }
     if ((passes & kPassMerge) && need_merge) {
@@ -1445,6 +1367,17 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp, 
             return PKV_ERR_CUDA;
     }
     return PKV_OK;
+}
+
+
+// The TMA pass prefetches each next batch of blocks into L2 (PKV_TMA_PREFETCH=0 turns
+// it off, for measurement).
+bool tma_l2_prefetch() {
+    static const bool on = [] {
+        const char* v = std::getenv("PKV_TMA_PREFETCH");
+        return !(v && std::strcmp(v, "0") == 0);
+    }();
+    return on;
 }
 
 // Which partition kernel runs: the TMA pipeline unless PKV_DECODE_KERNEL=ldg
@@ -1528,6 +1461,7 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
     prm.len_bound = len_bound;
     prm.partition_blocks = partition_blocks;
     prm.skip_blocks = prefix_blocks;
+    prm.l2_prefetch = tma_l2_prefetch();
     prm.prefix_parts = prefix_parts;
     prm.min_partition_blocks = pb_lower;
     prm.target_items = 0;

@@ -78,6 +78,10 @@ WORKLOADS = {
         "llama7b_long", 2114, 32, 32, 8, 128, 65536, "bf16", "lognormal:8192,0.5,32768", 2048,
         description="Llama/Mistral-7B-shaped long context: 32 seqs, lens lognormal "
                     "(median 8192, sigma 0.5, cap 32768), 32q/8kv, D=128, bf16, 65536-block pool"),
+    "llama7b_prefill": Workload(
+        "llama7b_prefill", 2116, 8, 32, 8, 128, 1536, "bf16", "fixed_all:2048", 128,
+        description="Llama-7B-shaped chunked prefill: 8 prompts x 2048 tokens, the whole "
+                    "prompt as one chunk, 32q/8kv, D=128, bf16"),
     "prefix_shared": Workload(
         "prefix_shared", 2115, 128, 16, 8, 128, 4096, "bf16", "prefix:1024,64,512", 96,
         prefix_blocks=64,
@@ -238,3 +242,43 @@ def algorithmic_bytes(w: Workload, lens: np.ndarray, with_write: bool = True) ->
     if with_write:
         total += 2 * B * Hkv * D * 2 * 2
     return total
+
+
+def make_prefill_inputs(w: Workload, chunk: int, device="cpu") -> dict:
+    """A chunked-prefill step of ``w``: every sequence's last ``chunk`` tokens
+    (or all of them, if shorter) are query rows.  Keys as in make_inputs for
+    the pools and tables, plus q_rows [R,Hq,D], k_rows/v_rows [R,Hkv,D] (the
+    chunk's K/V), cu_q_lens [B+1] int32 and the rows' slots (int64), listed
+    by walking each table block by block."""
+    inp = make_inputs(w, device=device, num_layers=1, poison=False)
+    lens = inp["context_lens_host"]
+    tables = inp["block_tables_host"]
+    qlens = np.minimum(lens, chunk).astype(np.int64)
+    cu = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    slots = []
+    for s in range(w.num_seqs):
+        n = int(lens[s])
+        for t in range(n - int(qlens[s]), n):
+            slots.append(int(tables[s, t // BLOCK_SIZE]) * BLOCK_SIZE + t % BLOCK_SIZE)
+    dev = torch.device(device)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(w.seed * 1000 + 11)
+    R = int(cu[-1])
+    inp.update(
+        q_rows=_randn((R, w.num_q_heads, w.head_dim), w.torch_dtype, dev, gen),
+        k_rows=_randn((R, w.num_kv_heads, w.head_dim), w.torch_dtype, dev, gen),
+        v_rows=_randn((R, w.num_kv_heads, w.head_dim), w.torch_dtype, dev, gen),
+        cu_q_lens=torch.from_numpy(cu).to(dev), cu_q_lens_host=cu,
+        row_slots=torch.tensor(slots, dtype=torch.int64, device=dev),
+        max_q_len=int(qlens.max()))
+    return inp
+
+
+def prefill_flops(lens: np.ndarray, qlens: np.ndarray, num_q_heads: int, head_dim: int) -> int:
+    """Multiply-adds x 2 of causal attention: row at position p reads p + 1 keys,
+    for q.k and for p.v."""
+    total = 0
+    for n, ql in zip(lens.astype(np.int64), qlens.astype(np.int64)):
+        # sum over p = n-ql .. n-1 of (p + 1)
+        total += ql * (2 * n - ql + 1) // 2
+    return int(4 * total * num_q_heads * head_dim)

@@ -302,3 +302,59 @@ def failing_pins(o) -> list:
         except Exception:  # an assertion, or the oracle rejecting its inputs
             bad.append(pin.__name__)
     return bad
+
+
+# --- prefill (causal, packed chunks) -------------------------------------------
+
+def pin_prefill_vs_sdpa_causal(o):
+    """Prefill oracle vs torch SDPA (float64) with an explicit causal mask built
+    from positions, on contexts gathered by enumeration."""
+    import torch.nn.functional as F
+    from pkv_testutil import token_slots
+    rng = np.random.default_rng(61)
+    for dt, (Hq, Hkv, D) in [(F16, (4, 2, 8)), (BF16, (6, 3, 16)), (F16, (2, 2, 4))]:
+        enc = _bf16 if dt == BF16 else _f16
+        lens = [5, 33, 17, 1]
+        qlens = [5, 7, 1, 1]          # a whole prompt, a chunk, and decode-like rows
+        NB = 12
+        perm = rng.permutation(NB)
+        MB = 3
+        tables = np.zeros((4, MB), np.int32)
+        pos = 0
+        for s, n in enumerate(lens):
+            nb = (n + 15) // 16
+            tables[s, :nb] = perm[pos:pos + nb]
+            pos += nb
+        k = enc(rng.standard_normal((NB, BS, Hkv, D)))
+        v = enc(rng.standard_normal((NB, BS, Hkv, D)))
+        cu = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+        q = enc(rng.standard_normal((cu[-1], Hq, D)))
+        scale = 0.37
+        got = o.prefill_attention(dt, q, k, v, tables, np.array(lens, np.int32), cu, scale)
+        kf = k.reshape(NB * BS, Hkv, D)
+        vf = v.reshape(NB * BS, Hkv, D)
+        for s, (n, ql) in enumerate(zip(lens, qlens)):
+            sl = np.array(token_slots(tables[s], n))
+            K = torch.from_numpy(lib_decode(kf[sl], dt)).permute(1, 0, 2).repeat_interleave(
+                Hq // Hkv, dim=0)
+            V = torch.from_numpy(lib_decode(vf[sl], dt)).permute(1, 0, 2).repeat_interleave(
+                Hq // Hkv, dim=0)
+            Q = torch.from_numpy(lib_decode(q[cu[s]:cu[s + 1]], dt)).permute(1, 0, 2)
+            qpos = torch.arange(n - ql, n).unsqueeze(1)
+            kpos = torch.arange(n).unsqueeze(0)
+            mask = kpos <= qpos                                   # [ql, n]
+            ref = F.scaled_dot_product_attention(Q, K, V, attn_mask=mask, scale=scale)
+            want = ref.permute(1, 0, 2).numpy()
+            assert np.allclose(got[cu[s]:cu[s + 1]], want, rtol=1e-11, atol=1e-12), s
+
+
+def pin_prefill_last_row_is_decode(o):
+    """The last row of a chunk sees the whole context: it equals decode attention."""
+    q, k, v, tb, ln = _small_case(71, BF16, lens=(1, 17, 40))
+    cu = np.array([0, 1, 2, 3], np.int32)
+    a = o.prefill_attention(BF16, q, k, v, tb, ln, cu, 0.4)
+    b = o.decode_attention(BF16, q, k, v, tb, ln, 0.4)
+    assert np.array_equal(a, b)
+
+
+ALL_PINS += [pin_prefill_vs_sdpa_causal, pin_prefill_last_row_is_decode]

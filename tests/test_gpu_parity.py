@@ -21,7 +21,7 @@ pytestmark = pytest.mark.gpu
 
 # sequences the oracle checks per workload (None = all)
 ORACLE_SEQS = {"tiny": None, "qwen3_0p6b": None, "tinyllama_1p1b": 24, "llama7b_long": 5,
-               "prefix_shared": 40}
+               "prefix_shared": 40, "llama7b_prefill": 3}
 
 
 @pytest.fixture(scope="module", autouse=True)

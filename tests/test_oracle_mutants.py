@@ -46,6 +46,8 @@ MUTANTS = {
     "slot_position_len": ("int p = n - 1;", "int p = n;"),
     "write_padding_not_skipped": ("if (slot < 0) continue;", "if (slot < 0) slot = 0;"),
     "write_v_into_k": ("memcpy(v_cache + dst, v_new", "memcpy(k_cache + dst, v_new"),
+    "prefill_not_causal": ("int p = n - rows + r;", "int p = n - 1;"),
+    "prefill_position_off_by_one": ("int p = n - rows + r;", "int p = n - rows + r - 1 + (r == 0);"),
 }
 
 
