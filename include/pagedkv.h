@@ -450,6 +450,16 @@ pkv_status paged_attention_decode_noalloc(const void* q, const void* k_cache,
  * `reset` is non-zero.  Synchronises the device. */
 pkv_status pkv_device_status(unsigned int* flags, int reset);
 
+/* The status word as a status code, for one stream: waits for `stream`,
+ * reads and clears the word, and returns PKV_ERR_CUDA if a kernel timed out
+ * (PKV_DEV_TIMEOUT) or the stream holds a CUDA error, else PKV_ERR_BAD_BLOCK_ID
+ * if a table entry was out of range, else PKV_ERR_INVALID_ARG if a length or a
+ * slot was, else PKV_OK.  The word is per device, so bits set by work on other
+ * streams of the device are read (and cleared) too.  The pages define no such
+ * call: it reports the device-side checks every kernel here makes instead of
+ * trapping. */
+pkv_status paged_kv_last_error(pkv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -25,6 +25,7 @@ __all__ = [
     "paged_attention_cascade_workspace_bytes", "paged_attention_decode_cascade",
     "paged_kv_decode_step_cascade", "new_cascade_workspace", "paged_attention_prefill",
     "paged_kv_decode_step_staging_bytes", "paged_kv_decode_step_host", "pkv_device_status",
+    "paged_kv_last_error",
     "BlockAllocator", "new_workspace", "paged_kv_block_hash", "paged_kv_copy_blocks", "paged_attention_decode_noalloc",
     "NOALLOC_SCRATCH_BYTES",
 ]
@@ -91,6 +92,7 @@ _SIGS = {
     "paged_kv_decode_step_host": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp, _i, _i,
                                    _i, _i, _i, _i, _i, _f, _vp, _sz, _i, _vp], _i),
     "pkv_device_status": ([ctypes.POINTER(ctypes.c_uint), _i], _i),
+    "paged_kv_last_error": ([ctypes.c_void_p], _i),
     "paged_kv_num_cached": ([_vp], _i),
     "paged_kv_block_hash": ([ctypes.c_uint64, _vp, _i], ctypes.c_uint64),
     "paged_kv_prefix_insert": ([_vp, ctypes.c_int32, ctypes.c_uint64], _i),
@@ -479,6 +481,12 @@ def pkv_device_status(reset: bool = True) -> int:
     flags = ctypes.c_uint(0)
     _check("pkv_device_status", lib().pkv_device_status(ctypes.byref(flags), int(reset)))
     return flags.value
+
+
+def paged_kv_last_error(stream=None) -> int:
+    """Status code for the device checks of work on `stream` (waits for it; clears
+    the device status word).  Returned, not raised: 0 means no flag was set."""
+    return int(lib().paged_kv_last_error(_stream(stream)))
 
 
 class BlockAllocator:

@@ -91,6 +91,22 @@ pkv_status pkv_device_status(unsigned int* flags, int reset) {
     return PKV_OK;
 }
 
+pkv_status paged_kv_last_error(pkv_stream_t stream) {
+    unsigned int* p = pkv::status_word();
+    if (!p) return PKV_ERR_CUDA;
+    unsigned int flags = 0;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return PKV_ERR_CUDA;
+    if (cudaMemcpyAsync(&flags, p, sizeof(unsigned int), cudaMemcpyDeviceToHost, stream) !=
+            cudaSuccess ||
+        cudaMemsetAsync(p, 0, sizeof(unsigned int), stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (flags & PKV_DEV_TIMEOUT) return PKV_ERR_CUDA;
+    if (flags & PKV_DEV_BAD_BLOCK_ID) return PKV_ERR_BAD_BLOCK_ID;
+    if (flags & (PKV_DEV_BAD_LENGTH | PKV_DEV_BAD_SLOT)) return PKV_ERR_INVALID_ARG;
+    return PKV_OK;
+}
+
 size_t paged_kv_decode_step_staging_bytes(int num_seqs, int num_q_heads, int num_kv_heads,
                                           int head_dim, int max_blocks_per_seq) {
     if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||

@@ -114,7 +114,6 @@ struct DecodeParams {
     int max_blocks_per_seq, num_blocks, len_bound;
     int partition_blocks;      // > 0: fixed partition length (blocks)
     int skip_blocks;           // cascade: leading shared blocks handled by the prefix pass
-    int l2_prefetch;           // TMA pass: prefetch the next batch of blocks into L2
     int prefix_parts;          // cascade: workspace rows per sequence written by the prefix pass
     int min_partition_blocks;  // lower bound of the adaptive choice
     int target_items;
@@ -582,7 +581,7 @@ constexpr int kTmaConsumers = 8;
 constexpr int kTmaThreads = (kTmaConsumers + 1) * 32;
 constexpr int kTmaItemsPerCta = 8;
 constexpr int kTmaMaxStages = 8;
-template <typename T, int D>
+template <typename T, int D, bool kOneHead>
 __global__ void __launch_bounds__(kTmaThreads, 1)
     decode_partition_tma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
                                 const __grid_constant__ CUtensorMap tmap_v, int nstages,
@@ -641,13 +640,30 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     const int total_blocks = cta_sum<NC + 1>(my_blocks, red);
     int PB = p.partition_blocks;
     if (PB <= 0) {
-        // items cover heads_per_item KV heads of their blocks
-        const long long want =
-            ((long long)total_blocks * (p.num_kv_heads / heads_per_item) + p.target_items - 1) /
-            p.target_items;
-        const long long lo = p.min_partition_blocks;
-        const long long hi = kAdaptiveMaxBlocks > lo ? kAdaptiveMaxBlocks : lo;
-        PB = (int)(want < lo ? lo : (want > hi ? hi : want));
+        const int groups0 = p.num_kv_heads / (kOneHead ? 1 : heads_per_item);
+        if ((long long)B * groups0 >= 4ll * gridDim.x) {
+            // enough items without splitting: one partition per sequence
+            int my_max = 0;
+            for (int s = tid; s < B; s += kTmaThreads) {
+                const int nb = (sm_len[s] + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE - p.skip_blocks;
+                my_max = max(my_max, nb);
+            }
+            for (int o = 16; o > 0; o >>= 1) my_max = max(my_max, __shfl_xor_sync(0xffffffffu, my_max, o));
+            __syncthreads();
+            if (lane == 0) red[warp] = my_max;
+            __syncthreads();
+            int mx = 0;
+#pragma unroll
+            for (int w = 0; w < NC + 1; ++w) mx = max(mx, red[w]);
+            PB = max(mx, p.min_partition_blocks);
+        } else {
+            // items cover heads_per_item KV heads of their blocks: aim at target_items
+            const long long want =
+                ((long long)total_blocks * groups0 + p.target_items - 1) / p.target_items;
+            const long long lo = p.min_partition_blocks;
+            const long long hi = kAdaptiveMaxBlocks > lo ? kAdaptiveMaxBlocks : lo;
+            PB = (int)(want < lo ? lo : (want > hi ? hi : want));
+        }
     }
     const int chunk = (B + kTmaThreads - 1) / kTmaThreads;
     const int s_lo = min(B, tid * chunk), s_hi = min(B, s_lo + chunk);
@@ -674,7 +690,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     // contiguous run of the pool -- are fetched together).  Consumer warp w
     // serves head hg*HPI + w % HPI of the item and every CPH-th block of it,
     // CPH = NC / HPI consumers per head.
-    const int HPI = heads_per_item;
+    const int HPI = kOneHead ? 1 : heads_per_item;  // a constant in the one-head build
     const int groups = Hkv / HPI;
     const int total_items = total_parts * groups;
     const int CPH = NC / HPI;
@@ -737,15 +753,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             int id_cur = bi < BB ? lane_id(table, it.lo, it.hi) : -1;
             for (int jb = it.lo; jb < it.hi; jb += BB) {
                 const int cnt = min(BB, it.hi - jb);   // blocks in this batch
-                // the next batch's blocks: ids now, and into L2 ahead of their copies
+                // the next batch's table entries are loaded one batch ahead
                 const int id_next = bi < BB ? lane_id(table, jb + BB, it.hi) : -1;
-                if (p.l2_prefetch && id_next >= 0) {
-#pragma unroll
-                    for (int hh = 0; hh < HALVES; ++hh) {
-                        tma_prefetch_rows(&tmap_k, hh * 64, h, id_next * PKV_BLOCK_SIZE);
-                        tma_prefetch_rows(&tmap_v, hh * 64, h, id_next * PKV_BLOCK_SIZE);
-                    }
-                }
                 if (bi < cnt && !*abort_flag) {
                     const int id = id_cur;
                     const int w = wl;
@@ -1305,20 +1314,47 @@ int tma_stages(int head_dim, int num_seqs, int group) {
     return ns < 2 ? 0 : (int)std::min<long long>(ns, kTmaMaxStages);
 }
 
-// KV heads per TMA item.  All heads of a block together keep its contiguous
-// run in one place (measured best at head_dim 64, where one head's rows are
-// only 128 bytes); one head per item keeps partitions long and partials few
-// (measured best at head_dim 128 with long contexts).  PKV_HEADS_PER_ITEM=1 or
-// =all overrides.
-int tma_heads_per_item(int head_dim, int num_kv_heads) {
-    static const int mode = [] {
+// KV heads per TMA item.  One head per item keeps each consumer's share of a
+// partition long and the partials few; several heads per item fetch more of a
+// block's contiguous run at once and keep consumers busy when contexts are
+// short.  Rule, from a sweep of 1/2/4/8 heads per item on four workloads:
+// one head when unsplit (sequence, head) items already give every SM 4 of
+// them; otherwise the fewest heads that make max_blocks * heads >= 256, i.e.
+// at least 32 blocks per consumer of a longest sequence (28-layer steps with
+// 2..32-block contexts ran 1.12x faster at 8 heads per item than at 1).
+// PKV_HEADS_PER_ITEM=<n> or =all overrides.
+int tma_heads_per_item(int num_seqs, int max_blocks, int num_kv_heads) {
+    // consumers split evenly over the heads of an item, so a valid count
+    // divides both the KV heads and the consumer warps
+    auto valid = [&](int h) { return h >= 1 && num_kv_heads % h == 0 && kTmaConsumers % h == 0; };
+    static const int forced = [] {
         const char* v = std::getenv("PKV_HEADS_PER_ITEM");
         if (!v) return 0;
-        return std::strcmp(v, "all") == 0 ? 2 : (std::strcmp(v, "1") == 0 ? 1 : 0);
+        return std::strcmp(v, "all") == 0 ? -1 : std::atoi(v);
     }();
-    if (mode == 1) return 1;
-    if (mode == 2) return num_kv_heads;
-    return head_dim == 64 ? num_kv_heads : 1;
+    if (forced == -1) {
+        int h = std::min(num_kv_heads, kTmaConsumers);
+        while (!valid(h)) --h;
+        return h;
+    }
+    if (forced > 0) return valid(forced) ? forced : 1;
+    if ((long long)num_seqs * num_kv_heads >= 4ll * sm_count()) return 1;
+    int hpi = 1;
+    for (int h = 2; h <= kTmaConsumers; ++h) {
+        if ((long long)max_blocks * hpi >= 32ll * kTmaConsumers) break;
+        if (valid(h)) hpi = h;
+    }
+    return hpi;
+}
+
+// Adaptive partitioning aims at this many items per CTA (PKV_TMA_ITEMS overrides).
+int tma_items_per_cta(int heads_per_item) {
+    static const int forced = [] {
+        const char* v = std::getenv("PKV_TMA_ITEMS");
+        return v ? std::atoi(v) : 0;
+    }();
+    if (forced > 0) return forced;
+    return heads_per_item == 1 ? kTmaItemsPerCta : kTmaItemsPerCta / 2;
 }
 
 template <typename T, int D>
@@ -1332,7 +1368,10 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp, 
         if (!make_pool_map(&tmk, prm.k_cache, prm.num_blocks, prm.num_kv_heads, D, dt) ||
             !make_pool_map(&tmv, prm.v_cache, prm.num_blocks, prm.num_kv_heads, D, dt))
             return PKV_ERR_CUDA;
-        auto kern = decode_partition_tma_kernel<T, D>;
+        // items cover `hpi` KV heads of one partition
+        const int hpi = tma_heads_per_item(prm.num_seqs, max_blocks, prm.num_kv_heads);
+        auto kern = hpi == 1 ? decode_partition_tma_kernel<T, D, true>
+                             : decode_partition_tma_kernel<T, D, false>;
         const size_t smem =
             tma_fixed_smem(D, prm.num_seqs, prm.group) + (size_t)nstages * tma_stage_smem(D);
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
@@ -1340,14 +1379,12 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp, 
             return PKV_ERR_CUDA;
         const int sms = sm_count();
         if (sms <= 0) return PKV_ERR_CUDA;
-        // items cover `hpi` KV heads of one partition
-        const int hpi = tma_heads_per_item(D, prm.num_kv_heads);
         const long long items_upper = (long long)prm.num_seqs *
                                       std::max(1, ceil_div(max_blocks, pb_lower)) *
                                       (prm.num_kv_heads / hpi);
         const int grid = (int)std::max<long long>(1, std::min<long long>(items_upper, sms));
         // per-head items: 8 per CTA; all-heads items carry Hkv heads each: 4 per CTA
-        prm.target_items = grid * (hpi == 1 ? kTmaItemsPerCta : kTmaItemsPerCta / 2);
+        prm.target_items = grid * tma_items_per_cta(hpi);
         kern<<<grid, kTmaThreads, smem, stream>>>(prm, tmk, tmv, nstages, hpi);
         if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
     }
@@ -1369,16 +1406,6 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp, 
     return PKV_OK;
 }
 
-
-// The TMA pass prefetches each next batch of blocks into L2 (PKV_TMA_PREFETCH=0 turns
-// it off, for measurement).
-bool tma_l2_prefetch() {
-    static const bool on = [] {
-        const char* v = std::getenv("PKV_TMA_PREFETCH");
-        return !(v && std::strcmp(v, "0") == 0);
-    }();
-    return on;
-}
 
 // Which partition kernel runs: the TMA pipeline unless PKV_DECODE_KERNEL=ldg
 // selects the register-pipelined kernel (kept for comparison).
@@ -1461,7 +1488,6 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
     prm.len_bound = len_bound;
     prm.partition_blocks = partition_blocks;
     prm.skip_blocks = prefix_blocks;
-    prm.l2_prefetch = tma_l2_prefetch();
     prm.prefix_parts = prefix_parts;
     prm.min_partition_blocks = pb_lower;
     prm.target_items = 0;

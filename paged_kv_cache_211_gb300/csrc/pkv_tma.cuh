@@ -83,17 +83,6 @@ __device__ __forceinline__ void tma_load_rows(void* dst, const CUtensorMap* map,
         : "memory");
 }
 
-// The same box, fetched only into L2 (no shared memory, no barrier): a later
-// copy of it then finds it there.
-__device__ __forceinline__ void tma_prefetch_rows(const CUtensorMap* map, int x, int head,
-                                                  int row) {
-    asm volatile(
-        "cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];\n" ::"l"(
-            reinterpret_cast<uint64_t>(map)),
-        "r"(x), "r"(head), "r"(row)
-        : "memory");
-}
-
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])

@@ -190,8 +190,10 @@ def test_bad_device_values_are_flagged_not_read(cuda_device):
     pkv.paged_attention_decode(q, kc, vc, inp["block_tables"], inp["context_lens"], max_len,
                                w.scale, out, ws)
     torch.cuda.synchronize()
-    flags = pkv.pkv_device_status(reset=True)
+    flags = pkv.pkv_device_status(reset=False)
     assert flags & pkv.DEV_BAD_BLOCK_ID and flags & pkv.DEV_BAD_LENGTH
+    assert pkv.paged_kv_last_error() == 4        # PKV_ERR_BAD_BLOCK_ID; clears the word
+    assert pkv.paged_kv_last_error() == 0
     assert torch.isfinite(out.float()).all()
     assert torch.count_nonzero(out[2]) == 0      # an invalid length gives a zero row
     assert_attention_close(bits(out)[:1], want, oracle.BF16, "row without bad values")
@@ -211,7 +213,8 @@ def test_reshape_and_cache_padding_and_bad_slots(cuda_device):
                                       np.array([3, 191, 17]))
     pkv.reshape_and_cache(kn, vn, kc, vc, slots)
     torch.cuda.synchronize()
-    assert pkv.pkv_device_status(reset=True) == pkv.DEV_BAD_SLOT
+    assert pkv.pkv_device_status(reset=False) == pkv.DEV_BAD_SLOT
+    assert pkv.paged_kv_last_error() == 1        # PKV_ERR_INVALID_ARG
     assert np.array_equal(bits(kc), wk) and np.array_equal(bits(vc), wv)
 
 
