@@ -239,8 +239,10 @@ pkv_status paged_attention_decode(const void* q, const void* k_cache, const void
                                   size_t workspace_bytes, pkv_dtype dtype, pkv_stream_t stream);
 
 /* As paged_attention_decode, with the partition length fixed by the caller:
- * partition_blocks > 0 physical blocks (16 tokens each) per partition; 0
- * picks it from the device-side lengths as paged_attention_decode does.
+ * a sequence of n blocks is cut into ceil(n / partition_blocks) partitions
+ * of near-equal size (at most partition_blocks physical blocks of 16 tokens
+ * each); 0 picks the length from the device-side lengths as
+ * paged_attention_decode does.
  * The result does not depend on the partition length beyond fp32 rounding.
  * partition_blocks must be >= paged_attention_min_partition_blocks(
  * max_context_len) so that the workspace bound holds. */

@@ -711,8 +711,13 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         it.ws_row = it.gp + p.prefix_parts * (a + 1);            // this item's row
         it.n = sm_len[a];
         it.nblk = (it.n + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
-        it.lo = p.skip_blocks + (it.gp - sm_off[a]) * PB;
-        it.hi = min(it.nblk, it.lo + PB);
+        // the k partitions of a sequence split its blocks evenly (sizes differ
+        // by at most one, none above PB): a ragged last partition would leave
+        // the CTAs that draw it idle at the end of the pass
+        const int k = sm_off[a + 1] - sm_off[a], i = it.gp - sm_off[a];
+        const int rest = max(it.nblk - p.skip_blocks, 0);
+        it.lo = p.skip_blocks + (int)((long long)i * rest / k);
+        it.hi = p.skip_blocks + (int)((long long)(i + 1) * rest / k);
         return it;
     };
 
