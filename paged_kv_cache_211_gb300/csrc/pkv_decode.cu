@@ -77,12 +77,19 @@ struct WsLayout {
     size_t offsets, m, l, o, total;
 };
 
+// Largest grid of the even-split partition pass; its workspace holds two rows
+// of every query head per CTA.
+constexpr int kMaxEvenGrid = 256;
+// Shortest table bound (in blocks) for which the TMA pass splits evenly.
+constexpr int kEvenMinBlocks = 64;
+
 WsLayout ws_layout(int num_seqs, int num_q_heads, int head_dim, int max_context_len,
                    int extra_rows_per_seq = 0) {
     const int mb = ceil_div(std::max(max_context_len, 0), PKV_BLOCK_SIZE);
     const int parts =
         std::max(1, ceil_div(mb, min_partition_blocks(max_context_len))) + extra_rows_per_seq;
-    const size_t rows = (size_t)num_seqs * parts * num_q_heads;
+    const size_t rows = std::max((size_t)num_seqs * parts * num_q_heads,
+                                 (size_t)2 * kMaxEvenGrid * num_q_heads);
     WsLayout w;
     w.offsets = 0;
     w.m = align256((size_t)(num_seqs + 1) * 4);
@@ -117,6 +124,7 @@ struct DecodeParams {
     int prefix_parts;          // cascade: workspace rows per sequence written by the prefix pass
     int min_partition_blocks;  // lower bound of the adaptive choice
     int target_items;
+    int even_split;            // TMA pass: cut the (sequence, head group, block) units evenly
     float scale_log2;          // scale * log2(e): scores live in base 2
 };
 
@@ -638,8 +646,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         my_blocks += (n + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
     }
     const int total_blocks = cta_sum<NC + 1>(my_blocks, red);
+    const bool even = p.even_split != 0;  // uniform over the grid
     int PB = p.partition_blocks;
-    if (PB <= 0) {
+    if (!even && PB <= 0) {
         const int groups0 = p.num_kv_heads / (kOneHead ? 1 : heads_per_item);
         if ((long long)B * groups0 >= 4ll * gridDim.x) {
             // enough items without splitting: one partition per sequence
@@ -667,13 +676,18 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     }
     const int chunk = (B + kTmaThreads - 1) / kTmaThreads;
     const int s_lo = min(B, tid * chunk), s_hi = min(B, s_lo + chunk);
+    // item mode: partitions per sequence; even split: blocks per sequence
+    auto units_of = [&](int s) {
+        return even ? (sm_len[s] + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE
+                    : item_parts(sm_len[s], PB, p.skip_blocks, p.prefix_parts);
+    };
     int mine = 0;
-    for (int s = s_lo; s < s_hi; ++s) mine += item_parts(sm_len[s], PB, p.skip_blocks, p.prefix_parts);
+    for (int s = s_lo; s < s_hi; ++s) mine += units_of(s);
     int total_parts = 0;
     int run = cta_exclusive_scan<NC + 1>(mine, red, &total_parts);
     for (int s = s_lo; s < s_hi; ++s) {
         sm_off[s] = run;
-        run += item_parts(sm_len[s], PB, p.skip_blocks, p.prefix_parts);
+        run += units_of(s);
     }
     if (tid == 0) sm_off[B] = total_parts;
     __syncthreads();
@@ -694,32 +708,105 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     const int groups = Hkv / HPI;
     const int total_items = total_parts * groups;
     const int CPH = NC / HPI;
+    // A work item: blocks [lo, hi) of sequence s for head group hg.  dest < 0:
+    // the item is the whole of its (sequence, group) and writes the output;
+    // else its partials go to workspace rows dest + (query head within group).
     struct Item {
-        int s, gp, hg, nparts, ws_row, n, nblk, lo, hi;
+        int s, hg, n, nblk, lo, hi, dest;
     };
+    // Item mode (caller-fixed partition length, cascade suffixes): partition gp
+    // of every group, items dealt round-robin to the CTAs.
     auto item_of = [&](int item) {
         Item it;
-        it.gp = item / groups;
-        it.hg = item - it.gp * groups;
+        const int gp = item / groups;
+        it.hg = item - gp * groups;
         int a = 0, b = B - 1;
         while (a < b) {
             const int mid = (a + b + 1) >> 1;
-            if (sm_off[mid] <= it.gp) a = mid; else b = mid - 1;
+            if (sm_off[mid] <= gp) a = mid; else b = mid - 1;
         }
         it.s = a;
-        it.nparts = sm_off[a + 1] - sm_off[a] + p.prefix_parts;  // workspace rows of s
-        it.ws_row = it.gp + p.prefix_parts * (a + 1);            // this item's row
+        const int nparts = sm_off[a + 1] - sm_off[a] + p.prefix_parts;  // workspace rows of s
+        const int ws_row = gp + p.prefix_parts * (a + 1);               // this item's row
+        it.dest = nparts == 1 ? -1 : ws_row * Hq + it.hg * HPI * g;
         it.n = sm_len[a];
         it.nblk = (it.n + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
         // the k partitions of a sequence split its blocks evenly (sizes differ
         // by at most one, none above PB): a ragged last partition would leave
         // the CTAs that draw it idle at the end of the pass
-        const int k = sm_off[a + 1] - sm_off[a], i = it.gp - sm_off[a];
+        const int k = sm_off[a + 1] - sm_off[a], i = gp - sm_off[a];
         const int rest = max(it.nblk - p.skip_blocks, 0);
         it.lo = p.skip_blocks + (int)((long long)i * rest / k);
         it.hi = p.skip_blocks + (int)((long long)(i + 1) * rest / k);
         return it;
     };
+    // Even split: the U = groups * (total blocks) units, ordered (sequence,
+    // group, block), are cut into gridDim.x ranges of equal size; this CTA's
+    // range is a run of segments, each a whole (sequence, group) written
+    // straight to the output except possibly the first and the last, which
+    // leave partials in workspace slots 2c and 2c + 1 (c = this CTA).
+    const long long U = even ? (long long)groups * sm_off[B] : 0;
+    const long long u_begin = U * blockIdx.x / gridDim.x;
+    const long long u_end = U * (blockIdx.x + 1) / gridDim.x;
+    struct Cursor {
+        int item, s;
+        long long u;
+    };
+    auto cursor_begin = [&]() {
+        Cursor c;
+        c.item = blockIdx.x;
+        c.u = u_begin;
+        c.s = 0;
+        if (even && u_begin < u_end) {  // the sequence holding unit u_begin
+            int a = 0, b = B - 1;
+            while (a < b) {
+                const int mid = (a + b + 1) >> 1;
+                if ((long long)groups * sm_off[mid] <= u_begin) a = mid; else b = mid - 1;
+            }
+            c.s = a;
+        }
+        return c;
+    };
+    auto next_item = [&](Cursor& c, Item& it) -> bool {
+        if (!even) {
+            if (c.item >= total_items) return false;
+            it = item_of(c.item);
+            c.item += gridDim.x;
+            return true;
+        }
+        if (c.u >= u_end) return false;
+        const int s = c.s;
+        const int nb = sm_off[s + 1] - sm_off[s];
+        const long long r = c.u - (long long)groups * sm_off[s];
+        const int hg = (int)(r / nb);
+        const int b0 = (int)(r - (long long)hg * nb);
+        const long long left = u_end - c.u;
+        const int len = (long long)(nb - b0) < left ? nb - b0 : (int)left;
+        it.s = s;
+        it.hg = hg;
+        it.n = sm_len[s];
+        it.nblk = nb;
+        it.lo = b0;
+        it.hi = b0 + len;
+        it.dest = (b0 == 0 && len == nb)
+                      ? -1
+                      : (2 * (int)blockIdx.x + (c.u == u_begin ? 0 : 1)) * (HPI * g);
+        c.u += len;
+        if (b0 + len == nb && hg == groups - 1) {  // on to the next sequence with blocks
+            int t = s + 1;
+            while (t < B && sm_off[t + 1] == sm_off[t]) ++t;
+            c.s = t;
+        }
+        return true;
+    };
+    if (even) {
+        // empty (or invalid) sequences have no units: their rows are zeros
+        for (int s = blockIdx.x; s < B; s += gridDim.x) {
+            if (sm_len[s] != 0) continue;
+            uint4* o = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + (size_t)s * Hq * D);
+            for (int x = tid; x < Hq * D / 8; x += kTmaThreads) o[x] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
 
     if (warp == NC) {
         // ------------------------------------------------------------ producer
@@ -751,8 +838,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             }
             return id;
         };
-        for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
-            const Item it = item_of(item);
+        Cursor cur = cursor_begin();
+        Item it;
+        while (next_item(cur, it)) {
             const int32_t* table = p.block_tables + (size_t)it.s * p.max_blocks_per_seq;
             const int h = it.hg * HPI + hl;
             int id_cur = bi < BB ? lane_id(table, it.lo, it.hi) : -1;
@@ -811,8 +899,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     const int gid = lane >> 2, tig = lane & 3;
     const T* __restrict__ q = static_cast<const T*>(p.q);
     int ncons = 0;  // stages this warp has consumed
-    for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
-        const Item it = item_of(item);
+    Cursor cur = cursor_begin();
+    Item it;
+    while (next_item(cur, it)) {
         const int s = it.s, n = it.n;
         const int h = it.hg * HPI + hl;
         // q fragment: column gid of the score MMA is query head h*g + gid
@@ -985,7 +1074,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                 acc[4] += e * u2.x; acc[5] += e * u2.y; acc[6] += e * u2.z; acc[7] += e * u2.w;
             }
             const int qh = (it.hg * HPI + hk) * g + hh;
-            if (it.nparts == 1) {
+            if (it.dest < 0) {
                 const float inv = L > 0.f ? 1.f / L : 0.f;
                 uint4 packed;
                 packed.x = E::pack(acc[0] * inv, acc[1] * inv);
@@ -995,7 +1084,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                 *reinterpret_cast<uint4*>(static_cast<T*>(p.out) + ((size_t)s * Hq + qh) * D +
                                           d0) = packed;
             } else {
-                const size_t row = (size_t)it.ws_row * Hq + qh;
+                const size_t row = (size_t)it.dest + hk * g + hh;
                 float* dst = p.ws_o + row * D + d0;
                 *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
                 *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
@@ -1184,6 +1273,10 @@ struct MergeParams {
     void* out;
     int num_seqs, num_q_heads;
     int min_rows;  // merge sequences with at least this many workspace rows
+    // even split of the TMA pass (even_grid > 0): ws_offsets holds block
+    // offsets, and the CTAs that covered a (sequence, group) left its partials
+    // in their slots (two per CTA, even_heads query heads each)
+    int even_grid, even_heads, groups;
 };
 
 // Log-sum-exp merge of a sequence's partitions, one warp per (sequence, query head):
@@ -1198,11 +1291,43 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const MergeParams p) 
     if (wg >= p.num_seqs * p.num_q_heads) return;
     const int Hq = p.num_q_heads;
     const int s = wg / Hq, qh = wg - s * Hq;
-    const int off = p.ws_offsets[s];
-    const int np = p.ws_offsets[s + 1] - off;
-    if (np < p.min_rows) return;  // a one-row sequence was written by the partition pass
+    // the workspace rows of (s, qh): np of them, row(i) for i < np (-1: none)
+    int np;
+    size_t base = 0;
+    int c0 = 0, lq = 0;
+    long long U = 0, start = 0;
+    const long long G = p.even_grid;
+    if (G > 0) {
+        const int nb = p.ws_offsets[s + 1] - p.ws_offsets[s];
+        if (nb == 0) return;  // zeros, written by the partition pass
+        U = (long long)p.groups * p.ws_offsets[p.num_seqs];
+        const int hg = qh / p.even_heads;
+        lq = qh - hg * p.even_heads;
+        start = (long long)p.groups * p.ws_offsets[s] + (long long)hg * nb;
+        // CTA holding unit u: the largest c with floor(c * U / G) <= u
+        auto cta_of = [&](long long u) { return (int)(((u + 1) * G + U - 1) / U - 1); };
+        c0 = cta_of(start);
+        np = cta_of(start + nb - 1) - c0 + 1;
+        if (np < 2) return;  // one CTA covered it and wrote the output
+    } else {
+        const int off = p.ws_offsets[s];
+        np = p.ws_offsets[s + 1] - off;
+        if (np < p.min_rows) return;  // a one-row sequence was written by the partition pass
+        base = (size_t)off * Hq + qh;
+    }
+    auto row_of = [&](int i) -> long long {
+        if (G == 0) return (long long)(base + (size_t)i * Hq);
+        const long long c = c0 + i;
+        const long long b = c * U / G;
+        if (b == (c + 1) * U / G) return -1;  // a CTA with no units (U < G)
+        const long long slot = (i == 0 && b < start) ? 2 * c + 1 : 2 * c;
+        return slot * p.even_heads + lq;
+    };
     float M = -INFINITY;
-    for (int i = lane; i < np; i += 32) M = fmaxf(M, p.ws_m[(size_t)(off + i) * Hq + qh]);
+    for (int i = lane; i < np; i += 32) {
+        const long long r = row_of(i);
+        if (r >= 0) M = fmaxf(M, p.ws_m[r]);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float Ms = M == -INFINITY ? 0.f : M;
@@ -1212,7 +1337,9 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const MergeParams p) 
     for (int e = 0; e < PER; ++e) acc[e] = 0.f;
 #pragma unroll 4
     for (int i = 0; i < np; ++i) {
-        const size_t r = (size_t)(off + i) * Hq + qh;
+        const long long rr = row_of(i);
+        if (rr < 0) continue;
+        const size_t r = (size_t)rr;
         const float w = fast_exp2(p.ws_m[r] - Ms);
         L += w * p.ws_l[r];
         const float* src = p.ws_o + r * D + lane * PER;
@@ -1322,13 +1449,15 @@ int tma_stages(int head_dim, int num_seqs, int group) {
 // KV heads per TMA item.  One head per item keeps each consumer's share of a
 // partition long and the partials few; several heads per item fetch more of a
 // block's contiguous run at once and keep consumers busy when contexts are
-// short.  Rule, from a sweep of 1/2/4/8 heads per item on four workloads:
-// one head when unsplit (sequence, head) items already give every SM 4 of
-// them; otherwise the fewest heads that make max_blocks * heads >= 256, i.e.
+// short.  Rule, from sweeps of 1/2/4/8 heads per item on four workloads:
+// under an even split, the fewest heads that fetch 256 bytes of each row;
+// else one head when unsplit (sequence, head) items already give every SM 4
+// of them; otherwise the fewest heads that make max_blocks * heads >= 256, i.e.
 // at least 32 blocks per consumer of a longest sequence (28-layer steps with
 // 2..32-block contexts ran 1.12x faster at 8 heads per item than at 1).
 // PKV_HEADS_PER_ITEM=<n> or =all overrides.
-int tma_heads_per_item(int num_seqs, int max_blocks, int num_kv_heads) {
+int tma_heads_per_item(int num_seqs, int max_blocks, int num_kv_heads, int head_dim,
+                       bool even) {
     // consumers split evenly over the heads of an item, so a valid count
     // divides both the KV heads and the consumer warps
     auto valid = [&](int h) { return h >= 1 && num_kv_heads % h == 0 && kTmaConsumers % h == 0; };
@@ -1343,6 +1472,14 @@ int tma_heads_per_item(int num_seqs, int max_blocks, int num_kv_heads) {
         return h;
     }
     if (forced > 0) return valid(forced) ? forced : 1;
+    if (even) {
+        // an even split walks one head group of a sequence at a time: fetch
+        // at least 256 contiguous bytes of each row (one D = 64 head is 128;
+        // measured 1.17x faster with two heads per item there)
+        int h = std::max(1, 128 / head_dim);
+        while (h < num_kv_heads && !valid(h)) ++h;
+        return valid(h) ? h : 1;
+    }
     if ((long long)num_seqs * num_kv_heads >= 4ll * sm_count()) return 1;
     int hpi = 1;
     for (int h = 2; h <= kTmaConsumers; ++h) {
@@ -1363,18 +1500,48 @@ int tma_items_per_cta(int heads_per_item) {
 }
 
 template <typename T, int D>
-pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp, int pb_lower,
+pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp_in, int pb_lower,
                              int max_blocks, bool need_merge, int passes, int nstages,
                              cudaStream_t stream) {
     DecodeParams prm = prm_in;
+    MergeParams mp = mp_in;
+    const int sms = sm_count();
+    if (sms <= 0) return PKV_ERR_CUDA;
+    // The adaptive, non-cascade pass over long contexts splits the work
+    // evenly over the CTAs (measured: CTAs of the round-robin item split
+    // finished up to 17 % apart on lognormal lengths).  Short contexts (under
+    // kEvenMinBlocks blocks) keep items: cut evenly, nearly every sequence
+    // would span CTAs and need a merge (measured 1.2x slower on 2..32-block
+    // contexts).  A caller-fixed partition length or a cascade suffix keeps
+    // items of whole partitions.
+    const bool even = prm.prefix_parts == 0 && prm.partition_blocks <= 0 &&
+                      max_blocks >= kEvenMinBlocks;
+    // items cover `hpi` KV heads of one partition
+    const int hpi = tma_heads_per_item(prm.num_seqs, max_blocks, prm.num_kv_heads, D, even);
+    const int groups = prm.num_kv_heads / hpi;
+    int grid;
+    if (even) {
+        const long long units_upper = (long long)prm.num_seqs * groups * std::max(1, max_blocks);
+        grid = (int)std::max<long long>(1, std::min<long long>(units_upper,
+                                                              std::min(sms, kMaxEvenGrid)));
+        prm.even_split = 1;
+        mp.even_grid = grid;
+        mp.even_heads = hpi * prm.group;
+        mp.groups = groups;
+        need_merge = max_blocks > 1;  // a one-block (sequence, group) is never cut
+    } else {
+        const long long items_upper =
+            (long long)prm.num_seqs * std::max(1, ceil_div(max_blocks, pb_lower)) * groups;
+        grid = (int)std::max<long long>(1, std::min<long long>(items_upper, sms));
+        // per-head items: 8 per CTA; all-heads items carry Hkv heads each: 4 per CTA
+        prm.target_items = grid * tma_items_per_cta(hpi);
+    }
     if (passes & kPassPartition) {
         CUtensorMap tmk, tmv;
         const pkv_dtype dt = std::is_same<T, __nv_bfloat16>::value ? PKV_BF16 : PKV_F16;
         if (!make_pool_map(&tmk, prm.k_cache, prm.num_blocks, prm.num_kv_heads, D, dt) ||
             !make_pool_map(&tmv, prm.v_cache, prm.num_blocks, prm.num_kv_heads, D, dt))
             return PKV_ERR_CUDA;
-        // items cover `hpi` KV heads of one partition
-        const int hpi = tma_heads_per_item(prm.num_seqs, max_blocks, prm.num_kv_heads);
         auto kern = hpi == 1 ? decode_partition_tma_kernel<T, D, true>
                              : decode_partition_tma_kernel<T, D, false>;
         const size_t smem =
@@ -1382,14 +1549,6 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp, 
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
             return PKV_ERR_CUDA;
-        const int sms = sm_count();
-        if (sms <= 0) return PKV_ERR_CUDA;
-        const long long items_upper = (long long)prm.num_seqs *
-                                      std::max(1, ceil_div(max_blocks, pb_lower)) *
-                                      (prm.num_kv_heads / hpi);
-        const int grid = (int)std::max<long long>(1, std::min<long long>(items_upper, sms));
-        // per-head items: 8 per CTA; all-heads items carry Hkv heads each: 4 per CTA
-        prm.target_items = grid * tma_items_per_cta(hpi);
         kern<<<grid, kTmaThreads, smem, stream>>>(prm, tmk, tmv, nstages, hpi);
         if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
     }
@@ -1496,6 +1655,7 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
     prm.prefix_parts = prefix_parts;
     prm.min_partition_blocks = pb_lower;
     prm.target_items = 0;
+    prm.even_split = 0;
     prm.scale_log2 = scale * kLog2e;
 
     MergeParams mp;
@@ -1507,6 +1667,9 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
     mp.num_seqs = num_seqs;
     mp.num_q_heads = num_q_heads;
     mp.min_rows = prefix_parts > 0 ? 1 : 2;
+    mp.even_grid = 0;  // the TMA pass sets the even-split fields
+    mp.even_heads = 0;
+    mp.groups = 0;
 
     // partition kernel (TMA pipeline or register pipeline) and merge kernel
     // the TMA kernel maps its 8 consumer warps onto the KV heads (Hkv must divide 8)

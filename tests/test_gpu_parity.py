@@ -129,11 +129,39 @@ def test_partition_length_invariance(name, cuda_device):
     assert pkv.pkv_device_status() == 0
 
 
-def _custom(dev, dtype, lens, Hq, Hkv, D, NB, seed, poison=True):
+def _custom(dev, dtype, lens, Hq, Hkv, D, NB, seed, poison=True, table_blocks=None):
     w = wl.Workload("custom", seed, len(lens), Hq, Hkv, D, NB, dtype,
                     "fixed:" + ",".join(str(n) for n in lens),
-                    max(1, (max(lens) + 15) // 16))
+                    table_blocks or max(1, (max(lens) + 15) // 16))
     return w, wl.make_inputs(w, device=dev, num_layers=1, poison=poison)
+
+
+@pytest.mark.parametrize("dtype,Hkv,D", [("bf16", 8, 128), ("f16", 2, 128), ("bf16", 4, 64)])
+def test_even_split_edge_cases(dtype, Hkv, D, cuda_device):
+    """The adaptive pass cuts the (sequence, head group, block) units evenly over
+    the CTAs: fewer units than CTAs (a wide table and a large length bound, so
+    most CTAs get nothing and a sequence's pieces sit in CTAs with empty ones
+    between them), empty sequences, and one long sequence cut across many CTAs
+    among short ones."""
+    cases = (([17, 0, 5, 1, 300], 4096, 256),
+             ([3000] + [1 + (7 * i) % 40 for i in range(50)], 3000, None))
+    for k, (lens, bound, tb) in enumerate(cases):
+        w, inp = _custom(cuda_device, dtype, lens, 4 * Hkv, Hkv, D, 600, seed=90 + k,
+                         table_blocks=tb)
+        keep = np.array([i for i, n in enumerate(lens) if n > 0])
+        empty = [i for i, n in enumerate(lens) if n == 0]
+        want, _, _ = compact_oracle_step(inp, keep)
+        q = inp["q"]
+        out = torch.full_like(q, float("nan"))
+        ws = pkv.new_workspace(w.num_seqs, w.num_q_heads, w.head_dim, bound, cuda_device)
+        pkv.paged_kv_decode_step(q, inp["k_new"][0], inp["v_new"][0], inp["k_cache"][0],
+                                 inp["v_cache"][0], inp["block_tables"], inp["context_lens"],
+                                 bound, w.scale, out, ws)
+        torch.cuda.synchronize()
+        assert pkv.pkv_device_status() == 0
+        for i in empty:
+            assert torch.count_nonzero(out[i]) == 0
+        assert_attention_close(bits(out)[keep], want, dtype_code(w), f"case {k}")
 
 
 @pytest.mark.parametrize("dtype,Hq,Hkv,D", [("bf16", 8, 8, 128), ("f16", 8, 1, 64),
