@@ -1,7 +1,11 @@
 // pkv_prefill.cu -- chunked-prefill attention over the paged cache.
 #include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <type_traits>
 
 #include "pkv_internal.cuh"
+#include "pkv_tc.cuh"
 #include "pkv_tma.cuh"
 
 namespace pkv {
@@ -253,13 +257,366 @@ __global__ void __launch_bounds__(kPrefillThreads)
     }
 }
 
+// ============================================================================
+// Chunked prefill on the 5th-generation tensor cores (the default).
+//
+// The same work split as above, with tiles of 128 (query token, query head)
+// rows and key tiles of 128 tokens (8 paged blocks):
+//   warp 0   TMA-loads the K blocks of each key tile into a 2-stage ring,
+//   warp 3   the V blocks into another (and marks blocks with bad ids),
+//   warp 1   (one thread) issues S(j) = Q K(j)^T into one of two tensor-memory
+//            score buffers, then O += P(j-1) V(j-1) into the tensor-memory
+//            output, each as tcgen05.mma over 128-byte swizzled shared
+//            memory (Q, K: K-major; P: K-major; V: MN-major), completion
+//            signalled through mbarriers;
+//   warps 4-7 (one thread per row) read S(j) from tensor memory, mask it
+//            (causal, bad blocks), run the online softmax and write P(j) as
+//            16-bit values into shared memory for the next MMA.
+// The output is rescaled only when a row's running maximum grows by more
+// than 2^8 (P then stays <= 256; the final O / l is unchanged), so most tiles
+// never touch O between MMAs.  V rows that no row of the tile may see (past
+// the causal bound, in a bad block, or never loaded) are zeroed before the
+// last P V so that no 0 x NaN reaches the accumulator.  Waits are bounded.
+// ============================================================================
+constexpr int kTcThreads = 256;
+constexpr int kTcRows = 128;     // (query token, query head) rows per tile
+constexpr int kTcKeys = 128;     // keys per key tile
+constexpr float kTcRescale = 8.f;  // log2 of the largest P before O is rescaled
+
 template <typename T, int D>
-pkv_status launch_prefill(const PrefillParams& prm, const void* k_cache, const void* v_cache,
-                          int num_blocks, int num_kv_heads, pkv_dtype dtype, cudaStream_t stream) {
+__global__ void __launch_bounds__(kTcThreads, 1)
+    prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmap_k,
+                      const __grid_constant__ CUtensorMap tmap_v) {
+    using E = Elem<T>;
+    constexpr int HALVES = D / 64;
+    constexpr int REG = kTcRows * 128;     // one 64-element half of 128 rows: 16 KB
+    constexpr int TILE = HALVES * REG;     // Q tile, or one K or V key tile
+    constexpr int PBYTES = 2 * REG;        // P: 128 rows x 128 keys
+    constexpr uint32_t kCols = 512;        // S0, S1 (128 columns each), O (D columns)
+    constexpr uint32_t kOCol = 256;
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    unsigned char* sq = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    unsigned char* sk = sq + TILE;          // 2 stages
+    unsigned char* sv = sk + 2 * TILE;      // 2 stages
+    unsigned char* sp = sv + 2 * TILE;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sp + PBYTES);
+    uint64_t* k_full = bars + 0;
+    uint64_t* k_empty = bars + 2;
+    uint64_t* v_full = bars + 4;
+    uint64_t* v_empty = bars + 6;
+    uint64_t* s_full = bars + 8;
+    uint64_t* s_free = bars + 10;
+    uint64_t* p_full = bars + 12;
+    uint64_t* pv_done = bars + 13;
+    uint64_t* mma_idle = bars + 14;
+    int* vbad = reinterpret_cast<int*>(bars + 16);           // [2] bad-block bits per V stage
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(vbad + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // heaviest tiles (last query rows: longest causal range) first
+    const int per_tile = p.num_seqs * p.num_kv_heads;
+    const int tile = p.tiles_per_seq - 1 - (int)(blockIdx.x / per_tile);
+    const int rem = blockIdx.x % per_tile;
+    const int s = rem / p.num_kv_heads, h = rem % p.num_kv_heads;
+    const int g = p.group, Hq = p.num_q_heads;
+    const int q0 = p.cu_q_lens[s], qlen = p.cu_q_lens[s + 1] - q0;
+    const int n = p.context_lens[s];
+    if (qlen <= 0 || n < qlen || n > p.max_blocks_per_seq * PKV_BLOCK_SIZE) {
+        if (tid == 0 && tile == 0 && h == 0 && (qlen < 0 || n < qlen ||
+                                                 n > p.max_blocks_per_seq * PKV_BLOCK_SIZE))
+            atomicOr(p.status, PKV_DEV_BAD_LENGTH);
+        return;
+    }
+    const int row0 = tile * kTcRows;
+    if (row0 >= qlen * g) return;
+    const int tok_last = min(qlen, (row0 + kTcRows + g - 1) / g) - 1;
+    const int p_last = n - qlen + tok_last;              // largest query position of the tile
+    const int nblk = p_last / PKV_BLOCK_SIZE + 1;        // blocks the tile reads
+    const int nkv = (nblk + 7) / 8;                      // key tiles
+
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_free[i], 4);
+        }
+        mbar_init(p_full, 4);
+        mbar_init(pv_done, 1);
+        mbar_init(mma_idle, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    if (warp == 2) tc_alloc(tmem_slot, kCols);
+    // Q rows (token t, head h*g + t's head) as the K-major A operand
+    {
+        const T* qb = static_cast<const T*>(p.q);
+        constexpr int CH = D / 8;  // 16-byte chunks per row
+        for (int x = tid; x < kTcRows * CH; x += kTcThreads) {
+            const int r = x / CH, c = x - r * CH;
+            const int R = row0 + r, t = R / g;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (t < qlen)
+                v = *reinterpret_cast<const uint4*>(
+                    qb + ((size_t)(q0 + t) * Hq + h * g + (R - t * g)) * D + c * 8);
+            *reinterpret_cast<uint4*>(sq + (c >> 3) * REG + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
+        }
+    }
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0 || warp == 3) {
+        // ------------------------------------------------ K (warp 0) / V (warp 3) producers
+        const bool isk = warp == 0;
+        const CUtensorMap* map = isk ? &tmap_k : &tmap_v;
+        uint64_t* full = isk ? k_full : v_full;
+        uint64_t* empty = isk ? k_empty : v_empty;
+        unsigned char* ring = isk ? sk : sv;
+        const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
+        int issued = 0;
+        for (int j = 0; j < nkv; ++j) {
+            const int b = j & 1, ph = (j >> 1) & 1;
+            bool ok = mbar_wait(&empty[b], ph ^ 1, abort_flag, p.status);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            const int nb = min(8, nblk - 8 * j);
+            int id = 0;
+            bool bad = false;
+            if (lane < nb) {
+                id = table[8 * j + lane];
+                bad = id < 0 || id >= p.num_blocks;
+                if (bad) id = 0;  // fetched, then masked and zeroed
+            }
+            const unsigned badm = __ballot_sync(0xffffffffu, bad);
+            if (lane == 0) {
+                if (isk && badm) atomicOr(p.status, PKV_DEV_BAD_BLOCK_ID);
+                if (!isk) vbad[b] = (int)badm;
+                mbar_arrive_expect_tx(&full[b], (uint32_t)(nb * HALVES * 2048));
+            }
+            __syncwarp();
+            if (lane < nb) {
+#pragma unroll
+                for (int hh = 0; hh < HALVES; ++hh)
+                    tma_load_rows(ring + b * TILE + hh * REG + lane * 2048, map, &full[b], hh * 64,
+                                  h, id * PKV_BLOCK_SIZE);
+            }
+            issued = j + 1;
+        }
+        // every copy issued must land before the CTA may exit
+        if (lane == 0)
+            for (int j = max(0, issued - 2); j < issued; ++j)
+                mbar_drain(&full[j & 1], (j >> 1) & 1, p.status);
+    } else if (warp == 1) {
+        // ------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+            const uint32_t id_s = tc_idesc_f16(kBf16, kTcRows, kTcKeys, 0, 0);
+            const uint32_t id_pv = tc_idesc_f16(kBf16, kTcRows, D, 0, 1);
+            const uint32_t aq = smem_addr(sq), ak = smem_addr(sk), av = smem_addr(sv),
+                           ap = smem_addr(sp);
+            auto issue_pv = [&](int i) -> bool {
+                const int bi = i & 1;
+                if (!mbar_wait(&v_full[bi], (i >> 1) & 1, abort_flag, p.status)) return false;
+                if (!mbar_wait(p_full, i & 1, abort_flag, p.status)) return false;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kTcKeys / 16; ++kk)
+                    tc_mma(tmem + kOCol,
+                           tc_smem_desc(ap + (kk >> 2) * REG + (kk & 3) * 32, 16, 1024),
+                           tc_smem_desc(av + bi * TILE + kk * 2048, REG, 1024), id_pv,
+                           i > 0 || kk > 0);
+                tc_commit(pv_done);
+                tc_commit(&v_empty[bi]);
+                return true;
+            };
+            bool live = true;
+            for (int j = 0; j < nkv && live; ++j) {
+                const int b = j & 1, ph = (j >> 1) & 1;
+                if (!mbar_wait(&k_full[b], ph, abort_flag, p.status)) break;
+                if (j >= 2 && !mbar_wait(&s_free[b], ph ^ 1, abort_flag, p.status)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks)
+                    tc_mma(tmem + b * kTcKeys,
+                           tc_smem_desc(aq + (ks >> 2) * REG + (ks & 3) * 32, 16, 1024),
+                           tc_smem_desc(ak + b * TILE + (ks >> 2) * REG + (ks & 3) * 32, 16, 1024),
+                           id_s, ks > 0);
+                tc_commit(&s_full[b]);
+                tc_commit(&k_empty[b]);
+                if (j >= 1) live = issue_pv(j - 1);
+            }
+            if (live && !*abort_flag) issue_pv(nkv - 1);
+            // nothing of this thread's may still run when tensor memory is freed
+            tc_commit(mma_idle);
+            mbar_drain(mma_idle, 0, p.status);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------- softmax, one thread per row
+        const int r = tid - 128;                              // row of the tile = TMEM lane
+        const uint32_t trow = tmem + ((uint32_t)(32 * (warp - 4)) << 16);
+        const int R = row0 + r, t = R / g;
+        const bool live_row = t < qlen;
+        const int pos = live_row ? n - qlen + t : -1;        // keys 0..pos are visible
+        const float sl2 = p.scale_log2;
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nkv; ++j) {
+            const int b = j & 1, ph = (j >> 1) & 1;
+            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[b], ph, abort_flag, p.status));
+            if (!ok) break;
+            tc_fence_after();
+            float sc[kTcKeys];
+#pragma unroll
+            for (int c = 0; c < kTcKeys / 32; ++c)
+                tc_ld32(trow + b * kTcKeys + 32 * c, reinterpret_cast<uint32_t(&)[32]>(sc[32 * c]));
+            tc_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_free[b]);
+            ok = __all_sync(0xffffffffu, mbar_wait(&v_full[b], ph, abort_flag, p.status));
+            if (!ok) break;
+            const unsigned bad = (unsigned)vbad[b];
+            const int key0 = kTcKeys * j;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kTcKeys; ++c) {
+                const bool vis = key0 + c <= pos && !((bad >> (c >> 4)) & 1u);
+                sc[c] = vis ? sc[c] * sl2 : -INFINITY;   // select: never scale garbage into use
+                mx = fmaxf(mx, sc[c]);
+            }
+            const float m_new = fmaxf(m_used, mx);
+            // lazy rescale of O (whole warp: tensor-memory access is warp-wide)
+            const bool grow = m_used != -INFINITY && m_new > m_used + kTcRescale;
+            if (j >= 1) {
+                // P(j) overwrites P(j-1), and O may be rescaled: P(j-1) V(j-1) must be done
+                ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (j - 1) & 1, abort_flag, p.status));
+                if (!ok) break;
+                tc_fence_after();
+            }
+            if (__any_sync(0xffffffffu, grow)) {
+                const float f = grow ? fast_exp2(m_used - m_new) : 1.f;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tc_ld32(trow + kOCol + 32 * c, o);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                    tc_st32(trow + kOCol + 32 * c, o);
+                }
+                tc_wait_st();
+                l *= f;
+            }
+            if (m_used == -INFINITY || grow) m_used = m_new;
+            const float ms = m_used == -INFINITY ? 0.f : m_used;
+            // P row: 16 chunks of 8 keys; chunk c in half c / 8 of the P tile
+#pragma unroll
+            for (int c = 0; c < kTcKeys / 8; ++c) {
+                uint32_t w4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float p0 = fast_exp2(sc[8 * c + 2 * e] - ms);
+                    const float p1 = fast_exp2(sc[8 * c + 2 * e + 1] - ms);
+                    l += p0 + p1;
+                    w4[e] = E::pack(p0, p1);
+                }
+                *reinterpret_cast<uint4*>(sp + (c >> 3) * REG + r * 128 +
+                                          (((c & 7) ^ (r & 7)) << 4)) =
+                    make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+            // V rows no row may see must be finite zeros before P V (0 x NaN = NaN)
+            if (j == nkv - 1 || bad) {
+                unsigned char* vt = sv + b * TILE;
+                for (int x = r; x < kTcKeys * 8 * HALVES; x += 128) {
+                    const int key = x / (8 * HALVES), rest = x - key * (8 * HALVES);
+                    if (key0 + key <= p_last && !((bad >> (key >> 4)) & 1u)) continue;
+                    *reinterpret_cast<uint4*>(vt + (rest >> 3) * REG + key * 128 + ((rest & 7) << 4)) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+            tc_fence_before();  // the rescaled O is ordered before the next MMA
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+        }
+        // epilogue: O / l for the live rows
+        if (ok && !*abort_flag) {
+            ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (nkv - 1) & 1, abort_flag, p.status));
+            if (ok) {
+                tc_fence_after();
+                const float inv = l > 0.f ? 1.f / l : 0.f;
+                T* dst = static_cast<T*>(p.out) +
+                         ((size_t)(q0 + (live_row ? t : 0)) * Hq + h * g + (R - t * g)) * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tc_ld32(trow + kOCol + 32 * c, o);
+                    tc_wait_ld();
+                    if (live_row) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            *reinterpret_cast<uint4*>(dst + 32 * c + 8 * e) = make_uint4(
+                                E::pack(__uint_as_float(o[8 * e]) * inv, __uint_as_float(o[8 * e + 1]) * inv),
+                                E::pack(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv),
+                                E::pack(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv),
+                                E::pack(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv));
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tc_dealloc(tmem, kCols);
+    }
+}
+
+template <int D>
+size_t prefill_tc_smem() {
+    return 1024 + (size_t)5 * (D / 64) * kTcRows * 128 + 2 * kTcRows * 128 + 256;
+}
+
+// Which prefill kernel runs: the tcgen05 one unless PKV_PREFILL_KERNEL=mma
+// selects the mma.sync kernel (kept for comparison).
+bool use_tc_prefill() {
+    static const bool tc = [] {
+        const char* v = std::getenv("PKV_PREFILL_KERNEL");
+        return !(v && std::strcmp(v, "mma") == 0);
+    }();
+    return tc;
+}
+
+template <typename T, int D>
+pkv_status launch_prefill(const PrefillParams& prm_in, const void* k_cache, const void* v_cache,
+                          int num_blocks, int num_kv_heads, int max_q_len, pkv_dtype dtype,
+                          cudaStream_t stream) {
     CUtensorMap tmk, tmv;
     if (!make_pool_map(&tmk, k_cache, num_blocks, num_kv_heads, D, dtype) ||
         !make_pool_map(&tmv, v_cache, num_blocks, num_kv_heads, D, dtype))
         return PKV_ERR_CUDA;
+    PrefillParams prm = prm_in;
+    if (use_tc_prefill()) {
+        prm.tiles_per_seq = ceil_div(max_q_len * prm.group, kTcRows);
+        auto kern = prefill_tc_kernel<T, D>;
+        const size_t smem = prefill_tc_smem<D>();
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return PKV_ERR_CUDA;
+        const long long grid = (long long)prm.num_seqs * num_kv_heads * prm.tiles_per_seq;
+        if (grid > 0x7fffffffll) return PKV_ERR_UNSUPPORTED;
+        kern<<<(unsigned)grid, kTcThreads, smem, stream>>>(prm, tmk, tmv);
+        return cuda_status(cudaGetLastError());
+    }
+    prm.tiles_per_seq = ceil_div(max_q_len * prm.group, kPrefillRows);
     auto kern = prefill_tma_kernel<T, D>;
     const size_t smem = 1024 + (size_t)kPrefillStages * (2 * 16 * D * 2) + kPrefillStages * 20 + 16;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
@@ -311,19 +668,19 @@ pkv_status paged_attention_prefill(const void* q, const void* k_cache, const voi
     prm.group = g;
     prm.max_blocks_per_seq = max_blocks_per_seq;
     prm.num_blocks = num_blocks;
-    prm.tiles_per_seq = pkv::ceil_div(max_q_len * g, pkv::kPrefillRows);
+    prm.tiles_per_seq = 0;  // set by the launcher for the kernel it picks
     prm.scale_log2 = scale * pkv::kLog2e;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (dtype == PKV_BF16)
         return head_dim == 128
                    ? pkv::launch_prefill<__nv_bfloat16, 128>(prm, k_cache, v_cache, num_blocks,
-                                                            num_kv_heads, dtype, st)
+                                                            num_kv_heads, max_q_len, dtype, st)
                    : pkv::launch_prefill<__nv_bfloat16, 64>(prm, k_cache, v_cache, num_blocks,
-                                                           num_kv_heads, dtype, st);
+                                                           num_kv_heads, max_q_len, dtype, st);
     return head_dim == 128 ? pkv::launch_prefill<__half, 128>(prm, k_cache, v_cache, num_blocks,
-                                                              num_kv_heads, dtype, st)
+                                                              num_kv_heads, max_q_len, dtype, st)
                            : pkv::launch_prefill<__half, 64>(prm, k_cache, v_cache, num_blocks,
-                                                             num_kv_heads, dtype, st);
+                                                             num_kv_heads, max_q_len, dtype, st);
 }
 
 }  // extern "C"

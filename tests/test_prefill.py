@@ -99,3 +99,45 @@ def test_prefill_flags_a_chunk_longer_than_its_context(cuda_device):
     torch.cuda.synchronize()
     assert pkv.pkv_device_status(reset=True) & pkv.DEV_BAD_LENGTH
     assert torch.count_nonzero(out[8:]) == 0       # the bad sequence was skipped
+
+
+def test_prefill_long_chunk_over_a_cached_prefix(cuda_device):
+    """Many 128-row tiles and key tiles: a 400-token chunk after 1600 cached
+    tokens, beside a whole 1200-token prompt."""
+    specs = [(2000, 400), (1200, 1200), (129, 129)]
+    c = _case(cuda_device, "bf16", specs, 16, 4, 128, seed=41)
+    out, want, code, _, _ = _run(c, 128, cuda_device)
+    assert_attention_close(bits(out), want, code, "long chunk")
+
+
+def test_prefill_rescales_when_scores_grow(cuda_device):
+    """Scores that climb along the context move a row's running maximum by far
+    more than the kernel lets P grow, so the output is rescaled between tiles."""
+    specs = [(1100, 600), (700, 700)]
+    c = _case(cuda_device, "f16", specs, 8, 2, 128, seed=43)
+    # K of token t scaled by (1 + t / 64): later keys score ever higher
+    need = [(n + 15) // 16 for n, _ in specs]
+    for s, (n, _) in enumerate(specs):
+        sl = token_slots(c["tables"][s], 16 * need[s])
+        for t in range(n - specs[s][1]):
+            row = c["kc"].view(-1, 2, 128)[sl[t]]
+            c["kc"].view(-1, 2, 128)[sl[t]] = (row.float() * (1 + t / 64)).to(row.dtype)
+    c["kn"] = (c["kn"].float() * 12).to(c["kn"].dtype)
+    c["q"] = (c["q"].float() * 2).to(c["q"].dtype)
+    out, want, code, _, _ = _run(c, 128, cuda_device)
+    assert_attention_close(bits(out), want, code, "growing scores")
+
+
+def test_prefill_flags_a_bad_block_id(cuda_device):
+    c = _case(cuda_device, "bf16", [(300, 300)], 8, 2, 128, seed=47)
+    _run(c, 128, cuda_device)
+    tables = c["tables"].copy()
+    tables[0, 5] = 1 << 30
+    out = torch.full_like(c["q"], float("nan"))
+    pkv.paged_attention_prefill(c["q"], c["kc"], c["vc"], torch.from_numpy(tables).to(cuda_device),
+                                torch.from_numpy(c["lens"]).to(cuda_device),
+                                torch.from_numpy(c["cu"]).to(cuda_device), c["maxq"],
+                                128 ** -0.5, out)
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_status(reset=True) & pkv.DEV_BAD_BLOCK_ID
+    assert torch.isfinite(out.float()).all()
