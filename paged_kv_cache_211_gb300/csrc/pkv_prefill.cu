@@ -291,7 +291,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr int HALVES = D / 64;
     constexpr int REG = kTcRows * 128;     // one 64-element half of 128 rows: 16 KB
     constexpr int TILE = HALVES * REG;     // Q tile, or one K or V key tile
-    constexpr int PBYTES = 2 * REG;        // P: 128 rows x 128 keys
+    constexpr int PBYTES = 2 * REG;        // one P buffer: 128 rows x 128 keys (two of them)
     constexpr uint32_t kCols = 512;        // S0, S1 (128 columns each), O (D columns)
     constexpr uint32_t kOCol = 256;
     extern __shared__ unsigned char smem_raw[];
@@ -299,8 +299,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     unsigned char* sq = smem_raw + (((raw + 1023u) & ~1023u) - raw);
     unsigned char* sk = sq + TILE;          // 2 stages
     unsigned char* sv = sk + 2 * TILE;      // 2 stages
-    unsigned char* sp = sv + 2 * TILE;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sp + PBYTES);
+    unsigned char* sp = sv + 2 * TILE;      // 2 buffers
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sp + 2 * PBYTES);
     uint64_t* k_full = bars + 0;
     uint64_t* k_empty = bars + 2;
     uint64_t* v_full = bars + 4;
@@ -308,9 +308,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t* s_full = bars + 8;
     uint64_t* s_free = bars + 10;
     uint64_t* p_full = bars + 12;
-    uint64_t* pv_done = bars + 13;
-    uint64_t* mma_idle = bars + 14;
-    int* vbad = reinterpret_cast<int*>(bars + 16);           // [2] bad-block bits per V stage
+    uint64_t* pv_done = bars + 14;
+    uint64_t* mma_idle = bars + 16;
+    int* vbad = reinterpret_cast<int*>(bars + 18);           // [2] bad-block bits per V stage
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(vbad + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -344,9 +344,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&v_empty[i], 1);
             mbar_init(&s_full[i], 1);
             mbar_init(&s_free[i], 4);
+            mbar_init(&p_full[i], 4);
+            mbar_init(&pv_done[i], 1);
         }
-        mbar_init(p_full, 4);
-        mbar_init(pv_done, 1);
         mbar_init(mma_idle, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
@@ -420,26 +420,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t id_pv = tc_idesc_f16(kBf16, kTcRows, D, 0, 1);
             const uint32_t aq = smem_addr(sq), ak = smem_addr(sk), av = smem_addr(sv),
                            ap = smem_addr(sp);
+            // P(i) V(i) into O; P(i) and V(i) sit in buffer / stage i % 2
             auto issue_pv = [&](int i) -> bool {
-                const int bi = i & 1;
-                if (!mbar_wait(&v_full[bi], (i >> 1) & 1, abort_flag, p.status)) return false;
-                if (!mbar_wait(p_full, i & 1, abort_flag, p.status)) return false;
+                const int bi = i & 1, phi = (i >> 1) & 1;
+                if (!mbar_wait(&v_full[bi], phi, abort_flag, p.status)) return false;
+                if (!mbar_wait(&p_full[bi], phi, abort_flag, p.status)) return false;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < kTcKeys / 16; ++kk)
                     tc_mma(tmem + kOCol,
-                           tc_smem_desc(ap + (kk >> 2) * REG + (kk & 3) * 32, 16, 1024),
+                           tc_smem_desc(ap + bi * PBYTES + (kk >> 2) * REG + (kk & 3) * 32, 16,
+                                        1024),
                            tc_smem_desc(av + bi * TILE + kk * 2048, REG, 1024), id_pv,
                            i > 0 || kk > 0);
-                tc_commit(pv_done);
+                tc_commit(&pv_done[bi]);
                 tc_commit(&v_empty[bi]);
                 return true;
             };
-            bool live = true;
-            for (int j = 0; j < nkv && live; ++j) {
+            // S(j) = Q K(j)^T into score buffer j % 2 (free once softmax read S(j-2))
+            auto issue_s = [&](int j) -> bool {
                 const int b = j & 1, ph = (j >> 1) & 1;
-                if (!mbar_wait(&k_full[b], ph, abort_flag, p.status)) break;
-                if (j >= 2 && !mbar_wait(&s_free[b], ph ^ 1, abort_flag, p.status)) break;
+                if (!mbar_wait(&k_full[b], ph, abort_flag, p.status)) return false;
+                if (j >= 2 && !mbar_wait(&s_free[b], ph ^ 1, abort_flag, p.status)) return false;
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
@@ -449,9 +451,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                            id_s, ks > 0);
                 tc_commit(&s_full[b]);
                 tc_commit(&k_empty[b]);
-                if (j >= 1) live = issue_pv(j - 1);
+                return true;
+            };
+            // scores run two tiles ahead: S0, S1, PV0, S2, PV1, S3, ...
+            bool live = true;
+            for (int j = 0; j < min(2, nkv) && live; ++j) live = issue_s(j);
+            for (int i = 0; i < nkv && live; ++i) {
+                live = issue_pv(i);
+                if (live && i + 2 < nkv) live = issue_s(i + 2);
             }
-            if (live && !*abort_flag) issue_pv(nkv - 1);
             // nothing of this thread's may still run when tensor memory is freed
             tc_commit(mma_idle);
             mbar_drain(mma_idle, 0, p.status);
@@ -484,24 +492,49 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!ok) break;
             const unsigned bad = (unsigned)vbad[b];
             const int key0 = kTcKeys * j;
-            float mx = -INFINITY;
+            // Tiles below every row's causal bound with no bad block (most of
+            // them) need no mask: max over the raw scores, and the scale goes
+            // into the exponent's fma.  Others: select (never scale garbage
+            // into use), then the same exponent with a unit multiplier.
+            const bool plain = __all_sync(0xffffffffu, key0 + kTcKeys - 1 <= pos) && bad == 0u &&
+                               sl2 > 0.f;
+            float mx = -INFINITY, mul = sl2;
+            if (plain) {
 #pragma unroll
-            for (int c = 0; c < kTcKeys; ++c) {
-                const bool vis = key0 + c <= pos && !((bad >> (c >> 4)) & 1u);
-                sc[c] = vis ? sc[c] * sl2 : -INFINITY;   // select: never scale garbage into use
-                mx = fmaxf(mx, sc[c]);
+                for (int c = 0; c < kTcKeys; ++c) mx = fmaxf(mx, sc[c]);
+                mx *= sl2;
+            } else {
+                mul = 1.f;
+#pragma unroll
+                for (int c = 0; c < kTcKeys; ++c) {
+                    const bool vis = key0 + c <= pos && !((bad >> (c >> 4)) & 1u);
+                    sc[c] = vis ? sc[c] * sl2 : -INFINITY;
+                    mx = fmaxf(mx, sc[c]);
+                }
             }
             const float m_new = fmaxf(m_used, mx);
-            // lazy rescale of O (whole warp: tensor-memory access is warp-wide)
+            // lazy rescale: only when the maximum grew by more than 2^kTcRescale
             const bool grow = m_used != -INFINITY && m_new > m_used + kTcRescale;
-            if (j >= 1) {
-                // P(j) overwrites P(j-1), and O may be rescaled: P(j-1) V(j-1) must be done
-                ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (j - 1) & 1, abort_flag, p.status));
-                if (!ok) break;
-                tc_fence_after();
+            const float f = grow ? fast_exp2(m_used - m_new) : 1.f;
+            if (m_used == -INFINITY || grow) m_used = m_new;
+            const float ms = m_used == -INFINITY ? 0.f : m_used;
+            // P(j) in registers first: none of this waits on the tensor core
+            uint32_t pk[kTcKeys / 2];
+            float psum = 0.f;
+#pragma unroll
+            for (int c = 0; c < kTcKeys / 2; ++c) {
+                const float p0 = fast_exp2(fmaf(sc[2 * c], mul, -ms));
+                const float p1 = fast_exp2(fmaf(sc[2 * c + 1], mul, -ms));
+                psum += p0 + p1;
+                pk[c] = E::pack(p0, p1);
             }
             if (__any_sync(0xffffffffu, grow)) {
-                const float f = grow ? fast_exp2(m_used - m_new) : 1.f;
+                // O must hold P(j-1) V(j-1) before it is scaled (whole warp:
+                // tensor-memory access is warp-wide)
+                ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1,
+                                                       abort_flag, p.status));
+                if (!ok) break;
+                tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
@@ -512,25 +545,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tc_st32(trow + kOCol + 32 * c, o);
                 }
                 tc_wait_st();
-                l *= f;
             }
-            if (m_used == -INFINITY || grow) m_used = m_new;
-            const float ms = m_used == -INFINITY ? 0.f : m_used;
-            // P row: 16 chunks of 8 keys; chunk c in half c / 8 of the P tile
-#pragma unroll
-            for (int c = 0; c < kTcKeys / 8; ++c) {
-                uint32_t w4[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = fast_exp2(sc[8 * c + 2 * e] - ms);
-                    const float p1 = fast_exp2(sc[8 * c + 2 * e + 1] - ms);
-                    l += p0 + p1;
-                    w4[e] = E::pack(p0, p1);
-                }
-                *reinterpret_cast<uint4*>(sp + (c >> 3) * REG + r * 128 +
-                                          (((c & 7) ^ (r & 7)) << 4)) =
-                    make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            l = l * f + psum;
+            if (j >= 2) {
+                // P buffer b still feeds P(j-2) V(j-2) until that completes
+                ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[b], ((j - 2) >> 1) & 1, abort_flag,
+                                                       p.status));
+                if (!ok) break;
             }
+            // P row: 16 chunks of 8 keys; chunk c in half c / 8 of P buffer b
+            unsigned char* pb = sp + b * PBYTES;
+#pragma unroll
+            for (int c = 0; c < kTcKeys / 8; ++c)
+                *reinterpret_cast<uint4*>(pb + (c >> 3) * REG + r * 128 + (((c & 7) ^ (r & 7)) << 4)) =
+                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
             // V rows no row may see must be finite zeros before P V (0 x NaN = NaN)
             if (j == nkv - 1 || bad) {
                 unsigned char* vt = sv + b * TILE;
@@ -544,11 +572,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
             tc_fence_before();  // the rescaled O is ordered before the next MMA
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
+            if (lane == 0) mbar_arrive(&p_full[b]);
         }
         // epilogue: O / l for the live rows
         if (ok && !*abort_flag) {
-            ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (nkv - 1) & 1, abort_flag, p.status));
+            ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(nkv - 1) & 1], ((nkv - 1) >> 1) & 1,
+                                                   abort_flag, p.status));
             if (ok) {
                 tc_fence_after();
                 const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -582,7 +611,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 template <int D>
 size_t prefill_tc_smem() {
-    return 1024 + (size_t)5 * (D / 64) * kTcRows * 128 + 2 * kTcRows * 128 + 256;
+    return 1024 + (size_t)5 * (D / 64) * kTcRows * 128 + 4 * kTcRows * 128 + 256;
 }
 
 // Which prefill kernel runs: the tcgen05 one unless PKV_PREFILL_KERNEL=mma
