@@ -1,4 +1,5 @@
 // pkv_prefill.cu -- chunked-prefill attention over the paged cache.
+#include <algorithm>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -260,81 +261,102 @@ __global__ void __launch_bounds__(kPrefillThreads)
 // ============================================================================
 // Chunked prefill on the 5th-generation tensor cores (the default).
 //
-// The same work split as above, with tiles of 128 (query token, query head)
-// rows and key tiles of 128 tokens (8 paged blocks):
+// Work item: one sequence, one KV head and a tile of 128 (query token, query
+// head) rows; key tiles of 128 tokens (8 paged blocks).  A persistent CTA per
+// SM walks the items heaviest first (last query rows: longest causal range),
+// and its pipelines run on across items:
 //   warp 0   TMA-loads the K blocks of each key tile into a 2-stage ring,
 //   warp 3   the V blocks into another (and marks blocks with bad ids),
-//   warp 1   (one thread) issues S(j) = Q K(j)^T into one of two tensor-memory
-//            score buffers, then O += P(j-1) V(j-1) into the tensor-memory
-//            output, each as tcgen05.mma over 128-byte swizzled shared
-//            memory (Q, K: K-major; P: K-major; V: MN-major), completion
-//            signalled through mbarriers;
-//   warps 4-7 (one thread per row) read S(j) from tensor memory, mask it
-//            (causal, bad blocks), run the online softmax and write P(j) as
-//            16-bit values into shared memory for the next MMA.
-// The output is rescaled only when a row's running maximum grows by more
-// than 2^8 (P then stays <= 256; the final O / l is unchanged), so most tiles
-// never touch O between MMAs.  V rows that no row of the tile may see (past
-// the causal bound, in a bad block, or never loaded) are zeroed before the
-// last P V so that no 0 x NaN reaches the accumulator.  Waits are bounded.
+//   warp 2   owns tensor memory and copies each item's Q rows (cp.async)
+//            into one of two Q buffers while the previous item computes,
+//   warp 1   (one thread) issues S(J) = Q K(J)^T into one of two tensor-memory
+//            score buffers, two key tiles ahead of O += P(J) V(J) into the
+//            tensor-memory output, each as tcgen05.mma over 128-byte swizzled
+//            shared memory (Q, K, P K-major; V MN-major), with completion
+//            signalled through mbarriers,
+//   warps 4-7 (one thread per row) read S(J) from tensor memory, mask it
+//            (causal, bad blocks) where needed, run the online softmax, write
+//            P(J) as 16-bit values into shared memory, and at the end of an
+//            item read O, hand it back for the next item and store O / l.
+// O is rescaled only when a row's running maximum grows by more than 2^8 (P
+// then stays <= 256; O / l is unchanged), so most key tiles never touch O.  V
+// rows no row of the tile may see (past the causal bound, in a bad block, or
+// never loaded) are zeroed before P V so that no 0 x NaN reaches O.  Every
+// wait is bounded.
 // ============================================================================
 constexpr int kTcThreads = 256;
 constexpr int kTcRows = 128;     // (query token, query head) rows per tile
 constexpr int kTcKeys = 128;     // keys per key tile
 constexpr float kTcRescale = 8.f;  // log2 of the largest P before O is rescaled
 
+// One work item of the tensor-core prefill.
+struct TcItem {
+    int s, h, q0, qlen, n, row0, p_last, nblk, nkv;
+};
+
+// Item i of the heaviest-first order; false if it holds no rows (or its
+// sequence's lengths are invalid: flagged once, by the item of tile 0, head 0).
+__device__ __forceinline__ bool tc_item(const PrefillParams& p, int i, bool flag, TcItem& it) {
+    const int per_tile = p.num_seqs * p.num_kv_heads;
+    const int tile = p.tiles_per_seq - 1 - i / per_tile;
+    const int rem = i - (i / per_tile) * per_tile;
+    it.s = rem / p.num_kv_heads;
+    it.h = rem - it.s * p.num_kv_heads;
+    it.q0 = p.cu_q_lens[it.s];
+    it.qlen = p.cu_q_lens[it.s + 1] - it.q0;
+    it.n = p.context_lens[it.s];
+    if (it.qlen <= 0 || it.n < it.qlen || it.n > p.max_blocks_per_seq * PKV_BLOCK_SIZE) {
+        if (flag && tile == 0 && it.h == 0 &&
+            (it.qlen < 0 || it.n < it.qlen || it.n > p.max_blocks_per_seq * PKV_BLOCK_SIZE))
+            atomicOr(p.status, PKV_DEV_BAD_LENGTH);
+        return false;
+    }
+    const int g = p.group;
+    it.row0 = tile * kTcRows;
+    if (it.row0 >= it.qlen * g) return false;
+    const int tok_last = min(it.qlen, (it.row0 + kTcRows + g - 1) / g) - 1;
+    it.p_last = it.n - it.qlen + tok_last;
+    it.nblk = it.p_last / PKV_BLOCK_SIZE + 1;
+    it.nkv = (it.nblk + 7) / 8;
+    return true;
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmap_k,
-                      const __grid_constant__ CUtensorMap tmap_v) {
+                      const __grid_constant__ CUtensorMap tmap_v, int num_items) {
     using E = Elem<T>;
     constexpr int HALVES = D / 64;
     constexpr int REG = kTcRows * 128;     // one 64-element half of 128 rows: 16 KB
-    constexpr int TILE = HALVES * REG;     // Q tile, or one K or V key tile
-    constexpr int PBYTES = 2 * REG;        // one P buffer: 128 rows x 128 keys (two of them)
+    constexpr int TILE = HALVES * REG;     // a Q tile, or one K or V key tile
+    constexpr int PBYTES = 2 * REG;        // P: 128 rows x 128 keys
     constexpr uint32_t kCols = 512;        // S0, S1 (128 columns each), O (D columns)
     constexpr uint32_t kOCol = 256;
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
-    unsigned char* sq = smem_raw + (((raw + 1023u) & ~1023u) - raw);
-    unsigned char* sk = sq + TILE;          // 2 stages
+    unsigned char* sq = smem_raw + (((raw + 1023u) & ~1023u) - raw);   // 2 Q buffers
+    unsigned char* sk = sq + 2 * TILE;      // 2 stages
     unsigned char* sv = sk + 2 * TILE;      // 2 stages
-    unsigned char* sp = sv + 2 * TILE;      // 2 buffers
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sp + 2 * PBYTES);
+    unsigned char* sp = sv + 2 * TILE;      // 1 P buffer
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sp + PBYTES);
     uint64_t* k_full = bars + 0;
     uint64_t* k_empty = bars + 2;
     uint64_t* v_full = bars + 4;
     uint64_t* v_empty = bars + 6;
     uint64_t* s_full = bars + 8;
     uint64_t* s_free = bars + 10;
-    uint64_t* p_full = bars + 12;
-    uint64_t* pv_done = bars + 14;
-    uint64_t* mma_idle = bars + 16;
-    int* vbad = reinterpret_cast<int*>(bars + 18);           // [2] bad-block bits per V stage
+    uint64_t* q_full = bars + 12;
+    uint64_t* q_empty = bars + 14;
+    uint64_t* p_full = bars + 16;
+    uint64_t* pv_done = bars + 17;
+    uint64_t* o_free = bars + 18;
+    uint64_t* mma_idle = bars + 19;
+    int* vbad = reinterpret_cast<int*>(bars + 20);           // [2] bad-block bits per V stage
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(vbad + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    // heaviest tiles (last query rows: longest causal range) first
-    const int per_tile = p.num_seqs * p.num_kv_heads;
-    const int tile = p.tiles_per_seq - 1 - (int)(blockIdx.x / per_tile);
-    const int rem = blockIdx.x % per_tile;
-    const int s = rem / p.num_kv_heads, h = rem % p.num_kv_heads;
     const int g = p.group, Hq = p.num_q_heads;
-    const int q0 = p.cu_q_lens[s], qlen = p.cu_q_lens[s + 1] - q0;
-    const int n = p.context_lens[s];
-    if (qlen <= 0 || n < qlen || n > p.max_blocks_per_seq * PKV_BLOCK_SIZE) {
-        if (tid == 0 && tile == 0 && h == 0 && (qlen < 0 || n < qlen ||
-                                                 n > p.max_blocks_per_seq * PKV_BLOCK_SIZE))
-            atomicOr(p.status, PKV_DEV_BAD_LENGTH);
-        return;
-    }
-    const int row0 = tile * kTcRows;
-    if (row0 >= qlen * g) return;
-    const int tok_last = min(qlen, (row0 + kTcRows + g - 1) / g) - 1;
-    const int p_last = n - qlen + tok_last;              // largest query position of the tile
-    const int nblk = p_last / PKV_BLOCK_SIZE + 1;        // blocks the tile reads
-    const int nkv = (nblk + 7) / 8;                      // key tiles
 
     if (tid == 0) {
         for (int i = 0; i < 2; ++i) {
@@ -344,29 +366,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&v_empty[i], 1);
             mbar_init(&s_full[i], 1);
             mbar_init(&s_free[i], 4);
-            mbar_init(&p_full[i], 4);
-            mbar_init(&pv_done[i], 1);
+            mbar_init(&q_full[i], 1);
+            mbar_init(&q_empty[i], 1);
         }
+        mbar_init(p_full, 4);
+        mbar_init(pv_done, 1);
+        mbar_init(o_free, 4);
         mbar_init(mma_idle, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     if (warp == 2) tc_alloc(tmem_slot, kCols);
-    // Q rows (token t, head h*g + t's head) as the K-major A operand
-    {
-        const T* qb = static_cast<const T*>(p.q);
-        constexpr int CH = D / 8;  // 16-byte chunks per row
-        for (int x = tid; x < kTcRows * CH; x += kTcThreads) {
-            const int r = x / CH, c = x - r * CH;
-            const int R = row0 + r, t = R / g;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (t < qlen)
-                v = *reinterpret_cast<const uint4*>(
-                    qb + ((size_t)(q0 + t) * Hq + h * g + (R - t * g)) * D + c * 8);
-            *reinterpret_cast<uint4*>(sq + (c >> 3) * REG + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
-        }
-    }
-    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -379,39 +389,75 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint64_t* full = isk ? k_full : v_full;
         uint64_t* empty = isk ? k_empty : v_empty;
         unsigned char* ring = isk ? sk : sv;
-        const int32_t* table = p.block_tables + (size_t)s * p.max_blocks_per_seq;
-        int issued = 0;
-        for (int j = 0; j < nkv; ++j) {
-            const int b = j & 1, ph = (j >> 1) & 1;
-            bool ok = mbar_wait(&empty[b], ph ^ 1, abort_flag, p.status);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            const int nb = min(8, nblk - 8 * j);
-            int id = 0;
-            bool bad = false;
-            if (lane < nb) {
-                id = table[8 * j + lane];
-                bad = id < 0 || id >= p.num_blocks;
-                if (bad) id = 0;  // fetched, then masked and zeroed
-            }
-            const unsigned badm = __ballot_sync(0xffffffffu, bad);
-            if (lane == 0) {
-                if (isk && badm) atomicOr(p.status, PKV_DEV_BAD_BLOCK_ID);
-                if (!isk) vbad[b] = (int)badm;
-                mbar_arrive_expect_tx(&full[b], (uint32_t)(nb * HALVES * 2048));
-            }
-            __syncwarp();
-            if (lane < nb) {
+        int J = 0;  // key tiles issued by this CTA
+        bool live = true;
+        for (int i = blockIdx.x; i < num_items && live; i += gridDim.x) {
+            TcItem it;
+            if (!tc_item(p, i, isk && lane == 0, it)) continue;
+            const int32_t* table = p.block_tables + (size_t)it.s * p.max_blocks_per_seq;
+            for (int j = 0; j < it.nkv; ++j, ++J) {
+                const int b = J & 1, ph = (J >> 1) & 1;
+                live = __all_sync(0xffffffffu, mbar_wait(&empty[b], ph ^ 1, abort_flag, p.status));
+                if (!live) break;
+                const int nb = min(8, it.nblk - 8 * j);
+                int id = 0;
+                bool bad = false;
+                if (lane < nb) {
+                    id = table[8 * j + lane];
+                    bad = id < 0 || id >= p.num_blocks;
+                    if (bad) id = 0;  // fetched, then masked and zeroed
+                }
+                const unsigned badm = __ballot_sync(0xffffffffu, bad);
+                if (lane == 0) {
+                    if (isk && badm) atomicOr(p.status, PKV_DEV_BAD_BLOCK_ID);
+                    if (!isk) vbad[b] = (int)badm;
+                    mbar_arrive_expect_tx(&full[b], (uint32_t)(nb * HALVES * 2048));
+                }
+                __syncwarp();
+                if (lane < nb) {
 #pragma unroll
-                for (int hh = 0; hh < HALVES; ++hh)
-                    tma_load_rows(ring + b * TILE + hh * REG + lane * 2048, map, &full[b], hh * 64,
-                                  h, id * PKV_BLOCK_SIZE);
+                    for (int hh = 0; hh < HALVES; ++hh)
+                        tma_load_rows(ring + b * TILE + hh * REG + lane * 2048, map, &full[b],
+                                      hh * 64, it.h, id * PKV_BLOCK_SIZE);
+                }
             }
-            issued = j + 1;
         }
         // every copy issued must land before the CTA may exit
         if (lane == 0)
-            for (int j = max(0, issued - 2); j < issued; ++j)
-                mbar_drain(&full[j & 1], (j >> 1) & 1, p.status);
+            for (int j = max(0, J - 2); j < J; ++j) mbar_drain(&full[j & 1], (j >> 1) & 1, p.status);
+    } else if (warp == 2) {
+        // --------------------------------------- Q rows of each item (cp.async)
+        const T* qb = static_cast<const T*>(p.q);
+        constexpr int CH = D / 8;  // 16-byte chunks per row
+        int I = 0;
+        for (int i = blockIdx.x; i < num_items; i += gridDim.x) {
+            TcItem it;
+            if (!tc_item(p, i, false, it)) continue;
+            const int qbuf = I & 1;
+            if (!__all_sync(0xffffffffu,
+                            mbar_wait(&q_empty[qbuf], ((I >> 1) & 1) ^ 1, abort_flag, p.status)))
+                break;
+            unsigned char* dstb = sq + qbuf * TILE;
+            for (int x = lane; x < kTcRows * CH; x += 32) {
+                const int r = x / CH, c = x - r * CH;
+                const int R = it.row0 + r, t = R / g;
+                const bool live_row = t < it.qlen;
+                const T* src = qb + ((size_t)(it.q0 + (live_row ? t : 0)) * Hq + it.h * g +
+                                     (R - t * g)) * D + c * 8;
+                const uint32_t dst =
+                    smem_addr(dstb + (c >> 3) * REG + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+                // rows past the chunk are zero-filled (source size 0)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst),
+                             "l"(src), "r"(live_row ? 16 : 0)
+                             : "memory");
+            }
+            asm volatile("cp.async.commit_group;\n" ::: "memory");
+            asm volatile("cp.async.wait_all;\n" ::: "memory");
+            asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&q_full[qbuf]);
+            ++I;
+        }
     } else if (warp == 1) {
         // ------------------------------------------------------------- MMA issuer
         if (lane == 0) {
@@ -420,45 +466,75 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t id_pv = tc_idesc_f16(kBf16, kTcRows, D, 0, 1);
             const uint32_t aq = smem_addr(sq), ak = smem_addr(sk), av = smem_addr(sv),
                            ap = smem_addr(sp);
-            // P(i) V(i) into O; P(i) and V(i) sit in buffer / stage i % 2
-            auto issue_pv = [&](int i) -> bool {
-                const int bi = i & 1, phi = (i >> 1) & 1;
-                if (!mbar_wait(&v_full[bi], phi, abort_flag, p.status)) return false;
-                if (!mbar_wait(&p_full[bi], phi, abort_flag, p.status)) return false;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < kTcKeys / 16; ++kk)
-                    tc_mma(tmem + kOCol,
-                           tc_smem_desc(ap + bi * PBYTES + (kk >> 2) * REG + (kk & 3) * 32, 16,
-                                        1024),
-                           tc_smem_desc(av + bi * TILE + kk * 2048, REG, 1024), id_pv,
-                           i > 0 || kk > 0);
-                tc_commit(&pv_done[bi]);
-                tc_commit(&v_empty[bi]);
-                return true;
+            // Two cursors over the same sequence of key tiles (items in order,
+            // key tiles within each): scores run two tiles ahead of P V.
+            struct Cur {
+                int i, I, j, J, nkv;  // item index, items seen, key tile in item, global tile
             };
-            // S(j) = Q K(j)^T into score buffer j % 2 (free once softmax read S(j-2))
-            auto issue_s = [&](int j) -> bool {
-                const int b = j & 1, ph = (j >> 1) & 1;
+            auto advance = [&](Cur& c) -> bool {  // to the next key tile; false at the end
+                if (c.i >= 0 && ++c.j < c.nkv) {
+                    ++c.J;
+                    return true;
+                }
+                for (c.i = c.i < 0 ? (int)blockIdx.x : c.i + (int)gridDim.x; c.i < num_items;
+                     c.i += gridDim.x) {
+                    TcItem it;
+                    if (!tc_item(p, c.i, false, it)) continue;
+                    c.nkv = it.nkv;
+                    c.j = 0;
+                    ++c.I;
+                    ++c.J;
+                    return true;
+                }
+                return false;
+            };
+            auto issue_s = [&](const Cur& c) -> bool {
+                const int b = c.J & 1, ph = (c.J >> 1) & 1, qbuf = c.I & 1;
                 if (!mbar_wait(&k_full[b], ph, abort_flag, p.status)) return false;
-                if (j >= 2 && !mbar_wait(&s_free[b], ph ^ 1, abort_flag, p.status)) return false;
+                if (c.J >= 2 && !mbar_wait(&s_free[b], ph ^ 1, abort_flag, p.status)) return false;
+                if (c.j == 0 && !mbar_wait(&q_full[qbuf], (c.I >> 1) & 1, abort_flag, p.status))
+                    return false;
                 tc_fence_after();
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
                     tc_mma(tmem + b * kTcKeys,
-                           tc_smem_desc(aq + (ks >> 2) * REG + (ks & 3) * 32, 16, 1024),
+                           tc_smem_desc(aq + qbuf * TILE + (ks >> 2) * REG + (ks & 3) * 32, 16, 1024),
                            tc_smem_desc(ak + b * TILE + (ks >> 2) * REG + (ks & 3) * 32, 16, 1024),
                            id_s, ks > 0);
                 tc_commit(&s_full[b]);
                 tc_commit(&k_empty[b]);
+                if (c.j == c.nkv - 1) tc_commit(&q_empty[qbuf]);  // the item's last use of Q
                 return true;
             };
-            // scores run two tiles ahead: S0, S1, PV0, S2, PV1, S3, ...
-            bool live = true;
-            for (int j = 0; j < min(2, nkv) && live; ++j) live = issue_s(j);
-            for (int i = 0; i < nkv && live; ++i) {
-                live = issue_pv(i);
-                if (live && i + 2 < nkv) live = issue_s(i + 2);
+            auto issue_pv = [&](const Cur& c) -> bool {
+                const int b = c.J & 1;
+                if (!mbar_wait(&v_full[b], (c.J >> 1) & 1, abort_flag, p.status)) return false;
+                if (!mbar_wait(p_full, c.J & 1, abort_flag, p.status)) return false;
+                // the item's first P V overwrites O: the last item's O must have been read
+                if (c.j == 0 && c.I >= 1 && !mbar_wait(o_free, (c.I - 1) & 1, abort_flag, p.status))
+                    return false;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kTcKeys / 16; ++kk)
+                    tc_mma(tmem + kOCol, tc_smem_desc(ap + (kk >> 2) * REG + (kk & 3) * 32, 16, 1024),
+                           tc_smem_desc(av + b * TILE + kk * 2048, REG, 1024), id_pv,
+                           c.j > 0 || kk > 0);
+                tc_commit(pv_done);
+                tc_commit(&v_empty[b]);
+                return true;
+            };
+            Cur cs = {-1, -1, 0, -1, 0}, cp = {-1, -1, 0, -1, 0};
+            bool live = true, more_s = advance(cs);
+            for (int k = 0; k < 2 && more_s && live; ++k) {
+                live = issue_s(cs);
+                more_s = advance(cs);
+            }
+            while (live && advance(cp)) {
+                live = issue_pv(cp);
+                if (live && more_s) {
+                    live = issue_s(cs);
+                    more_s = advance(cs);
+                }
             }
             // nothing of this thread's may still run when tensor memory is freed
             tc_commit(mma_idle);
@@ -469,135 +545,136 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ------------------------------------------------- softmax, one thread per row
         const int r = tid - 128;                              // row of the tile = TMEM lane
         const uint32_t trow = tmem + ((uint32_t)(32 * (warp - 4)) << 16);
-        const int R = row0 + r, t = R / g;
-        const bool live_row = t < qlen;
-        const int pos = live_row ? n - qlen + t : -1;        // keys 0..pos are visible
         const float sl2 = p.scale_log2;
-        float m_used = -INFINITY, l = 0.f;
+        int J = 0, I = 0;
         bool ok = true;
-        for (int j = 0; j < nkv; ++j) {
-            const int b = j & 1, ph = (j >> 1) & 1;
-            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[b], ph, abort_flag, p.status));
+        for (int i = blockIdx.x; i < num_items && ok; i += gridDim.x) {
+            TcItem it;
+            if (!tc_item(p, i, false, it)) continue;
+            const int R = it.row0 + r, t = R / g;
+            const bool live_row = t < it.qlen;
+            const int pos = live_row ? it.n - it.qlen + t : -1;   // keys 0..pos are visible
+            float m_used = -INFINITY, l = 0.f;
+            for (int j = 0; j < it.nkv; ++j, ++J) {
+                const int b = J & 1, ph = (J >> 1) & 1;
+                ok = __all_sync(0xffffffffu, mbar_wait(&s_full[b], ph, abort_flag, p.status));
+                if (!ok) break;
+                tc_fence_after();
+                float sc[kTcKeys];
+#pragma unroll
+                for (int c = 0; c < kTcKeys / 32; ++c)
+                    tc_ld32(trow + b * kTcKeys + 32 * c,
+                            reinterpret_cast<uint32_t(&)[32]>(sc[32 * c]));
+                tc_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_free[b]);
+                ok = __all_sync(0xffffffffu, mbar_wait(&v_full[b], ph, abort_flag, p.status));
+                if (!ok) break;
+                const unsigned bad = (unsigned)vbad[b];
+                const int key0 = kTcKeys * j;
+                // Tiles below every row's causal bound with no bad block (most of
+                // them) need no mask: max over the raw scores, and the scale goes
+                // into the exponent's fma.  Others: select (never scale garbage
+                // into use), then the same exponent with a unit multiplier.
+                const bool plain = __all_sync(0xffffffffu, key0 + kTcKeys - 1 <= pos) &&
+                                   bad == 0u && sl2 > 0.f;
+                float mx = -INFINITY, mul = sl2;
+                if (plain) {
+#pragma unroll
+                    for (int c = 0; c < kTcKeys; ++c) mx = fmaxf(mx, sc[c]);
+                    mx *= sl2;
+                } else {
+                    mul = 1.f;
+#pragma unroll
+                    for (int c = 0; c < kTcKeys; ++c) {
+                        const bool vis = key0 + c <= pos && !((bad >> (c >> 4)) & 1u);
+                        sc[c] = vis ? sc[c] * sl2 : -INFINITY;
+                        mx = fmaxf(mx, sc[c]);
+                    }
+                }
+                const float m_new = fmaxf(m_used, mx);
+                // lazy rescale: only when the maximum grew by more than 2^kTcRescale
+                const bool grow = m_used != -INFINITY && m_new > m_used + kTcRescale;
+                const float f = grow ? fast_exp2(m_used - m_new) : 1.f;
+                if (m_used == -INFINITY || grow) m_used = m_new;
+                const float ms = m_used == -INFINITY ? 0.f : m_used;
+                // P(J) in registers first: none of this waits on the tensor core
+                uint32_t pk[kTcKeys / 2];
+                float psum = 0.f;
+#pragma unroll
+                for (int c = 0; c < kTcKeys / 2; ++c) {
+                    const float p0 = fast_exp2(fmaf(sc[2 * c], mul, -ms));
+                    const float p1 = fast_exp2(fmaf(sc[2 * c + 1], mul, -ms));
+                    psum += p0 + p1;
+                    pk[c] = E::pack(p0, p1);
+                }
+                if (J >= 1) {
+                    // P(J) overwrites P(J-1), and O may be rescaled: P(J-1) V(J-1) must be done
+                    ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (J - 1) & 1, abort_flag, p.status));
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                if (__any_sync(0xffffffffu, grow)) {
+                    // (whole warp: tensor-memory access is warp-wide)
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tc_ld32(trow + kOCol + 32 * c, o);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                        tc_st32(trow + kOCol + 32 * c, o);
+                    }
+                    tc_wait_st();
+                }
+                l = l * f + psum;
+                // P row: 16 chunks of 8 keys; chunk c in half c / 8 of the P tile
+#pragma unroll
+                for (int c = 0; c < kTcKeys / 8; ++c)
+                    *reinterpret_cast<uint4*>(sp + (c >> 3) * REG + r * 128 +
+                                              (((c & 7) ^ (r & 7)) << 4)) =
+                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+                // V rows no row may see must be finite zeros before P V (0 x NaN = NaN)
+                if (j == it.nkv - 1 || bad) {
+                    unsigned char* vt = sv + b * TILE;
+                    for (int x = r; x < kTcKeys * 8 * HALVES; x += 128) {
+                        const int key = x / (8 * HALVES), rest = x - key * (8 * HALVES);
+                        if (key0 + key <= it.p_last && !((bad >> (key >> 4)) & 1u)) continue;
+                        *reinterpret_cast<uint4*>(vt + (rest >> 3) * REG + key * 128 +
+                                                  ((rest & 7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+                tc_fence_before();  // a rescaled O is ordered before the next MMA
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full);
+            }
+            if (!ok) break;
+            // epilogue: O / l of the item's live rows; O goes back to the next item
+            ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (J - 1) & 1, abort_flag, p.status));
             if (!ok) break;
             tc_fence_after();
-            float sc[kTcKeys];
+            uint32_t o[D];
 #pragma unroll
-            for (int c = 0; c < kTcKeys / 32; ++c)
-                tc_ld32(trow + b * kTcKeys + 32 * c, reinterpret_cast<uint32_t(&)[32]>(sc[32 * c]));
+            for (int c = 0; c < D / 32; ++c)
+                tc_ld32(trow + kOCol + 32 * c, reinterpret_cast<uint32_t(&)[32]>(o[32 * c]));
             tc_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&s_free[b]);
-            ok = __all_sync(0xffffffffu, mbar_wait(&v_full[b], ph, abort_flag, p.status));
-            if (!ok) break;
-            const unsigned bad = (unsigned)vbad[b];
-            const int key0 = kTcKeys * j;
-            // Tiles below every row's causal bound with no bad block (most of
-            // them) need no mask: max over the raw scores, and the scale goes
-            // into the exponent's fma.  Others: select (never scale garbage
-            // into use), then the same exponent with a unit multiplier.
-            const bool plain = __all_sync(0xffffffffu, key0 + kTcKeys - 1 <= pos) && bad == 0u &&
-                               sl2 > 0.f;
-            float mx = -INFINITY, mul = sl2;
-            if (plain) {
-#pragma unroll
-                for (int c = 0; c < kTcKeys; ++c) mx = fmaxf(mx, sc[c]);
-                mx *= sl2;
-            } else {
-                mul = 1.f;
-#pragma unroll
-                for (int c = 0; c < kTcKeys; ++c) {
-                    const bool vis = key0 + c <= pos && !((bad >> (c >> 4)) & 1u);
-                    sc[c] = vis ? sc[c] * sl2 : -INFINITY;
-                    mx = fmaxf(mx, sc[c]);
-                }
-            }
-            const float m_new = fmaxf(m_used, mx);
-            // lazy rescale: only when the maximum grew by more than 2^kTcRescale
-            const bool grow = m_used != -INFINITY && m_new > m_used + kTcRescale;
-            const float f = grow ? fast_exp2(m_used - m_new) : 1.f;
-            if (m_used == -INFINITY || grow) m_used = m_new;
-            const float ms = m_used == -INFINITY ? 0.f : m_used;
-            // P(j) in registers first: none of this waits on the tensor core
-            uint32_t pk[kTcKeys / 2];
-            float psum = 0.f;
-#pragma unroll
-            for (int c = 0; c < kTcKeys / 2; ++c) {
-                const float p0 = fast_exp2(fmaf(sc[2 * c], mul, -ms));
-                const float p1 = fast_exp2(fmaf(sc[2 * c + 1], mul, -ms));
-                psum += p0 + p1;
-                pk[c] = E::pack(p0, p1);
-            }
-            if (__any_sync(0xffffffffu, grow)) {
-                // O must hold P(j-1) V(j-1) before it is scaled (whole warp:
-                // tensor-memory access is warp-wide)
-                ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1,
-                                                       abort_flag, p.status));
-                if (!ok) break;
-                tc_fence_after();
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    tc_ld32(trow + kOCol + 32 * c, o);
-                    tc_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-                    tc_st32(trow + kOCol + 32 * c, o);
-                }
-                tc_wait_st();
-            }
-            l = l * f + psum;
-            if (j >= 2) {
-                // P buffer b still feeds P(j-2) V(j-2) until that completes
-                ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[b], ((j - 2) >> 1) & 1, abort_flag,
-                                                       p.status));
-                if (!ok) break;
-            }
-            // P row: 16 chunks of 8 keys; chunk c in half c / 8 of P buffer b
-            unsigned char* pb = sp + b * PBYTES;
-#pragma unroll
-            for (int c = 0; c < kTcKeys / 8; ++c)
-                *reinterpret_cast<uint4*>(pb + (c >> 3) * REG + r * 128 + (((c & 7) ^ (r & 7)) << 4)) =
-                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-            // V rows no row may see must be finite zeros before P V (0 x NaN = NaN)
-            if (j == nkv - 1 || bad) {
-                unsigned char* vt = sv + b * TILE;
-                for (int x = r; x < kTcKeys * 8 * HALVES; x += 128) {
-                    const int key = x / (8 * HALVES), rest = x - key * (8 * HALVES);
-                    if (key0 + key <= p_last && !((bad >> (key >> 4)) & 1u)) continue;
-                    *reinterpret_cast<uint4*>(vt + (rest >> 3) * REG + key * 128 + ((rest & 7) << 4)) =
-                        make_uint4(0u, 0u, 0u, 0u);
-                }
-            }
-            asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-            tc_fence_before();  // the rescaled O is ordered before the next MMA
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[b]);
-        }
-        // epilogue: O / l for the live rows
-        if (ok && !*abort_flag) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&pv_done[(nkv - 1) & 1], ((nkv - 1) >> 1) & 1,
-                                                   abort_flag, p.status));
-            if (ok) {
-                tc_fence_after();
+            if (lane == 0) mbar_arrive(o_free);
+            ++I;
+            if (live_row) {
                 const float inv = l > 0.f ? 1.f / l : 0.f;
                 T* dst = static_cast<T*>(p.out) +
-                         ((size_t)(q0 + (live_row ? t : 0)) * Hq + h * g + (R - t * g)) * D;
+                         ((size_t)(it.q0 + t) * Hq + it.h * g + (R - t * g)) * D;
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    tc_ld32(trow + kOCol + 32 * c, o);
-                    tc_wait_ld();
-                    if (live_row) {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            *reinterpret_cast<uint4*>(dst + 32 * c + 8 * e) = make_uint4(
-                                E::pack(__uint_as_float(o[8 * e]) * inv, __uint_as_float(o[8 * e + 1]) * inv),
-                                E::pack(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv),
-                                E::pack(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv),
-                                E::pack(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv));
-                    }
-                }
+                for (int e = 0; e < D / 8; ++e)
+                    *reinterpret_cast<uint4*>(dst + 8 * e) = make_uint4(
+                        E::pack(__uint_as_float(o[8 * e]) * inv, __uint_as_float(o[8 * e + 1]) * inv),
+                        E::pack(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv),
+                        E::pack(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv),
+                        E::pack(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv));
             }
         }
     }
@@ -611,7 +688,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 template <int D>
 size_t prefill_tc_smem() {
-    return 1024 + (size_t)5 * (D / 64) * kTcRows * 128 + 4 * kTcRows * 128 + 256;
+    // 2 Q buffers, 2 K and 2 V stages, one P buffer, barriers; 1 KB alignment slack
+    return 1024 + (size_t)6 * (D / 64) * kTcRows * 128 + 2 * kTcRows * 128 + 256;
 }
 
 // Which prefill kernel runs: the tcgen05 one unless PKV_PREFILL_KERNEL=mma
@@ -640,9 +718,12 @@ pkv_status launch_prefill(const PrefillParams& prm_in, const void* k_cache, cons
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
             return PKV_ERR_CUDA;
-        const long long grid = (long long)prm.num_seqs * num_kv_heads * prm.tiles_per_seq;
-        if (grid > 0x7fffffffll) return PKV_ERR_UNSUPPORTED;
-        kern<<<(unsigned)grid, kTcThreads, smem, stream>>>(prm, tmk, tmv);
+        const long long items = (long long)prm.num_seqs * num_kv_heads * prm.tiles_per_seq;
+        if (items > 0x7fffffffll) return PKV_ERR_UNSUPPORTED;
+        const int sms = sm_count();
+        if (sms <= 0) return PKV_ERR_CUDA;
+        const int grid = (int)std::min<long long>(items, sms);  // persistent: one CTA per SM
+        kern<<<grid, kTcThreads, smem, stream>>>(prm, tmk, tmv, (int)items);
         return cuda_status(cudaGetLastError());
     }
     prm.tiles_per_seq = ceil_div(max_q_len * prm.group, kPrefillRows);
