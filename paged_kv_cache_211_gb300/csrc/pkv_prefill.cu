@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(kPrefillThreads)
 // never loaded) are zeroed before P V so that no 0 x NaN reaches O.  Every
 // wait is bounded.
 // ============================================================================
-constexpr int kTcThreads = 256;
+constexpr int kTcThreads = 384;
 constexpr int kTcRows = 128;     // (query token, query head) rows per tile
 constexpr int kTcKeys = 128;     // keys per key tile
 constexpr float kTcRescale = 8.f;  // log2 of the largest P before O is rescaled
@@ -329,15 +329,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr int HALVES = D / 64;
     constexpr int REG = kTcRows * 128;     // one 64-element half of 128 rows: 16 KB
     constexpr int TILE = HALVES * REG;     // a Q tile, or one K or V key tile
-    constexpr int PBYTES = 2 * REG;        // P: 128 rows x 128 keys
-    constexpr uint32_t kCols = 512;        // S0, S1 (128 columns each), O (D columns)
-    constexpr uint32_t kOCol = 256;
+    constexpr int PBYTES = 2 * REG;        // P: 128 rows x 128 keys (one half per group)
+    constexpr int HK = kTcKeys / 2;        // keys per softmax group
+    constexpr uint32_t kCols = 512;        // S0, S1 (128 columns each), O_0, O_1 (128 each)
+    constexpr uint32_t kOCol = 256;        // O of group q at kOCol + 128 q
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     unsigned char* sq = smem_raw + (((raw + 1023u) & ~1023u) - raw);   // 2 Q buffers
     unsigned char* sk = sq + 2 * TILE;      // 2 stages
     unsigned char* sv = sk + 2 * TILE;      // 2 stages
-    unsigned char* sp = sv + 2 * TILE;      // 1 P buffer
+    unsigned char* sp = sv + 2 * TILE;      // P: keys 0-63 (group 0), 64-127 (group 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(sp + PBYTES);
     uint64_t* k_full = bars + 0;
     uint64_t* k_empty = bars + 2;
@@ -347,13 +348,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t* s_free = bars + 10;
     uint64_t* q_full = bars + 12;
     uint64_t* q_empty = bars + 14;
-    uint64_t* p_full = bars + 16;
-    uint64_t* pv_done = bars + 17;
-    uint64_t* o_free = bars + 18;
-    uint64_t* mma_idle = bars + 19;
-    int* vbad = reinterpret_cast<int*>(bars + 20);           // [2] bad-block bits per V stage
+    uint64_t* p_full = bars + 16;          // [group]
+    uint64_t* pv_done = bars + 18;         // [group]
+    uint64_t* o_ready = bars + 20;         // an item's last P V done (both groups)
+    uint64_t* o_free = bars + 21;          // group 1 has read both O halves of an item
+    uint64_t* xchg = bars + 22;            // [lane quarter]: group 0's (m, l) written
+    uint64_t* xfree = bars + 26;           // [lane quarter]: ... and read by group 1
+    uint64_t* mma_idle = bars + 30;
+    int* vbad = reinterpret_cast<int*>(bars + 31);           // [2] bad-block bits per V stage
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(vbad + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    float* xml = reinterpret_cast<float*>(tmem_slot + 2);    // [2][128]: group 0's m, l per row
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int g = p.group, Hq = p.num_q_heads;
@@ -365,12 +370,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_free[i], 4);
+            mbar_init(&s_free[i], 8);
             mbar_init(&q_full[i], 1);
             mbar_init(&q_empty[i], 1);
+            mbar_init(&p_full[i], 4);
+            mbar_init(&pv_done[i], 1);
         }
-        mbar_init(p_full, 4);
-        mbar_init(pv_done, 1);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&xchg[i], 32);
+            mbar_init(&xfree[i], 32);
+        }
+        mbar_init(o_ready, 1);
         mbar_init(o_free, 4);
         mbar_init(mma_idle, 1);
         *abort_flag = 0;
@@ -506,21 +516,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (c.j == c.nkv - 1) tc_commit(&q_empty[qbuf]);  // the item's last use of Q
                 return true;
             };
+            // O_q += P_q V_q over key half q of the tile (q = softmax group)
             auto issue_pv = [&](const Cur& c) -> bool {
                 const int b = c.J & 1;
                 if (!mbar_wait(&v_full[b], (c.J >> 1) & 1, abort_flag, p.status)) return false;
-                if (!mbar_wait(p_full, c.J & 1, abort_flag, p.status)) return false;
-                // the item's first P V overwrites O: the last item's O must have been read
+                // the item's first P V overwrites O: the last item's must have been read
                 if (c.j == 0 && c.I >= 1 && !mbar_wait(o_free, (c.I - 1) & 1, abort_flag, p.status))
                     return false;
-                tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kTcKeys / 16; ++kk)
-                    tc_mma(tmem + kOCol, tc_smem_desc(ap + (kk >> 2) * REG + (kk & 3) * 32, 16, 1024),
-                           tc_smem_desc(av + b * TILE + kk * 2048, REG, 1024), id_pv,
-                           c.j > 0 || kk > 0);
-                tc_commit(pv_done);
+                for (int q = 0; q < 2; ++q) {
+                    if (!mbar_wait(&p_full[q], c.J & 1, abort_flag, p.status)) return false;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < HK / 16; ++kk)
+                        tc_mma(tmem + kOCol + 128 * q,
+                               tc_smem_desc(ap + q * REG + kk * 32, 16, 1024),
+                               tc_smem_desc(av + b * TILE + (q * (HK / 16) + kk) * 2048, REG, 1024),
+                               id_pv, c.j > 0 || kk > 0);
+                    tc_commit(&pv_done[q]);
+                }
                 tc_commit(&v_empty[b]);
+                if (c.j == c.nkv - 1) tc_commit(o_ready);  // O of the item is complete
                 return true;
             };
             Cur cs = {-1, -1, 0, -1, 0}, cp = {-1, -1, 0, -1, 0};
@@ -541,10 +557,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_drain(mma_idle, 0, p.status);
         }
         __syncwarp();
-    } else if (warp >= 4) {
-        // ------------------------------------------------- softmax, one thread per row
-        const int r = tid - 128;                              // row of the tile = TMEM lane
-        const uint32_t trow = tmem + ((uint32_t)(32 * (warp - 4)) << 16);
+    } else {
+        // ------------------------- softmax: two groups of four warps, one thread per
+        // (row, key half); each group runs its own online softmax over its half of
+        // every key tile into its own O, and the halves merge at the end of an item
+        const int q = (warp - 4) >> 2;                       // group: key half
+        const int wq = warp & 3;                             // tensor-memory lane quarter
+        const int r = 32 * wq + lane;                        // row of the tile
+        const uint32_t trow = tmem + ((uint32_t)(32 * wq) << 16);
+        const uint32_t ocol = kOCol + 128 * q;
         const float sl2 = p.scale_log2;
         int J = 0, I = 0;
         bool ok = true;
@@ -560,10 +581,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 ok = __all_sync(0xffffffffu, mbar_wait(&s_full[b], ph, abort_flag, p.status));
                 if (!ok) break;
                 tc_fence_after();
-                float sc[kTcKeys];
+                float sc[HK];
 #pragma unroll
-                for (int c = 0; c < kTcKeys / 32; ++c)
-                    tc_ld32(trow + b * kTcKeys + 32 * c,
+                for (int c = 0; c < HK / 32; ++c)
+                    tc_ld32(trow + b * kTcKeys + HK * q + 32 * c,
                             reinterpret_cast<uint32_t(&)[32]>(sc[32 * c]));
                 tc_wait_ld();
                 tc_fence_before();
@@ -571,47 +592,56 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (lane == 0) mbar_arrive(&s_free[b]);
                 ok = __all_sync(0xffffffffu, mbar_wait(&v_full[b], ph, abort_flag, p.status));
                 if (!ok) break;
-                const unsigned bad = (unsigned)vbad[b];
-                const int key0 = kTcKeys * j;
-                // Tiles below every row's causal bound with no bad block (most of
+                const unsigned bad = ((unsigned)vbad[b] >> (4 * q)) & 0xFu;  // this half's blocks
+                const int key0 = kTcKeys * j + HK * q;
+                // Halves below every row's causal bound with no bad block (most of
                 // them) need no mask: max over the raw scores, and the scale goes
                 // into the exponent's fma.  Others: select (never scale garbage
                 // into use), then the same exponent with a unit multiplier.
-                const bool plain = __all_sync(0xffffffffu, key0 + kTcKeys - 1 <= pos) &&
-                                   bad == 0u && sl2 > 0.f;
-                float mx = -INFINITY, mul = sl2;
+                const bool plain = __all_sync(0xffffffffu, key0 + HK - 1 <= pos) && bad == 0u &&
+                                   sl2 > 0.f;
+                // eight independent partial maxima / sums: no long dependency chain
+                float mxp[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) mxp[e] = -INFINITY;
+                float mul = sl2;
                 if (plain) {
 #pragma unroll
-                    for (int c = 0; c < kTcKeys; ++c) mx = fmaxf(mx, sc[c]);
-                    mx *= sl2;
+                    for (int c = 0; c < HK; ++c) mxp[c & 7] = fmaxf(mxp[c & 7], sc[c]);
                 } else {
                     mul = 1.f;
 #pragma unroll
-                    for (int c = 0; c < kTcKeys; ++c) {
+                    for (int c = 0; c < HK; ++c) {
                         const bool vis = key0 + c <= pos && !((bad >> (c >> 4)) & 1u);
                         sc[c] = vis ? sc[c] * sl2 : -INFINITY;
-                        mx = fmaxf(mx, sc[c]);
+                        mxp[c & 7] = fmaxf(mxp[c & 7], sc[c]);
                     }
                 }
+                float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                                 fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+                if (plain) mx *= sl2;
                 const float m_new = fmaxf(m_used, mx);
                 // lazy rescale: only when the maximum grew by more than 2^kTcRescale
                 const bool grow = m_used != -INFINITY && m_new > m_used + kTcRescale;
                 const float f = grow ? fast_exp2(m_used - m_new) : 1.f;
                 if (m_used == -INFINITY || grow) m_used = m_new;
                 const float ms = m_used == -INFINITY ? 0.f : m_used;
-                // P(J) in registers first: none of this waits on the tensor core
-                uint32_t pk[kTcKeys / 2];
-                float psum = 0.f;
+                // P in registers first: none of this waits on the tensor core
+                uint32_t pk[HK / 2];
+                float psp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int c = 0; c < kTcKeys / 2; ++c) {
+                for (int c = 0; c < HK / 2; ++c) {
                     const float p0 = fast_exp2(fmaf(sc[2 * c], mul, -ms));
                     const float p1 = fast_exp2(fmaf(sc[2 * c + 1], mul, -ms));
-                    psum += p0 + p1;
+                    psp[c & 7] += p0 + p1;
                     pk[c] = E::pack(p0, p1);
                 }
+                const float psum = ((psp[0] + psp[1]) + (psp[2] + psp[3])) +
+                                   ((psp[4] + psp[5]) + (psp[6] + psp[7]));
                 if (J >= 1) {
-                    // P(J) overwrites P(J-1), and O may be rescaled: P(J-1) V(J-1) must be done
-                    ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (J - 1) & 1, abort_flag, p.status));
+                    // P overwrites the last tile's, and O may be rescaled: that P V must be done
+                    ok = __all_sync(0xffffffffu,
+                                    mbar_wait(&pv_done[q], (J - 1) & 1, abort_flag, p.status));
                     if (!ok) break;
                     tc_fence_after();
                 }
@@ -620,62 +650,89 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t o[32];
-                        tc_ld32(trow + kOCol + 32 * c, o);
+                        tc_ld32(trow + ocol + 32 * c, o);
                         tc_wait_ld();
 #pragma unroll
                         for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
-                        tc_st32(trow + kOCol + 32 * c, o);
+                        tc_st32(trow + ocol + 32 * c, o);
                     }
                     tc_wait_st();
                 }
                 l = l * f + psum;
-                // P row: 16 chunks of 8 keys; chunk c in half c / 8 of the P tile
+                // P row: 8 chunks of 8 keys in this group's half of the P tile
 #pragma unroll
-                for (int c = 0; c < kTcKeys / 8; ++c)
-                    *reinterpret_cast<uint4*>(sp + (c >> 3) * REG + r * 128 +
-                                              (((c & 7) ^ (r & 7)) << 4)) =
+                for (int c = 0; c < HK / 8; ++c)
+                    *reinterpret_cast<uint4*>(sp + q * REG + r * 128 + ((c ^ (r & 7)) << 4)) =
                         make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-                // V rows no row may see must be finite zeros before P V (0 x NaN = NaN)
+                // V rows of this half no row may see must be finite zeros before
+                // P V (0 x NaN = NaN)
                 if (j == it.nkv - 1 || bad) {
                     unsigned char* vt = sv + b * TILE;
-                    for (int x = r; x < kTcKeys * 8 * HALVES; x += 128) {
-                        const int key = x / (8 * HALVES), rest = x - key * (8 * HALVES);
-                        if (key0 + key <= it.p_last && !((bad >> (key >> 4)) & 1u)) continue;
-                        *reinterpret_cast<uint4*>(vt + (rest >> 3) * REG + key * 128 +
+                    for (int x = r; x < HK * 8 * HALVES; x += 128) {
+                        const int kq = x / (8 * HALVES), rest = x - kq * (8 * HALVES);
+                        if (key0 + kq <= it.p_last && !((bad >> (kq >> 4)) & 1u)) continue;
+                        *reinterpret_cast<uint4*>(vt + (rest >> 3) * REG + (HK * q + kq) * 128 +
                                                   ((rest & 7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
                     }
                 }
                 asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
                 tc_fence_before();  // a rescaled O is ordered before the next MMA
                 __syncwarp();
-                if (lane == 0) mbar_arrive(p_full);
+                if (lane == 0) mbar_arrive(&p_full[q]);
             }
             if (!ok) break;
-            // epilogue: O / l of the item's live rows; O goes back to the next item
-            ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (J - 1) & 1, abort_flag, p.status));
+            // epilogue: group 0 hands its (m, l) to group 1, which stores
+            // (O_0 2^(m_0 - M) + O_1 2^(m_1 - M)) / (l_0 2^(m_0 - M) + l_1 2^(m_1 - M))
+            if (q == 0) {
+                if (I >= 1 && !__all_sync(0xffffffffu, mbar_wait(&xfree[wq], (I - 1) & 1,
+                                                                 abort_flag, p.status))) {
+                    ok = false;
+                    break;
+                }
+                xml[r] = m_used;
+                xml[128 + r] = l;
+                mbar_arrive(&xchg[wq]);
+                ++I;
+                continue;
+            }
+            ok = __all_sync(0xffffffffu, mbar_wait(&xchg[wq], I & 1, abort_flag, p.status));
+            if (!ok) break;
+            const float m0 = xml[r], l0 = xml[128 + r];
+            mbar_arrive(&xfree[wq]);
+            const float M = fmaxf(m0, m_used);
+            const float Ms = M == -INFINITY ? 0.f : M;
+            const float w0 = fast_exp2(m0 - Ms), w1 = fast_exp2(m_used - Ms);
+            const float L = l0 * w0 + l * w1;
+            const float inv = L > 0.f ? 1.f / L : 0.f;
+            ok = __all_sync(0xffffffffu, mbar_wait(o_ready, I & 1, abort_flag, p.status));
             if (!ok) break;
             tc_fence_after();
-            uint32_t o[D];
+            T* dst = static_cast<T*>(p.out) +
+                     ((size_t)(it.q0 + (live_row ? t : 0)) * Hq + it.h * g + (R - t * g)) * D;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c)
-                tc_ld32(trow + kOCol + 32 * c, reinterpret_cast<uint32_t(&)[32]>(o[32 * c]));
-            tc_wait_ld();
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o0[32], o1[32];
+                tc_ld32(trow + kOCol + 32 * c, o0);
+                tc_ld32(trow + kOCol + 128 + 32 * c, o1);
+                tc_wait_ld();
+                if (live_row) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float v[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            v[u] = (__uint_as_float(o0[8 * e + u]) * w0 +
+                                    __uint_as_float(o1[8 * e + u]) * w1) * inv;
+                        *reinterpret_cast<uint4*>(dst + 32 * c + 8 * e) =
+                            make_uint4(E::pack(v[0], v[1]), E::pack(v[2], v[3]),
+                                       E::pack(v[4], v[5]), E::pack(v[6], v[7]));
+                    }
+                }
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(o_free);
             ++I;
-            if (live_row) {
-                const float inv = l > 0.f ? 1.f / l : 0.f;
-                T* dst = static_cast<T*>(p.out) +
-                         ((size_t)(it.q0 + t) * Hq + it.h * g + (R - t * g)) * D;
-#pragma unroll
-                for (int e = 0; e < D / 8; ++e)
-                    *reinterpret_cast<uint4*>(dst + 8 * e) = make_uint4(
-                        E::pack(__uint_as_float(o[8 * e]) * inv, __uint_as_float(o[8 * e + 1]) * inv),
-                        E::pack(__uint_as_float(o[8 * e + 2]) * inv, __uint_as_float(o[8 * e + 3]) * inv),
-                        E::pack(__uint_as_float(o[8 * e + 4]) * inv, __uint_as_float(o[8 * e + 5]) * inv),
-                        E::pack(__uint_as_float(o[8 * e + 6]) * inv, __uint_as_float(o[8 * e + 7]) * inv));
-            }
         }
     }
     tc_fence_before();
@@ -688,8 +745,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 template <int D>
 size_t prefill_tc_smem() {
-    // 2 Q buffers, 2 K and 2 V stages, one P buffer, barriers; 1 KB alignment slack
-    return 1024 + (size_t)6 * (D / 64) * kTcRows * 128 + 2 * kTcRows * 128 + 256;
+    // 2 Q buffers, 2 K and 2 V stages, one P buffer, barriers, the (m, l)
+    // hand-over; 1 KB alignment slack (231 680 bytes at D = 128)
+    return 1024 + (size_t)6 * (D / 64) * kTcRows * 128 + 2 * kTcRows * 128 + 256 + 1024;
 }
 
 // Which prefill kernel runs: the tcgen05 one unless PKV_PREFILL_KERNEL=mma
