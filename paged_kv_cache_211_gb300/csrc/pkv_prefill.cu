@@ -329,7 +329,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     constexpr int HALVES = D / 64;
     constexpr int REG = kTcRows * 128;     // one 64-element half of 128 rows: 16 KB
     constexpr int TILE = HALVES * REG;     // a Q tile, or one K or V key tile
-    constexpr int PBYTES = 2 * REG;        // P: 128 rows x 128 keys (one half per group)
     constexpr int HK = kTcKeys / 2;        // keys per softmax group
     constexpr uint32_t kCols = 512;        // S0, S1 (128 columns each), O_0, O_1 (128 each)
     constexpr uint32_t kOCol = 256;        // O of group q at kOCol + 128 q
@@ -338,14 +337,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     unsigned char* sq = smem_raw + (((raw + 1023u) & ~1023u) - raw);   // 2 Q buffers
     unsigned char* sk = sq + 2 * TILE;      // 2 stages
     unsigned char* sv = sk + 2 * TILE;      // 2 stages
-    unsigned char* sp = sv + 2 * TILE;      // P: keys 0-63 (group 0), 64-127 (group 1)
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sp + PBYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sv + 2 * TILE);
     uint64_t* k_full = bars + 0;
     uint64_t* k_empty = bars + 2;
     uint64_t* v_full = bars + 4;
     uint64_t* v_empty = bars + 6;
     uint64_t* s_full = bars + 8;
-    uint64_t* s_free = bars + 10;
     uint64_t* q_full = bars + 12;
     uint64_t* q_empty = bars + 14;
     uint64_t* p_full = bars + 16;          // [group]
@@ -370,7 +367,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&v_full[i], 1);
             mbar_init(&v_empty[i], 1);
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_free[i], 8);
             mbar_init(&q_full[i], 1);
             mbar_init(&q_empty[i], 1);
             mbar_init(&p_full[i], 4);
@@ -474,8 +470,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
             const uint32_t id_s = tc_idesc_f16(kBf16, kTcRows, kTcKeys, 0, 0);
             const uint32_t id_pv = tc_idesc_f16(kBf16, kTcRows, D, 0, 1);
-            const uint32_t aq = smem_addr(sq), ak = smem_addr(sk), av = smem_addr(sv),
-                           ap = smem_addr(sp);
+            const uint32_t aq = smem_addr(sq), ak = smem_addr(sk), av = smem_addr(sv);
             // Two cursors over the same sequence of key tiles (items in order,
             // key tiles within each): scores run two tiles ahead of P V.
             struct Cur {
@@ -498,10 +493,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 return false;
             };
+            // S(J) overwrites score buffer J % 2, which held S(J-2) and then
+            // P(J-2): P(J-2) V(J-2) was issued before it by this thread, and
+            // one thread's tcgen05.mma run in issue order
             auto issue_s = [&](const Cur& c) -> bool {
                 const int b = c.J & 1, ph = (c.J >> 1) & 1, qbuf = c.I & 1;
                 if (!mbar_wait(&k_full[b], ph, abort_flag, p.status)) return false;
-                if (c.J >= 2 && !mbar_wait(&s_free[b], ph ^ 1, abort_flag, p.status)) return false;
                 if (c.j == 0 && !mbar_wait(&q_full[qbuf], (c.I >> 1) & 1, abort_flag, p.status))
                     return false;
                 tc_fence_after();
@@ -516,7 +513,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (c.j == c.nkv - 1) tc_commit(&q_empty[qbuf]);  // the item's last use of Q
                 return true;
             };
-            // O_q += P_q V_q over key half q of the tile (q = softmax group)
+            // O_q += P_q V_q over key half q of the tile (q = softmax group);
+            // P_q sits in tensor memory over the first 32 columns of the
+            // group's half of score buffer J % 2
             auto issue_pv = [&](const Cur& c) -> bool {
                 const int b = c.J & 1;
                 if (!mbar_wait(&v_full[b], (c.J >> 1) & 1, abort_flag, p.status)) return false;
@@ -529,10 +528,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < HK / 16; ++kk)
-                        tc_mma(tmem + kOCol + 128 * q,
-                               tc_smem_desc(ap + q * REG + kk * 32, 16, 1024),
-                               tc_smem_desc(av + b * TILE + (q * (HK / 16) + kk) * 2048, REG, 1024),
-                               id_pv, c.j > 0 || kk > 0);
+                        tc_mma_tmem_a(tmem + kOCol + 128 * q, tmem + b * kTcKeys + HK * q + 8 * kk,
+                                      tc_smem_desc(av + b * TILE + (q * (HK / 16) + kk) * 2048, REG,
+                                                   1024),
+                                      id_pv, c.j > 0 || kk > 0);
                     tc_commit(&pv_done[q]);
                 }
                 tc_commit(&v_empty[b]);
@@ -587,9 +586,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tc_ld32(trow + b * kTcKeys + HK * q + 32 * c,
                             reinterpret_cast<uint32_t(&)[32]>(sc[32 * c]));
                 tc_wait_ld();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s_free[b]);
                 ok = __all_sync(0xffffffffu, mbar_wait(&v_full[b], ph, abort_flag, p.status));
                 if (!ok) break;
                 const unsigned bad = ((unsigned)vbad[b] >> (4 * q)) & 0xFu;  // this half's blocks
@@ -638,15 +634,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 const float psum = ((psp[0] + psp[1]) + (psp[2] + psp[3])) +
                                    ((psp[4] + psp[5]) + (psp[6] + psp[7]));
+                // P(J-1) V(J-1) done: O may be rescaled below, and waiting
+                // here, before P(J) is released, keeps every wait on pv_done at
+                // most one phase behind (after the release P(J) V(J) could
+                // complete first and make the parity ambiguous).  It has almost
+                // always completed by now.
                 if (J >= 1) {
-                    // P overwrites the last tile's, and O may be rescaled: that P V must be done
                     ok = __all_sync(0xffffffffu,
                                     mbar_wait(&pv_done[q], (J - 1) & 1, abort_flag, p.status));
                     if (!ok) break;
                     tc_fence_after();
                 }
+                // P over the scores just read (tensor memory, this group's half)
+                tc_st32(trow + b * kTcKeys + HK * q, reinterpret_cast<uint32_t(&)[32]>(pk[0]));
                 if (__any_sync(0xffffffffu, grow)) {
-                    // (whole warp: tensor-memory access is warp-wide)
+                    // O_q holds P(J-1) V(J-1): scale it (whole warp: tensor-memory
+                    // access is warp-wide)
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         uint32_t o[32];
@@ -656,14 +659,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
                         tc_st32(trow + ocol + 32 * c, o);
                     }
-                    tc_wait_st();
                 }
+                tc_wait_st();
                 l = l * f + psum;
-                // P row: 8 chunks of 8 keys in this group's half of the P tile
-#pragma unroll
-                for (int c = 0; c < HK / 8; ++c)
-                    *reinterpret_cast<uint4*>(sp + q * REG + r * 128 + ((c ^ (r & 7)) << 4)) =
-                        make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
                 // V rows of this half no row may see must be finite zeros before
                 // P V (0 x NaN = NaN)
                 if (j == it.nkv - 1 || bad) {
@@ -676,7 +674,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                 }
                 asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-                tc_fence_before();  // a rescaled O is ordered before the next MMA
+                tc_fence_before();  // P and a rescaled O are ordered before the next MMA
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&p_full[q]);
             }
@@ -745,9 +743,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 template <int D>
 size_t prefill_tc_smem() {
-    // 2 Q buffers, 2 K and 2 V stages, one P buffer, barriers, the (m, l)
-    // hand-over; 1 KB alignment slack (231 680 bytes at D = 128)
-    return 1024 + (size_t)6 * (D / 64) * kTcRows * 128 + 2 * kTcRows * 128 + 256 + 1024;
+    // 2 Q buffers, 2 K and 2 V stages, barriers and the (m, l) hand-over
+    // (under 2 KB); 1 KB alignment slack
+    return 1024 + (size_t)6 * (D / 64) * kTcRows * 128 + 2048;
 }
 
 // Which prefill kernel runs: the tcgen05 one unless PKV_PREFILL_KERNEL=mma

@@ -51,6 +51,18 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]; A holds M rows in tensor-memory lanes, two
+// 16-bit K elements per 32-bit column (element 2c in the low half of column
+// c), so a K-step of 16 is 8 columns.  Issued by one thread.
+__device__ __forceinline__ void tc_mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
+        : "memory");
+}
+
 // One arrival on `bar` once every tcgen05 operation this thread issued so far completes.
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
     asm volatile(
