@@ -285,6 +285,33 @@ __global__ void __launch_bounds__(kPrefillThreads)
 // wait is bounded.
 // ============================================================================
 constexpr int kTcThreads = 384;
+
+// Two-wide fp32 arithmetic and the three-input maximum of this architecture
+// (PTX fma/add .f32x2 on packed register pairs, max.f32 with three sources):
+// half the instructions of the softmax's inner loop.
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
 constexpr int kTcRows = 128;     // (query token, query head) rows per tile
 constexpr int kTcKeys = 128;     // keys per key tile
 constexpr float kTcRescale = 8.f;  // log2 of the largest P before O is rescaled
@@ -603,7 +630,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 float mul = sl2;
                 if (plain) {
 #pragma unroll
-                    for (int c = 0; c < HK; ++c) mxp[c & 7] = fmaxf(mxp[c & 7], sc[c]);
+                    for (int c = 0; c < HK; c += 2)
+                        mxp[(c >> 1) & 7] = max3(mxp[(c >> 1) & 7], sc[c], sc[c + 1]);
                 } else {
                     mul = 1.f;
 #pragma unroll
@@ -624,14 +652,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const float ms = m_used == -INFINITY ? 0.f : m_used;
                 // P in registers first: none of this waits on the tensor core
                 uint32_t pk[HK / 2];
-                float psp[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                const uint64_t mul2 = f2(mul, mul), nms2 = f2(-ms, -ms);
+                uint64_t acc2[4] = {f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
                 for (int c = 0; c < HK / 2; ++c) {
-                    const float p0 = fast_exp2(fmaf(sc[2 * c], mul, -ms));
-                    const float p1 = fast_exp2(fmaf(sc[2 * c + 1], mul, -ms));
-                    psp[c & 7] += p0 + p1;
+                    float a0, a1;
+                    f2_split(f2_fma(f2(sc[2 * c], sc[2 * c + 1]), mul2, nms2), a0, a1);
+                    const float p0 = fast_exp2(a0), p1 = fast_exp2(a1);
+                    acc2[c & 3] = f2_add(acc2[c & 3], f2(p0, p1));
                     pk[c] = E::pack(p0, p1);
                 }
+                float psp[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) f2_split(acc2[e], psp[2 * e], psp[2 * e + 1]);
                 const float psum = ((psp[0] + psp[1]) + (psp[2] + psp[3])) +
                                    ((psp[4] + psp[5]) + (psp[6] + psp[7]));
                 // P(J-1) V(J-1) done: O may be rescaled below, and waiting
