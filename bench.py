@@ -538,7 +538,11 @@ def run_prefill(args):
                                         "query_rows": int(qlens.sum()), "flops": flops},
         "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(tf / peak, 4) if peak else None,
-                     "note": "mma.sync m16n8k16 against the measured cuBLAS bf16 peak"},
+                     "kernel": ("prefill_tma_kernel (mma.sync m16n8k16)"
+                                if os.environ.get("PKV_PREFILL_KERNEL") == "mma" else
+                                "prefill_tc_kernel (tcgen05.mma kind::f16)"),
+                     "note": "causal FLOPs (4 * visible pairs * D * query heads) against the "
+                             "measured cuBLAS bf16 burst peak"},
         "gpu_launches": K}), flush=True)
 
 
