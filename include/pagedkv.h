@@ -39,6 +39,14 @@
  *    never dereferenced, the affected row is skipped or zero-filled, and a
  *    bit is set in the device status word (pkv_device_status).  No kernel
  *    traps, asserts or spins without a bound.
+ *  - The decode partition pass uses programmatic dependent launch.  If the
+ *    kernel before it on the stream lets its dependents start early
+ *    (griddepcontrol.launch_dependents; of this library's kernels only a
+ *    merge pass does, after its own partition pass has finished), the pass
+ *    may begin before that kernel ends.  Until that kernel completes, the
+ *    pass only reads context_lens, block_tables and the K/V pools.  It reads
+ *    q, k_new and v_new, and writes any output, only after the kernel
+ *    completes.
  */
 #ifndef PAGEDKV_H_
 #define PAGEDKV_H_

@@ -125,6 +125,7 @@ struct DecodeParams {
     int min_partition_blocks;  // lower bound of the adaptive choice
     int target_items;
     int even_split;            // TMA pass: cut the (sequence, head group, block) units evenly
+    int trigger_merge;         // TMA pass: a merge pass follows (let it launch early)
     float scale_log2;          // scale * log2(e): scores live in base 2
 };
 
@@ -629,7 +630,10 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
 
-    // validated lengths, partition length, partitions per sequence (all warps)
+    // validated lengths, partition length, partitions per sequence (all warps).
+    // This grid may start while the previous kernel of the stream (a merge
+    // pass) still runs: until the consumers' griddepcontrol.wait below it only
+    // reads the lengths, the tables and the cache, and writes shared memory.
     int my_blocks = 0;
     for (int s = tid; s < B; s += kTmaThreads) {
         int n = p.context_lens[s];
@@ -639,10 +643,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         }
         if (n > 0 && p.prefix_parts && p.k_new && (n - 1) / PKV_BLOCK_SIZE < p.skip_blocks) {
             if (blockIdx.x == 0) atomicOr(p.status, PKV_DEV_BAD_LENGTH);
-            if (p.slot_out && blockIdx.x == 0) p.slot_out[s] = -1;
         }
         sm_len[s] = n;
-        if (n == 0 && p.slot_out && blockIdx.x == 0) p.slot_out[s] = -1;
         my_blocks += (n + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
     }
     const int total_blocks = cta_sum<NC + 1>(my_blocks, red);
@@ -691,11 +693,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     }
     if (tid == 0) sm_off[B] = total_parts;
     __syncthreads();
-    if (blockIdx.x == 0) {
-        for (int s = tid; s <= B; s += kTmaThreads)
-            p.ws_offsets[s] = sm_off[s] + p.prefix_parts * s;
-    }
-    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    // only a merge pass may start early: a following partition pass (of the
+    // next call) must see this pass's cache writes complete
+    if (p.trigger_merge) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
     const int Hq = p.num_q_heads, Hkv = p.num_kv_heads;
     const size_t row_stride = (size_t)Hkv * D;
@@ -799,14 +799,6 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         }
         return true;
     };
-    if (even) {
-        // empty (or invalid) sequences have no units: their rows are zeros
-        for (int s = blockIdx.x; s < B; s += gridDim.x) {
-            if (sm_len[s] != 0) continue;
-            uint4* o = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + (size_t)s * Hq * D);
-            for (int x = tid; x < Hq * D / 8; x += kTmaThreads) o[x] = make_uint4(0u, 0u, 0u, 0u);
-        }
-    }
 
     if (warp == NC) {
         // ------------------------------------------------------------ producer
@@ -894,6 +886,30 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     }
 
     // -------------------------------------------------------------- consumers
+    // q, k_new, v_new and every output may belong to the previous kernel:
+    // wait for it (the producer above prefetches the cache meanwhile)
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    if (blockIdx.x == 0) {
+        for (int s = tid; s <= B; s += NC * 32)
+            p.ws_offsets[s] = sm_off[s] + p.prefix_parts * s;
+        if (p.slot_out) {
+            // no slot for an empty or invalid sequence, nor for a cascade
+            // token that would land in a shared block
+            for (int s = tid; s < B; s += NC * 32) {
+                const int n = sm_len[s];
+                if (n == 0 || (p.prefix_parts && p.k_new && (n - 1) / PKV_BLOCK_SIZE < p.skip_blocks))
+                    p.slot_out[s] = -1;
+            }
+        }
+    }
+    if (even) {
+        // empty (or invalid) sequences have no units: their rows are zeros
+        for (int s = blockIdx.x; s < B; s += gridDim.x) {
+            if (sm_len[s] != 0) continue;
+            uint4* o = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + (size_t)s * Hq * D);
+            for (int x = tid; x < Hq * D / 8; x += NC * 32) o[x] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
     const int w = warp;
     const int hl = w % HPI, sub = w / HPI;  // this consumer's head in the group, block phase
     const int gid = lane >> 2, tig = lane & 3;
@@ -1284,8 +1300,11 @@ struct MergeParams {
 template <typename T, int D>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const MergeParams p) {
     constexpr int PER = D / 32;
-    // launched early (programmatic dependent launch): wait for the partition pass
+    // launched early (programmatic dependent launch): wait for the partition
+    // pass; only then let the next grid (the next call's partition pass)
+    // start, so that it never overlaps this call's partition pass
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int wg = blockIdx.x * 4 + (threadIdx.x >> 5);
     if (wg >= p.num_seqs * p.num_q_heads) return;
@@ -1536,6 +1555,7 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp_i
         // per-head items: 8 per CTA; all-heads items carry Hkv heads each: 4 per CTA
         prm.target_items = grid * tma_items_per_cta(hpi);
     }
+    prm.trigger_merge = (passes & kPassMerge) && need_merge;
     if (passes & kPassPartition) {
         CUtensorMap tmk, tmv;
         const pkv_dtype dt = std::is_same<T, __nv_bfloat16>::value ? PKV_BF16 : PKV_F16;
@@ -1549,8 +1569,20 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp_i
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
             return PKV_ERR_CUDA;
-        kern<<<grid, kTmaThreads, smem, stream>>>(prm, tmk, tmv, nstages, hpi);
-        if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+        // programmatic dependent launch: the prologue and the first cache
+        // loads overlap the previous merge pass (see the kernel)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(kTmaThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, kern, prm, tmk, tmv, nstages, hpi) != cudaSuccess)
+            return PKV_ERR_CUDA;
     }
     if ((passes & kPassMerge) && need_merge) {
         const int warps = prm.num_seqs * prm.num_q_heads;
@@ -1656,6 +1688,7 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
     prm.min_partition_blocks = pb_lower;
     prm.target_items = 0;
     prm.even_split = 0;
+    prm.trigger_merge = 0;
     prm.scale_log2 = scale * kLog2e;
 
     MergeParams mp;
