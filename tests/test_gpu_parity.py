@@ -303,3 +303,48 @@ def test_layer_views_of_a_layer_major_pool(cuda_device):
         torch.cuda.synchronize()
         assert_attention_close(bits(out), want, oracle.F16, f"layer {layer}")
     assert pkv.pkv_device_status() == 0
+
+
+@pytest.mark.parametrize("dtype,Hq,Hkv,D,lens", [
+    ("bf16", 32, 8, 128, [1500, 2100, 33, 700]),     # long: partitions and a merge per step
+    ("f16", 16, 8, 128, [17, 64, 100, 31]),          # short: no merge
+])
+def test_consecutive_steps_see_the_previous_token(dtype, Hq, Hkv, D, lens, cuda_device):
+    """Two decode steps enqueued back to back, as a decoder runs them: the
+    second step's partition pass may start while the first step's merge still
+    runs, and its context includes the token the first step wrote."""
+    lens2 = [n + 1 for n in lens]
+    w, inp = _custom(cuda_device, dtype, lens2, Hq, Hkv, D, 512, seed=71)
+    tables = inp["block_tables_host"]
+    dev = cuda_device
+    g = torch.Generator(device=dev).manual_seed(72)
+    dt = inp["q"].dtype
+    rnd = lambda *sh: torch.randn(*sh, generator=g, device=dev).to(dt)
+    B = len(lens)
+    q1, q2 = rnd(B, Hq, D), rnd(B, Hq, D)
+    kn1, vn1, kn2, vn2 = rnd(B, Hkv, D), rnd(B, Hkv, D), rnd(B, Hkv, D), rnd(B, Hkv, D)
+    cl1 = torch.tensor(lens, dtype=torch.int32, device=dev)
+    cl2 = torch.tensor(lens2, dtype=torch.int32, device=dev)
+    kc, vc = inp["k_cache"][0], inp["v_cache"][0]
+    hk, hv = bits(kc), bits(vc)                        # the pools before either step
+    max_len = max(lens2)
+    ws = pkv.new_workspace(B, Hq, D, max_len, dev)
+    out1, out2 = torch.empty_like(q1), torch.empty_like(q2)
+    torch.cuda.synchronize()
+    pkv.paged_kv_decode_step(q1, kn1, vn1, kc, vc, inp["block_tables"], cl1, max_len, w.scale,
+                             out1, ws)
+    pkv.paged_kv_decode_step(q2, kn2, vn2, kc, vc, inp["block_tables"], cl2, max_len, w.scale,
+                             out2, ws)
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_status() == 0
+    code = dtype_code(w)
+    nb = w.num_blocks
+    s1 = oracle.slot_mapping(tables, np.array(lens, np.int32), 16, nb)
+    hk, hv = oracle.reshape_and_cache(bits(kn1), bits(vn1), hk, hv, s1)
+    s2 = oracle.slot_mapping(tables, np.array(lens2, np.int32), 16, nb)
+    hk, hv = oracle.reshape_and_cache(bits(kn2), bits(vn2), hk, hv, s2)
+    want = oracle.decode_attention(code, bits(q2), hk, hv, tables, np.array(lens2, np.int32),
+                                   w.scale)
+    assert_attention_close(bits(out2), want, code, "second step")
+    assert np.array_equal(bits(kc).reshape(-1, Hkv, D)[s1], bits(kn1))
+    assert np.array_equal(bits(kc).reshape(-1, Hkv, D)[s2], bits(kn2))
