@@ -572,26 +572,28 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
 // ============================================================================
 // Partition pass, TMA version (the default).
 //
-// One persistent CTA per SM: four consumer warps do exactly the arithmetic of
-// the kernel above, and one producer warp feeds them.  The producer walks the
-// same items and blocks, reads the block table 32 entries at a time, and for
-// each block issues cp.async.bulk.tensor copies of the 16 rows x D K and V
-// tiles of its KV head (boxes of 16 rows x 64 elements, 128-byte swizzle)
-// into a ring of shared-memory stages, one ring per consumer warp, tracked
-// by "full" / "empty" mbarriers.  The producer runs ahead across item
-// boundaries, so up to (ring size) blocks per consumer are in flight
-// regardless of registers.  Consumers read their operands with ldmatrix
-// (.trans for V), which the swizzle makes conflict-free, and release each
-// stage as soon as its fragments are in registers.  Every mbarrier wait is
-// bounded: on a time-out the kernel sets PKV_DEV_TIMEOUT, stops issuing and
-// waiting, lets every copy it issued land, and returns.
+// One persistent CTA per SM of eight warps, each doing the arithmetic of the
+// kernel above on its share of the blocks.  Every warp feeds itself: it walks
+// its blocks twice, once to load and once to consume, and keeps a ring of
+// shared-memory stages, each holding the 16 rows x D K and V tiles of one
+// block of its KV head.  The tiles arrive by cp.async.bulk.tensor copies of
+// boxes of 16 rows x 64 elements with the 128-byte swizzle, each stage
+// tracked by a "full" mbarrier.  Lane 0 refills a stage with the block one
+// ring ahead as soon as the warp's fragments of it are in registers (read
+// with ldmatrix, .trans for V, conflict-free under the swizzle).  Every slot
+// but the one being read is therefore in flight at all times, across item
+// boundaries.  Every mbarrier wait is bounded: on a time-out the kernel sets
+// PKV_DEV_TIMEOUT, stops issuing and waiting, lets every copy it issued land,
+// and returns.
 // ============================================================================
 constexpr int kTmaConsumers = 8;
-constexpr int kTmaThreads = (kTmaConsumers + 1) * 32;
+// threads of the TMA partition kernel: 8 consumer warps, plus the producer
+// warp unless the consumers feed themselves
+__host__ __device__ constexpr int tma_threads(bool self_feed) { return (kTmaConsumers + (self_feed ? 0 : 1)) * 32; }
 constexpr int kTmaItemsPerCta = 8;
 constexpr int kTmaMaxStages = 8;
-template <typename T, int D, bool kOneHead>
-__global__ void __launch_bounds__(kTmaThreads, 1)
+template <typename T, int D, bool kOneHead, bool kSelfFeed>
+__global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
     decode_partition_tma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
                                 const __grid_constant__ CUtensorMap tmap_v, int nstages,
                                 int heads_per_item) {
@@ -614,6 +616,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     float* sm_o = reinterpret_cast<float*>(last_use + NC * nstages);   // [NC][g][DP]
     float* sm_m = sm_o + NC * g * DP;                                  // [NC][8]
     float* sm_l = sm_m + NC * kMaxGroup;                               // [NC][8]
+    constexpr int NT = tma_threads(kSelfFeed), NW = NT / 32;  // threads, warps
     int* red = reinterpret_cast<int*>(sm_l + NC * kMaxGroup);          // [NC + 1]
     volatile int* abort_flag = red + NC + 1;
     int* sm_len = red + NC + 2 + NC;                                   // [B]
@@ -635,7 +638,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     // pass) still runs: until the consumers' griddepcontrol.wait below it only
     // reads the lengths, the tables and the cache, and writes shared memory.
     int my_blocks = 0;
-    for (int s = tid; s < B; s += kTmaThreads) {
+    for (int s = tid; s < B; s += NT) {
         int n = p.context_lens[s];
         if (n < 0 || n > p.len_bound) {
             if (blockIdx.x == 0) atomicOr(p.status, PKV_DEV_BAD_LENGTH);
@@ -647,7 +650,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         sm_len[s] = n;
         my_blocks += (n + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
     }
-    const int total_blocks = cta_sum<NC + 1>(my_blocks, red);
+    const int total_blocks = cta_sum<NW>(my_blocks, red);
     const bool even = p.even_split != 0;  // uniform over the grid
     int PB = p.partition_blocks;
     if (!even && PB <= 0) {
@@ -655,7 +658,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         if ((long long)B * groups0 >= 4ll * gridDim.x) {
             // enough items without splitting: one partition per sequence
             int my_max = 0;
-            for (int s = tid; s < B; s += kTmaThreads) {
+            for (int s = tid; s < B; s += NT) {
                 const int nb = (sm_len[s] + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE - p.skip_blocks;
                 my_max = max(my_max, nb);
             }
@@ -665,7 +668,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             __syncthreads();
             int mx = 0;
 #pragma unroll
-            for (int w = 0; w < NC + 1; ++w) mx = max(mx, red[w]);
+            for (int w = 0; w < NW; ++w) mx = max(mx, red[w]);
             PB = max(mx, p.min_partition_blocks);
         } else {
             // items cover heads_per_item KV heads of their blocks: aim at target_items
@@ -676,7 +679,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             PB = (int)(want < lo ? lo : (want > hi ? hi : want));
         }
     }
-    const int chunk = (B + kTmaThreads - 1) / kTmaThreads;
+    const int chunk = (B + NT - 1) / NT;
     const int s_lo = min(B, tid * chunk), s_hi = min(B, s_lo + chunk);
     // item mode: partitions per sequence; even split: blocks per sequence
     auto units_of = [&](int s) {
@@ -686,7 +689,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     int mine = 0;
     for (int s = s_lo; s < s_hi; ++s) mine += units_of(s);
     int total_parts = 0;
-    int run = cta_exclusive_scan<NC + 1>(mine, red, &total_parts);
+    int run = cta_exclusive_scan<NW>(mine, red, &total_parts);
     for (int s = s_lo; s < s_hi; ++s) {
         sm_off[s] = run;
         run += units_of(s);
@@ -800,7 +803,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         return true;
     };
 
-    if (warp == NC) {
+    constexpr bool self_feed = kSelfFeed;
+    if (!self_feed && warp == NC) {
         // ------------------------------------------------------------ producer
         // Batches of BB blocks x HPI heads, lane t issuing (block jb + t / HPI,
         // head t % HPI of the group) for consumer t % HPI + HPI * ((block - lo) % CPH).  A batch
@@ -886,8 +890,79 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     }
 
     // -------------------------------------------------------------- consumers
+    // Self-feeding (measured faster when items carry 4 or more heads, i.e. few
+    // consumers per head and short per-head runs): every warp feeds its own
+    // ring of nstages slots, lane 0 issuing the TMA copies of the block
+    // nstages ahead of the one the warp consumes as soon as the consumed
+    // stage's fragments are in registers.  Two walks over the same sequence of
+    // (item, block) give the blocks to fetch and the blocks to consume.
+    // Otherwise the producer warp above fills the rings.
+    const int w = warp;
+    const int hl = w % HPI, sub = w / HPI;  // this consumer's head in the group, block phase
+    struct Stream {
+        Cursor c;
+        Item it;
+        int j;
+        bool live;
+    };
+    Stream fs;  // the fetch walk: this warp's next block to load
+    fs.live = false;
+    fs.j = 0;
+    auto skip_done = [&](Stream& st) {  // past items this warp has no (more) block in
+        while (st.live && st.j >= st.it.hi) {
+            st.live = next_item(st.c, st.it);
+            if (st.live) st.j = st.it.lo + sub;
+        }
+    };
+    // lane 0 loads the table entry of the next block to fetch one fetch early,
+    // so that no refill waits on a global load
+    auto table_entry = [&](const Stream& st) {
+        return st.live && lane == 0
+                   ? p.block_tables[(size_t)st.it.s * p.max_blocks_per_seq + st.j]
+                   : 0;
+    };
+    int fs_id = 0;
+    int nfetch = 0;        // stages issued by this warp
+    bool feeding = true;   // false after a wait gave up: issue nothing more
+    auto fetch_next = [&]() {  // whole warp; lane 0 issues
+        if (!fs.live || !feeding) return;
+        const int k = w * nstages + nfetch % nstages;
+        if (lane == 0) {
+            int id = fs_id;
+            if (id < 0 || id >= p.num_blocks) {
+                atomicOr(p.status, PKV_DEV_BAD_BLOCK_ID);
+                id = -1;  // block 0 is fetched and fully masked
+            }
+            stage_id[k] = id;
+            last_use[k] = nfetch;
+            mbar_arrive_expect_tx(&full[k], STAGE);
+            unsigned char* st = ring + (size_t)k * STAGE;
+            const int row = (id < 0 ? 0 : id) * PKV_BLOCK_SIZE;
+            const int h = fs.it.hg * HPI + hl;
+#pragma unroll
+            for (int hh = 0; hh < HALVES; ++hh) {
+                tma_load_rows(st + hh * 2048, &tmap_k, &full[k], hh * 64, h, row);
+                tma_load_rows(st + TILE + hh * 2048, &tmap_v, &full[k], hh * 64, h, row);
+            }
+        }
+        ++nfetch;
+        fs.j += CPH;
+        skip_done(fs);
+        fs_id = table_entry(fs);
+    };
+    // the first nstages blocks: only the cache is read, so this may overlap
+    // the previous kernel
+    if constexpr (kSelfFeed) {
+        fs.c = cursor_begin();
+        fs.live = next_item(fs.c, fs.it);
+        fs.j = fs.live ? fs.it.lo + sub : 0;
+        skip_done(fs);
+        fs_id = table_entry(fs);
+        for (int t = 0; t < nstages; ++t) fetch_next();
+    }
+
     // q, k_new, v_new and every output may belong to the previous kernel:
-    // wait for it (the producer above prefetches the cache meanwhile)
+    // wait for it
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
     if (blockIdx.x == 0) {
         for (int s = tid; s <= B; s += NC * 32)
@@ -910,8 +985,6 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             for (int x = tid; x < Hq * D / 8; x += NC * 32) o[x] = make_uint4(0u, 0u, 0u, 0u);
         }
     }
-    const int w = warp;
-    const int hl = w % HPI, sub = w / HPI;  // this consumer's head in the group, block phase
     const int gid = lane >> 2, tig = lane & 3;
     const T* __restrict__ q = static_cast<const T*>(p.q);
     int ncons = 0;  // stages this warp has consumed
@@ -945,7 +1018,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
 
         for (int j = it.lo + sub; j < it.hi; j += CPH, ++ncons) {
             const int k = w * nstages + ncons % nstages;
-            const bool ok = mbar_wait(&full[k], (ncons / nstages) & 1, abort_flag, p.status);
+            const bool ok = __all_sync(
+                0xffffffffu, mbar_wait(&full[k], (ncons / nstages) & 1, abort_flag, p.status));
             unsigned char* st = ring + (size_t)k * STAGE;
             const int id = ok ? stage_id[k] : -1;
             const int nv = id < 0 ? 0 : min(PKV_BLOCK_SIZE, n - j * PKV_BLOCK_SIZE);
@@ -984,8 +1058,17 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
                     ldsm_x4_trans(vf[ks], vt + swz(tok, 2 * ks + (mi & 1)));
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[k]);  // fragments are in registers
+            // the fragments are in registers: release the slot to the
+            // producer, or refill it with the block nstages ahead (the
+            // async-proxy copy after the warp's reads)
+            if constexpr (kSelfFeed) {
+                asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+                __syncwarp();
+                if (ok) fetch_next(); else feeding = false;
+            } else {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[k]);
+            }
             if (!ok || nv == 0) continue;
 
             float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
@@ -1111,6 +1194,15 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             }
         }
         asm volatile("bar.sync 1, %0;\n" ::"r"(NC * 32) : "memory");
+    }
+    // every copy this warp issued must land before the CTA may exit: wait for
+    // the last use issued into each of its slots (normally already consumed)
+    __syncwarp();
+    if (kSelfFeed && lane == 0) {
+        for (int k = w * nstages; k < (w + 1) * nstages; ++k) {
+            const int use = last_use[k];
+            if (use >= 0) mbar_drain(&full[k], (use / nstages) & 1, p.status);
+        }
     }
 }
 
@@ -1556,14 +1648,20 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp_i
         prm.target_items = grid * tma_items_per_cta(hpi);
     }
     prm.trigger_merge = (passes & kPassMerge) && need_merge;
+
     if (passes & kPassPartition) {
         CUtensorMap tmk, tmv;
         const pkv_dtype dt = std::is_same<T, __nv_bfloat16>::value ? PKV_BF16 : PKV_F16;
         if (!make_pool_map(&tmk, prm.k_cache, prm.num_blocks, prm.num_kv_heads, D, dt) ||
             !make_pool_map(&tmv, prm.v_cache, prm.num_blocks, prm.num_kv_heads, D, dt))
             return PKV_ERR_CUDA;
-        auto kern = hpi == 1 ? decode_partition_tma_kernel<T, D, true>
-                             : decode_partition_tma_kernel<T, D, false>;
+        // consumers that feed themselves measured faster with 4 or more heads
+        // per item (short contexts: 28-layer steps 8 % faster), the producer
+        // warp with 1 or 2 (long contexts: 10 % faster)
+        const bool self_feed = hpi >= 4;
+        auto kern = self_feed  ? decode_partition_tma_kernel<T, D, false, true>
+                    : hpi == 1 ? decode_partition_tma_kernel<T, D, true, false>
+                               : decode_partition_tma_kernel<T, D, false, false>;
         const size_t smem =
             tma_fixed_smem(D, prm.num_seqs, prm.group) + (size_t)nstages * tma_stage_smem(D);
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
@@ -1573,7 +1671,7 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp_i
         // loads overlap the previous merge pass (see the kernel)
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)grid);
-        cfg.blockDim = dim3(kTmaThreads);
+        cfg.blockDim = dim3(tma_threads(self_feed));
         cfg.dynamicSmemBytes = smem;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
