@@ -64,7 +64,7 @@ typedef struct CUstream_st* pkv_stream_t;
 typedef enum {
     PKV_OK = 0,
     PKV_ERR_INVALID_ARG = 1,   /* null pointer, bad size, inconsistent shapes */
-    PKV_ERR_UNSUPPORTED = 2,   /* a valid shape this build has no kernel for */
+    PKV_ERR_UNSUPPORTED = 2,   /* a valid shape the library has no kernel for */
     PKV_ERR_NO_BLOCKS = 3,     /* allocator: not enough free blocks (nothing taken) */
     PKV_ERR_BAD_BLOCK_ID = 4,  /* allocator: id out of range or not allocated */
     PKV_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed */

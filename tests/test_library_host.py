@@ -128,7 +128,7 @@ def test_host_validation_before_any_cuda_call(L):
     rc = L.paged_attention_decode(p, p, p, p, 4, p, 64, 2, 12, 8, 128, 10, 0.1, p, p, 1 << 20,
                                   0, None)
     assert rc == 1
-    # head_dim 96 and group 16 are valid shapes this build has no kernel for
+    # head_dim 96 and group 16 are valid shapes the library has no kernel for
     assert L.paged_attention_decode(p, p, p, p, 4, p, 64, 2, 16, 8, 96, 10, 0.1, p, p, 1 << 20,
                                     0, None) == 2
     assert L.paged_attention_decode(p, p, p, p, 4, p, 64, 2, 32, 2, 128, 10, 0.1, p, p, 1 << 20,
