@@ -405,11 +405,15 @@ size_t paged_kv_decode_step_staging_bytes(int num_seqs, int num_q_heads, int num
                                           int head_dim, int max_blocks_per_seq);
 
 /* paged_kv_decode_step with the step's inputs and its output in HOST memory
- * (page-locked, so that the copies are asynchronous): q_host, k_new_host,
- * v_new_host, block_tables_host and context_lens_host are copied into the
- * caller's device `staging` buffer on `stream` (one cudaMemcpyAsync each),
- * the step runs on the device-resident pools, and the attention output is
- * copied back to out_host.  The call returns once everything is enqueued:
+ * (page-locked): q_host, k_new_host, v_new_host, block_tables_host and
+ * context_lens_host are brought into the caller's device `staging` buffer on
+ * `stream`, the step runs on the device-resident pools, and the attention
+ * output lands in out_host.  Host buffers that have a device mapping
+ * (page-locked memory under unified addressing) are read by one staging
+ * kernel and the output is written to out_host by the attention kernels
+ * themselves; a buffer without one is moved by cudaMemcpyAsync.  The host
+ * buffers must stay unchanged until the stream reaches the step, as for any
+ * asynchronous copy.  The call returns once everything is enqueued:
  * synchronise `stream` before reading out_host.  Shapes and dtypes as for
  * paged_kv_decode_step; staging_bytes must be at least
  * paged_kv_decode_step_staging_bytes(...). */

@@ -1,5 +1,6 @@
 // pkv_api.cu -- library-wide entry points: version, status text, pool sizing,
 // the device status word, and the host-buffer decode step.
+#include <algorithm>
 #include <mutex>
 
 #include "pkv_internal.cuh"
@@ -122,6 +123,55 @@ size_t paged_kv_decode_step_staging_bytes(int num_seqs, int num_q_heads, int num
     return total;
 }
 
+namespace {
+
+// Up to five host-to-device copies done by one kernel that reads page-locked
+// host memory through its device mapping: one launch instead of one copy
+// engine transfer per input (each of which costs a few microseconds of set-up
+// at these sizes).
+struct StageJobs {
+    const void* src[5];
+    void* dst[5];
+    size_t bytes[5];
+    int n;
+};
+
+__global__ void __launch_bounds__(256) stage_inputs_kernel(const StageJobs jobs) {
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    const size_t t0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    for (int j = 0; j < jobs.n; ++j) {
+        const size_t bytes = jobs.bytes[j];
+        const bool vec = ((reinterpret_cast<uintptr_t>(jobs.src[j]) |
+                           reinterpret_cast<uintptr_t>(jobs.dst[j])) & 15u) == 0;
+        size_t done = 0;
+        if (vec) {
+            const uint4* s = static_cast<const uint4*>(jobs.src[j]);
+            uint4* d = static_cast<uint4*>(jobs.dst[j]);
+            const size_t n16 = bytes / 16;
+            for (size_t i = t0; i < n16; i += stride) d[i] = s[i];
+            done = n16 * 16;
+        }
+        // the rest in 4-byte words (every size here is a multiple of 4)
+        const uint32_t* s4 = static_cast<const uint32_t*>(jobs.src[j]);
+        uint32_t* d4 = static_cast<uint32_t*>(jobs.dst[j]);
+        for (size_t i = done / 4 + t0; i < bytes / 4; i += stride) d4[i] = s4[i];
+    }
+}
+
+// The device address of page-locked host memory, or null if the pointer has
+// none (not page-locked, or not mapped into the device's address space).
+const void* mapped_host(const void* host) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+        (void)cudaGetLastError();  // clear the error a plain pointer may leave
+        return nullptr;
+    }
+    if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr) return nullptr;
+    return a.devicePointer;
+}
+
+}  // namespace
+
 pkv_status paged_kv_decode_step_host(const void* q_host, const void* k_new_host,
                                      const void* v_new_host, const int32_t* block_tables_host,
                                      const int32_t* context_lens_host, void* out_host,
@@ -151,20 +201,44 @@ pkv_status paged_kv_decode_step_host(const void* q_host, const void* k_new_host,
     int32_t* bt_d = reinterpret_cast<int32_t*>(p);  p += align_up(bt_bytes, 256);
     int32_t* cl_d = reinterpret_cast<int32_t*>(p);  p += align_up(B * 4, 256);
     void* out_d = p;
-    const cudaMemcpyKind h2d = cudaMemcpyHostToDevice;
-    if (cudaMemcpyAsync(q_d, q_host, q_bytes, h2d, st) != cudaSuccess ||
-        cudaMemcpyAsync(kn_d, k_new_host, kv_bytes, h2d, st) != cudaSuccess ||
-        cudaMemcpyAsync(vn_d, v_new_host, kv_bytes, h2d, st) != cudaSuccess ||
-        cudaMemcpyAsync(bt_d, block_tables_host, bt_bytes, h2d, st) != cudaSuccess ||
-        cudaMemcpyAsync(cl_d, context_lens_host, B * 4, h2d, st) != cudaSuccess)
-        return PKV_ERR_CUDA;
+    // inputs with a device mapping are staged by one kernel, the others by
+    // one cudaMemcpyAsync each
+    const void* srcs[5] = {q_host, k_new_host, v_new_host, block_tables_host, context_lens_host};
+    void* dsts[5] = {q_d, kn_d, vn_d, bt_d, cl_d};
+    const size_t sizes[5] = {q_bytes, kv_bytes, kv_bytes, bt_bytes, B * 4};
+    StageJobs jobs;
+    jobs.n = 0;
+    for (int i = 0; i < 5; ++i) {
+        const void* mapped = mapped_host(srcs[i]);
+        if (mapped && (reinterpret_cast<uintptr_t>(mapped) & 3u) == 0) {
+            jobs.src[jobs.n] = mapped;
+            jobs.dst[jobs.n] = dsts[i];
+            jobs.bytes[jobs.n] = sizes[i];
+            ++jobs.n;
+        } else if (cudaMemcpyAsync(dsts[i], srcs[i], sizes[i], cudaMemcpyHostToDevice, st) !=
+                   cudaSuccess) {
+            return PKV_ERR_CUDA;
+        }
+    }
+    if (jobs.n > 0) {
+        size_t total = 0;
+        for (int i = 0; i < jobs.n; ++i) total += jobs.bytes[i];
+        const int blocks = (int)std::min<size_t>(128, (total / 16 + 255) / 256 + 1);
+        stage_inputs_kernel<<<blocks, 256, 0, st>>>(jobs);
+        if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    }
+    // the kernels only store to `out`: with a device mapping of out_host they
+    // write the result there directly, else into staging and one copy back
+    void* out_mapped = const_cast<void*>(mapped_host(out_host));
+    const bool direct = out_mapped && (reinterpret_cast<uintptr_t>(out_mapped) & 15u) == 0;
     pkv_status rc = paged_kv_decode_step(q_d, kn_d, vn_d, k_cache, v_cache, bt_d,
                                          max_blocks_per_seq, cl_d, max_context_len, num_seqs,
                                          num_q_heads, num_kv_heads, head_dim, num_blocks, scale,
-                                         out_d, nullptr, workspace, workspace_bytes, dtype,
-                                         stream);
+                                         direct ? out_mapped : out_d, nullptr, workspace,
+                                         workspace_bytes, dtype, stream);
     if (rc != PKV_OK) return rc;
-    if (cudaMemcpyAsync(out_host, out_d, q_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    if (!direct &&
+        cudaMemcpyAsync(out_host, out_d, q_bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return PKV_ERR_CUDA;
     return PKV_OK;
 }

@@ -71,12 +71,14 @@ def _run(c, D, dev):
 
 @pytest.mark.parametrize("dtype,Hq,Hkv,D", [("bf16", 32, 8, 128), ("f16", 32, 4, 64),
                                              ("bf16", 8, 8, 128), ("f16", 16, 8, 64),
-                                             ("bf16", 12, 4, 128)])
+                                             ("bf16", 12, 4, 128), ("f16", 32, 2, 128)])
 def test_prefill_matches_oracle(dtype, Hq, Hkv, D, cuda_device):
     specs = [(100, 100), (300, 64), (33, 1), (17, 17), (5, 3), (450, 160), (64, 16), (1, 1)]
     c = _case(cuda_device, dtype, specs, Hq, Hkv, D, seed=Hq + D)
     out, want, code, bt, cl = _run(c, D, cuda_device)
     assert_attention_close(bits(out), want, code, f"prefill g={Hq // Hkv} D={D}")
+    if Hq // Hkv > 8:
+        return                                    # decode attention serves g <= 8
     # the last row of every chunk sees the whole context: it is a decode row
     last = torch.from_numpy(c["cu"][1:] - 1).to(cuda_device).long()
     dec = torch.empty(len(specs), Hq, D, dtype=c["q"].dtype, device=cuda_device)
