@@ -474,6 +474,14 @@ pkv_status pkv_device_status(unsigned int* flags, int reset);
  * trapping. */
 pkv_status paged_kv_last_error(pkv_stream_t stream);
 
+/* Diagnostic of the bounded waits: launches one warp on `stream` that waits
+ * on an mbarrier nothing arrives on, with the same bounded wait every kernel
+ * here uses, limited to about 0.1 s.  The wait gives up, sets
+ * PKV_DEV_TIMEOUT in the device status word and the kernel returns; the
+ * context stays usable.  The pages have no counterpart: this exercises the
+ * failure path that replaces trapping or hanging. */
+pkv_status pkv_selftest_bounded_wait(pkv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -25,7 +25,7 @@ __all__ = [
     "paged_attention_cascade_workspace_bytes", "paged_attention_decode_cascade",
     "paged_kv_decode_step_cascade", "new_cascade_workspace", "paged_attention_prefill",
     "paged_kv_decode_step_staging_bytes", "paged_kv_decode_step_host", "pkv_device_status",
-    "paged_kv_last_error",
+    "paged_kv_last_error", "pkv_selftest_bounded_wait",
     "BlockAllocator", "new_workspace", "paged_kv_block_hash", "paged_kv_copy_blocks", "paged_attention_decode_noalloc",
     "NOALLOC_SCRATCH_BYTES",
 ]
@@ -93,6 +93,7 @@ _SIGS = {
                                    _i, _i, _i, _i, _i, _f, _vp, _sz, _i, _vp], _i),
     "pkv_device_status": ([ctypes.POINTER(ctypes.c_uint), _i], _i),
     "paged_kv_last_error": ([ctypes.c_void_p], _i),
+    "pkv_selftest_bounded_wait": ([ctypes.c_void_p], _i),
     "paged_kv_num_cached": ([_vp], _i),
     "paged_kv_block_hash": ([ctypes.c_uint64, _vp, _i], ctypes.c_uint64),
     "paged_kv_prefix_insert": ([_vp, ctypes.c_int32, ctypes.c_uint64], _i),
@@ -487,6 +488,11 @@ def paged_kv_last_error(stream=None) -> int:
     """Status code for the device checks of work on `stream` (waits for it; clears
     the device status word).  Returned, not raised: 0 means no flag was set."""
     return int(lib().paged_kv_last_error(_stream(stream)))
+
+
+def pkv_selftest_bounded_wait(stream=None) -> None:
+    """Enqueue the bounded-wait diagnostic (sets DEV_TIMEOUT after ~0.1 s)."""
+    _check("pkv_selftest_bounded_wait", lib().pkv_selftest_bounded_wait(_stream(stream)))
 
 
 class BlockAllocator:

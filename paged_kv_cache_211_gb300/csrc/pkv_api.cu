@@ -4,6 +4,7 @@
 #include <mutex>
 
 #include "pkv_internal.cuh"
+#include "pkv_tma.cuh"
 
 namespace {
 
@@ -158,6 +159,21 @@ __global__ void __launch_bounds__(256) stage_inputs_kernel(const StageJobs jobs)
     }
 }
 
+// One warp waits on an mbarrier that nothing arrives on, with the bounded wait
+// every kernel of the library uses (here limited to `limit` cycles): it must
+// give up, set PKV_DEV_TIMEOUT and return.
+__global__ void bounded_wait_selftest_kernel(unsigned int* status, long long limit) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        pkv::mbar_init(&bar, 1);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    __syncwarp();
+    pkv::mbar_wait(&bar, 0, &abort_flag, status, limit);
+}
+
 // The device address of page-locked host memory, or null if the pointer has
 // none (not page-locked, or not mapped into the device's address space).
 const void* mapped_host(const void* host) {
@@ -171,6 +187,15 @@ const void* mapped_host(const void* host) {
 }
 
 }  // namespace
+
+pkv_status pkv_selftest_bounded_wait(pkv_stream_t stream) {
+    unsigned int* status = pkv::status_word();
+    if (!status) return PKV_ERR_CUDA;
+    // ~0.1 s at the GB300's 2 GHz SM clock
+    bounded_wait_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        status, 200000000ll);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
 
 pkv_status paged_kv_decode_step_host(const void* q_host, const void* k_new_host,
                                      const void* v_new_host, const int32_t* block_tables_host,

@@ -46,14 +46,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Waits for the phase of `bar` with parity `parity`.  Returns false without
 // waiting once *abort is set, and sets *abort and the status bit when the
-// wait exceeds kWaitCycles.
+// wait exceeds `limit` cycles.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          unsigned int* status) {
+                                          unsigned int* status, long long limit = kWaitCycles) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (!*abort) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (clock64() - t0 > kWaitCycles) {
+        if (clock64() - t0 > limit) {
             *abort = 1;
             atomicOr(status, PKV_DEV_TIMEOUT);
             return false;

@@ -348,3 +348,18 @@ def test_consecutive_steps_see_the_previous_token(dtype, Hq, Hkv, D, lens, cuda_
     assert_attention_close(bits(out2), want, code, "second step")
     assert np.array_equal(bits(kc).reshape(-1, Hkv, D)[s1], bits(kn1))
     assert np.array_equal(bits(kc).reshape(-1, Hkv, D)[s2], bits(kn2))
+
+
+def test_bounded_wait_gives_up_and_reports(cuda_device):
+    """A kernel waiting on an mbarrier that nothing arrives on gives up after its
+    bound (~0.1 s here), flags PKV_DEV_TIMEOUT and returns; the context stays
+    usable for the next call."""
+    pkv.pkv_device_status(reset=True)
+    pkv.pkv_selftest_bounded_wait()
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_status(reset=True) & pkv.DEV_TIMEOUT
+    w, inp = _custom(cuda_device, "bf16", [40, 17, 300], 8, 4, 128, 64, seed=9)
+    want, _, _ = compact_oracle_step(inp, np.arange(3))
+    out, _ = _run_step(inp, cuda_device)
+    assert pkv.pkv_device_status() == 0
+    assert_attention_close(bits(out), want, oracle.BF16, "after a timed-out wait")
