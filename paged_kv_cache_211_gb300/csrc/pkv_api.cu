@@ -249,8 +249,23 @@ pkv_status paged_kv_decode_step_host(const void* q_host, const void* k_new_host,
         size_t total = 0;
         for (int i = 0; i < jobs.n; ++i) total += jobs.bytes[i];
         const int blocks = (int)std::min<size_t>(128, (total / 16 + 255) / 256 + 1);
-        stage_inputs_kernel<<<blocks, 256, 0, st>>>(jobs);
-        if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+        // programmatic dependent launch: after a previous step's merge pass it
+        // may run alongside it (that merge lets dependents start only once its
+        // partition pass, the last reader of the staging buffers, has
+        // finished, and itself reads only the workspace); this kernel never
+        // lets its own dependents start early, so the partition pass sees the
+        // staged inputs complete
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)blocks);
+        cfg.blockDim = dim3(256);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, stage_inputs_kernel, jobs) != cudaSuccess) return PKV_ERR_CUDA;
     }
     // the kernels only store to `out`: with a device mapping of out_host they
     // write the result there directly, else into staging and one copy back
