@@ -226,9 +226,11 @@ size_t paged_attention_workspace_bytes(int num_seqs, int num_q_heads, int head_d
  * and query head i, with n = context_lens[s] and KV head h = i / (num_q_heads
  * / num_kv_heads), over the n tokens found through block_tables[s]:
  *     z_t = scale * <q[s][i], K_t[h]>,  w = softmax(z),  out[s][i] = sum_t w_t V_t[h].
- * Long contexts are split into partitions processed in parallel; each keeps
- * a running max and sum (online softmax) and a merge kernel combines them by
- * log-sum-exp.
+ * The work is cut into pieces processed in parallel, each keeping a running
+ * max and sum (online softmax); a merge kernel combines the pieces of a
+ * sequence by log-sum-exp.  With a table of 64 or more blocks the (sequence,
+ * KV-head group, block) units are split evenly over the persistent CTAs;
+ * shorter tables are cut into partitions of near-equal size.
  *  q, out:     [num_seqs][num_q_heads][head_dim], dtype.
  *  k_cache, v_cache: one layer's pools, dtype.
  *  max_context_len: host upper bound on every context_lens[s] (sizes grids
@@ -266,10 +268,12 @@ int paged_attention_min_partition_blocks(int max_context_len);
 
 /* The two passes of paged_attention_decode_partitioned, enqueued separately
  * (same arguments, same workspace, same partition_blocks; call the partition
- * pass first).  The partition pass computes, per (partition, KV head), the
- * running max, running sum and unnormalised output of each query head and
- * writes sequences that fit in one partition straight to `out`; the merge
- * pass combines the partitions of the other sequences by log-sum-exp:
+ * pass first).  The partition pass computes, per piece (a partition, or with
+ * partition_blocks = 0 and a table of 64 or more blocks a CTA's share of a
+ * sequence and KV-head group), the running max, running sum and unnormalised
+ * output of each query head, and writes sequences held by one piece straight
+ * to `out`; the merge pass combines the pieces of the other sequences by
+ * log-sum-exp:
  *     M = max_p m_p,  L = sum_p l_p e^(m_p - M),  out = sum_p o_p e^(m_p - M) / L.
  * The merge pass enqueues nothing when no sequence can span two partitions. */
 pkv_status paged_attention_partition_pass(
