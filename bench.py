@@ -36,6 +36,9 @@ METRIC = "decode attn achieved HBM GB/s (% of GB300 peak) and tokens/s per layer
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
+# the long-context workload the >= 70 %-of-peak target is stated on; the
+# committed ncu summary covers its partition kernel
+DEFAULT_WORKLOAD = "llama7b_long"
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_partition_llama7b_long.md")
 KERNEL_SOURCES = ["paged_kv_cache_211_gb300/csrc/pkv_decode.cu",
                   "paged_kv_cache_211_gb300/csrc/pkv_internal.cuh",
@@ -48,7 +51,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="llama7b_long")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer loop")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill", action="store_true",
@@ -464,7 +467,8 @@ def run_ours(args):
     value = world * step_bytes / (ms / 1e3) / 1e9
     achieved = part_bytes / (t_part / 1e3) / 1e9
     cpu = None if args.no_cpu_baseline else cpu_baseline(inp, w)
-    traffic = recorded_traffic()
+    # the committed summary's DRAM bytes are those of the default workload only
+    traffic = recorded_traffic() if w.name == DEFAULT_WORKLOAD else None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5),
