@@ -82,14 +82,20 @@ struct WsLayout {
 constexpr int kMaxEvenGrid = 256;
 // Shortest table bound (in blocks) for which the TMA pass splits evenly.
 constexpr int kEvenMinBlocks = 64;
+// Most query heads one even-split slot holds (heads per item x group); the
+// workspace reserves two slots of that many rows per CTA.
+constexpr int kEvenMaxHeads = 16;
 
 WsLayout ws_layout(int num_seqs, int num_q_heads, int head_dim, int max_context_len,
                    int extra_rows_per_seq = 0) {
     const int mb = ceil_div(std::max(max_context_len, 0), PKV_BLOCK_SIZE);
     const int parts =
         std::max(1, ceil_div(mb, min_partition_blocks(max_context_len))) + extra_rows_per_seq;
-    const size_t rows = std::max((size_t)num_seqs * parts * num_q_heads,
-                                 (size_t)2 * kMaxEvenGrid * num_q_heads);
+    size_t rows = (size_t)num_seqs * parts * num_q_heads;
+    // the even split (bounds of kEvenMinBlocks blocks or more, no cascade)
+    // keeps two slots of up to kEvenMaxHeads query-head rows per CTA
+    if (extra_rows_per_seq == 0 && mb >= kEvenMinBlocks)
+        rows = std::max(rows, (size_t)2 * kMaxEvenGrid * std::min(num_q_heads, kEvenMaxHeads));
     WsLayout w;
     w.offsets = 0;
     w.m = align256((size_t)(num_seqs + 1) * 4);
@@ -1625,10 +1631,16 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp_i
     // would span CTAs and need a merge (measured 1.2x slower on 2..32-block
     // contexts).  A caller-fixed partition length or a cascade suffix keeps
     // items of whole partitions.
-    const bool even = prm.prefix_parts == 0 && prm.partition_blocks <= 0 &&
-                      max_blocks >= kEvenMinBlocks;
+    bool even = prm.prefix_parts == 0 && prm.partition_blocks <= 0 &&
+                max_blocks >= kEvenMinBlocks;
     // items cover `hpi` KV heads of one partition
-    const int hpi = tma_heads_per_item(prm.num_seqs, max_blocks, prm.num_kv_heads, D, even);
+    int hpi = tma_heads_per_item(prm.num_seqs, max_blocks, prm.num_kv_heads, D, even);
+    if (even && hpi * prm.group > kEvenMaxHeads) {
+        // more query heads per slot than the workspace keeps (only through
+        // the heads-per-item override): items instead
+        even = false;
+        hpi = tma_heads_per_item(prm.num_seqs, max_blocks, prm.num_kv_heads, D, false);
+    }
     const int groups = prm.num_kv_heads / hpi;
     int grid;
     if (even) {

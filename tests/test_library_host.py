@@ -67,8 +67,12 @@ def test_workspace_sizing():
     w1 = pkv.paged_attention_workspace_bytes(32, 32, 128, 32768)
     w2 = pkv.paged_attention_workspace_bytes(32, 32, 128, 100)   # 7 blocks -> <= 7 partitions
     assert w1 > w2 > 0 and w1 % 256 == 0
-    # the even split keeps two rows of every query head for each of up to 256 CTAs
-    assert w2 >= 2 * 256 * 32 * (128 + 2) * 4
+    # long contexts: the even split keeps two slots of up to 16 query-head rows
+    # for each of up to 256 CTAs; short ones never use it and reserve nothing
+    even_rows = 2 * 256 * 16 * (128 + 2) * 4
+    assert pkv.paged_attention_workspace_bytes(1, 32, 128, 32768) >= even_rows
+    assert pkv.paged_attention_workspace_bytes(1, 32, 128, 100) < even_rows
+    assert pkv.paged_attention_workspace_bytes(1, 4, 128, 32768) >= 2 * 256 * 4 * (128 + 2) * 4
     assert pkv.paged_attention_workspace_bytes(32, 32, 128, 1024) == w1   # 64 partitions either way
     # at most 64 partitions per sequence: 32 seqs x 64 x 32 heads x (128 + 2) floats
     assert w1 <= 32 * 64 * 32 * 130 * 4 + 4096
