@@ -366,13 +366,15 @@ pkv_status paged_kv_decode_step_cascade(const void* q, const void* k_new, const 
  * slots).  The query at position p attends to tokens 0..p of its sequence
  * (causal), query head i reading KV head i / (num_q_heads / num_kv_heads).
  * cu_q_lens: [num_seqs + 1] int32, device; max_q_len: host bound on every
- * q_len.  A sequence with q_len > context_len is flagged (PKV_DEV_BAD_LENGTH)
- * and skipped.  Supported: head_dim 64 or 128, num_q_heads / num_kv_heads
- * up to 16. */
+ * q_len; num_q_rows: the rows of q and out.  A sequence whose rows fall
+ * outside [0, num_q_rows), whose q_len exceeds max_q_len or its context_len,
+ * or whose context_len exceeds max_blocks_per_seq * 16 is flagged
+ * (PKV_DEV_BAD_LENGTH) and skipped: no row outside q and out is touched.
+ * Supported: head_dim 64 or 128, num_q_heads / num_kv_heads up to 16. */
 pkv_status paged_attention_prefill(const void* q, const void* k_cache, const void* v_cache,
                                    const int32_t* block_tables, int max_blocks_per_seq,
                                    const int32_t* context_lens, const int32_t* cu_q_lens,
-                                   int num_seqs, int max_q_len, int num_q_heads,
+                                   int num_seqs, int max_q_len, int num_q_rows, int num_q_heads,
                                    int num_kv_heads, int head_dim, int num_blocks, float scale,
                                    void* out, pkv_dtype dtype, pkv_stream_t stream);
 

@@ -86,8 +86,8 @@ _SIGS = {
                                         _f, _vp, _vp, _sz, _i, _vp], _i),
     "paged_kv_decode_step_cascade": ([_vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i,
                                       _i, _i, _f, _vp, _vp, _vp, _sz, _i, _vp], _i),
-    "paged_attention_prefill": ([_vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _f,
-                                 _vp, _i, _vp], _i),
+    "paged_attention_prefill": ([_vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
+                                 _f, _vp, _i, _vp], _i),
     "paged_kv_decode_step_staging_bytes": ([_i, _i, _i, _i, _i], _sz),
     "paged_kv_decode_step_host": ([_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp, _vp, _i, _i,
                                    _i, _i, _i, _i, _i, _f, _vp, _sz, _i, _vp], _i),
@@ -210,13 +210,29 @@ def _check_decode_shapes(q, k_cache, v_cache, block_tables, context_lens, out):
     NB, bs, Hkv, D2 = k_cache.shape
     if bs != BLOCK_SIZE or D2 != D or v_cache.shape != k_cache.shape:
         raise ValueError("pool shape must be [num_blocks, 16, num_kv_heads, head_dim]")
-    if block_tables.dtype != torch.int32 or block_tables.shape[0] != B:
+    _check_tables(block_tables, context_lens, B)
+    _check_dtypes(q, k_cache, v_cache, out)
+    return B, Hq, Hkv, D, NB
+
+
+def _check_tables(block_tables, context_lens, B):
+    if (block_tables.dtype != torch.int32 or block_tables.dim() != 2
+            or block_tables.shape[0] != B):
         raise ValueError("block_tables must be int32 [num_seqs, max_blocks_per_seq]")
     if context_lens.dtype != torch.int32 or context_lens.numel() != B:
         raise ValueError("context_lens must be int32 [num_seqs]")
-    if out.shape != q.shape or out.dtype != q.dtype or k_cache.dtype != q.dtype:
+
+
+def _check_new_rows(k_new, v_new, shape, dtype):
+    if (tuple(k_new.shape) != shape or tuple(v_new.shape) != shape or k_new.dtype != dtype
+            or v_new.dtype != dtype):
+        raise ValueError(f"k_new/v_new must be shaped {shape} in q's dtype")
+
+
+def _check_dtypes(q, k_cache, v_cache, out):
+    if (out.shape != q.shape or out.dtype != q.dtype or k_cache.dtype != q.dtype
+            or v_cache.dtype != q.dtype):
         raise ValueError("q, out and the pools must share one dtype; out shaped like q")
-    return B, Hq, Hkv, D, NB
 
 
 def paged_attention_decode(q, k_cache, v_cache, block_tables, context_lens, max_context_len,
@@ -292,8 +308,7 @@ def _decode_step(fn_name, q, k_new, v_new, k_cache, v_cache, block_tables, conte
                  max_context_len, scale, out, workspace, slot_mapping_out, stream):
     B, Hq, Hkv, D, NB = _check_decode_shapes(q, k_cache, v_cache, block_tables, context_lens,
                                              out)
-    if tuple(k_new.shape) != (B, Hkv, D) or v_new.shape != k_new.shape:
-        raise ValueError("k_new/v_new must be [num_seqs, num_kv_heads, head_dim]")
+    _check_new_rows(k_new, v_new, (B, Hkv, D), q.dtype)
     _check(fn_name, getattr(lib(), fn_name)(
         _dev(q, "q"), _dev(k_new, "k_new"), _dev(v_new, "v_new"), _dev(k_cache, "k_cache"),
         _dev(v_cache, "v_cache"), _dev(block_tables, "block_tables"), block_tables.shape[1],
@@ -351,8 +366,7 @@ def paged_kv_decode_step_cascade(q, k_new, v_new, k_cache, v_cache, block_tables
     """paged_kv_decode_step with the shared-prefix cascade."""
     B, Hq, Hkv, D, NB = _check_decode_shapes(q, k_cache, v_cache, block_tables, context_lens,
                                              out)
-    if tuple(k_new.shape) != (B, Hkv, D) or v_new.shape != k_new.shape:
-        raise ValueError("k_new/v_new must be [num_seqs, num_kv_heads, head_dim]")
+    _check_new_rows(k_new, v_new, (B, Hkv, D), q.dtype)
     _check("paged_kv_decode_step_cascade", lib().paged_kv_decode_step_cascade(
         _dev(q, "q"), _dev(k_new, "k_new"), _dev(v_new, "v_new"), _dev(k_cache, "k_cache"),
         _dev(v_cache, "v_cache"), _dev(block_tables, "block_tables"), block_tables.shape[1],
@@ -371,15 +385,15 @@ def paged_attention_prefill(q, k_cache, v_cache, block_tables, context_lens, cu_
     if bs != BLOCK_SIZE or D2 != D or v_cache.shape != k_cache.shape:
         raise ValueError("pool shape must be [num_blocks, 16, num_kv_heads, head_dim]")
     B = context_lens.numel()
+    _check_tables(block_tables, context_lens, B)
     if cu_q_lens.dtype != torch.int32 or cu_q_lens.numel() != B + 1:
         raise ValueError("cu_q_lens must be int32 [num_seqs + 1]")
-    if out.shape != q.shape or out.dtype != q.dtype or k_cache.dtype != q.dtype:
-        raise ValueError("q, out and the pools must share one dtype; out shaped like q")
+    _check_dtypes(q, k_cache, v_cache, out)
     _check("paged_attention_prefill", lib().paged_attention_prefill(
         _dev(q, "q"), _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"),
         _dev(block_tables, "block_tables"), block_tables.shape[1],
-        _dev(context_lens, "context_lens"), _dev(cu_q_lens, "cu_q_lens"), B, int(max_q_len), Hq,
-        Hkv, D, NB, float(scale), _dev(out, "out"), _dtype_code(q), _stream(stream)))
+        _dev(context_lens, "context_lens"), _dev(cu_q_lens, "cu_q_lens"), B, int(max_q_len), R,
+        Hq, Hkv, D, NB, float(scale), _dev(out, "out"), _dtype_code(q), _stream(stream)))
     return out
 
 
@@ -391,12 +405,9 @@ def paged_kv_decode_step_layers(q, k_new, v_new, k_cache, v_cache, block_tables,
     L2, NB, bs, Hkv, D2 = k_cache.shape
     if L2 != L or bs != BLOCK_SIZE or D2 != D or v_cache.shape != k_cache.shape:
         raise ValueError("pools must be [layers, num_blocks, 16, num_kv_heads, head_dim]")
-    if tuple(k_new.shape) != (L, B, Hkv, D) or v_new.shape != k_new.shape:
-        raise ValueError("k_new/v_new must be [layers, num_seqs, num_kv_heads, head_dim]")
-    if out.shape != q.shape or out.dtype != q.dtype or k_cache.dtype != q.dtype:
-        raise ValueError("q, out and the pools must share one dtype; out shaped like q")
-    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
-        raise ValueError("block tables and lengths must be int32")
+    _check_new_rows(k_new, v_new, (L, B, Hkv, D), q.dtype)
+    _check_dtypes(q, k_cache, v_cache, out)
+    _check_tables(block_tables, context_lens, B)
     _check("paged_kv_decode_step_layers", lib().paged_kv_decode_step_layers(
         _dev(q, "q"), _dev(k_new, "k_new"), _dev(v_new, "v_new"), _dev(k_cache, "k_cache"),
         _dev(v_cache, "v_cache"), _dev(block_tables, "block_tables"), block_tables.shape[1],
@@ -423,11 +434,12 @@ def paged_kv_decode_step_host(q_host, k_new_host, v_new_host, block_tables_host,
                               max_context_len, scale, workspace, stream=None):
     """paged_kv_decode_step with inputs/output in (pinned) host memory; enqueues only."""
     B, Hq, D = q_host.shape
-    NB, bs, Hkv, _ = k_cache.shape
-    if block_tables_host.dtype != torch.int32 or context_lens_host.dtype != torch.int32:
-        raise ValueError("block tables and lengths must be int32")
-    if out_host.shape != q_host.shape or out_host.dtype != q_host.dtype:
-        raise ValueError("out_host must be shaped like q_host")
+    NB, bs, Hkv, D2 = k_cache.shape
+    if bs != BLOCK_SIZE or D2 != D or v_cache.shape != k_cache.shape:
+        raise ValueError("pool shape must be [num_blocks, 16, num_kv_heads, head_dim]")
+    _check_new_rows(k_new_host, v_new_host, (B, Hkv, D), q_host.dtype)
+    _check_tables(block_tables_host, context_lens_host, B)
+    _check_dtypes(q_host, k_cache, v_cache, out_host)
     _check("paged_kv_decode_step_host", lib().paged_kv_decode_step_host(
         _host(q_host, "q_host"), _host(k_new_host, "k_new_host"),
         _host(v_new_host, "v_new_host"), _host(block_tables_host, "block_tables_host"),

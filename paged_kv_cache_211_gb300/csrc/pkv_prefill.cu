@@ -45,9 +45,19 @@ struct PrefillParams {
     const int32_t* cu_q_lens;
     unsigned int* status;
     int num_seqs, num_q_heads, num_kv_heads, group, max_blocks_per_seq, num_blocks;
+    int max_q_len, num_q_rows;  // host bounds: longest chunk, rows of q and out
     int tiles_per_seq;  // ceil(max_q_len * group / kPrefillRows)
     float scale_log2;
 };
+
+// A sequence's chunk is usable if its rows lie inside q/out, it is no longer
+// than the host bound the grid was sized for, and it fits its context and the
+// table.  qlen == 0 is a valid empty chunk (skipped without a flag).
+__device__ __forceinline__ bool prefill_lengths_ok(const PrefillParams& p, int q0, int qlen,
+                                                   int n) {
+    return qlen > 0 && q0 >= 0 && q0 <= p.num_q_rows - qlen && qlen <= p.max_q_len &&
+           n >= qlen && n <= p.max_blocks_per_seq * PKV_BLOCK_SIZE;
+}
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kPrefillThreads)
@@ -75,10 +85,8 @@ __global__ void __launch_bounds__(kPrefillThreads)
     const int g = p.group, Hq = p.num_q_heads;
     const int q0 = p.cu_q_lens[s], qlen = p.cu_q_lens[s + 1] - q0;
     const int n = p.context_lens[s];
-    if (qlen <= 0 || n < qlen || n > p.max_blocks_per_seq * PKV_BLOCK_SIZE) {
-        if (tid == 0 && tile == 0 && h == 0 && (qlen < 0 || n < qlen ||
-                                                 n > p.max_blocks_per_seq * PKV_BLOCK_SIZE))
-            atomicOr(p.status, PKV_DEV_BAD_LENGTH);
+    if (!prefill_lengths_ok(p, q0, qlen, n)) {
+        if (tid == 0 && tile == 0 && h == 0 && qlen != 0) atomicOr(p.status, PKV_DEV_BAD_LENGTH);
         return;
     }
     const int row0 = tile * kPrefillRows;      // first (token, head) row of the tile
@@ -332,10 +340,8 @@ __device__ __forceinline__ bool tc_item(const PrefillParams& p, int i, bool flag
     it.q0 = p.cu_q_lens[it.s];
     it.qlen = p.cu_q_lens[it.s + 1] - it.q0;
     it.n = p.context_lens[it.s];
-    if (it.qlen <= 0 || it.n < it.qlen || it.n > p.max_blocks_per_seq * PKV_BLOCK_SIZE) {
-        if (flag && tile == 0 && it.h == 0 &&
-            (it.qlen < 0 || it.n < it.qlen || it.n > p.max_blocks_per_seq * PKV_BLOCK_SIZE))
-            atomicOr(p.status, PKV_DEV_BAD_LENGTH);
+    if (!prefill_lengths_ok(p, it.q0, it.qlen, it.n)) {
+        if (flag && tile == 0 && it.h == 0 && it.qlen != 0) atomicOr(p.status, PKV_DEV_BAD_LENGTH);
         return false;
     }
     const int g = p.group;
@@ -835,10 +841,10 @@ extern "C" {
 pkv_status paged_attention_prefill(const void* q, const void* k_cache, const void* v_cache,
                                    const int32_t* block_tables, int max_blocks_per_seq,
                                    const int32_t* context_lens, const int32_t* cu_q_lens,
-                                   int num_seqs, int max_q_len, int num_q_heads,
+                                   int num_seqs, int max_q_len, int num_q_rows, int num_q_heads,
                                    int num_kv_heads, int head_dim, int num_blocks, float scale,
                                    void* out, pkv_dtype dtype, pkv_stream_t stream) {
-    if (num_seqs < 0 || max_q_len < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+    if (num_seqs < 0 || max_q_len < 0 || num_q_rows < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
         head_dim <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0)
         return PKV_ERR_INVALID_ARG;
     if (num_q_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
@@ -867,6 +873,8 @@ pkv_status paged_attention_prefill(const void* q, const void* k_cache, const voi
     prm.group = g;
     prm.max_blocks_per_seq = max_blocks_per_seq;
     prm.num_blocks = num_blocks;
+    prm.max_q_len = max_q_len;
+    prm.num_q_rows = num_q_rows;
     prm.tiles_per_seq = 0;  // set by the launcher for the kernel it picks
     prm.scale_log2 = scale * pkv::kLog2e;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -103,6 +103,33 @@ def test_prefill_flags_a_chunk_longer_than_its_context(cuda_device):
     assert torch.count_nonzero(out[8:]) == 0       # the bad sequence was skipped
 
 
+def test_prefill_flags_rows_outside_q_and_chunks_over_the_bound(cuda_device):
+    """cu_q_lens is read on the device: rows past q's end, a negative start or
+    a chunk longer than max_q_len are flagged and that sequence is skipped,
+    while the valid one is still served."""
+    c = _case(cuda_device, "bf16", [(40, 8), (30, 30)], 8, 2, 128, seed=5)
+    good, _, _, bt, cl = _run(c, 128, cuda_device)
+    cases = [
+        ([0, 8, 54], [40, 46], c["maxq"]),          # 46 rows from row 8: past q's 38 rows
+        ([0, 8, 38], [40, 30], 8),                  # 30 rows over a bound of 8
+        ([-4, 8, 38], [40, 30], c["maxq"]),         # a negative first row
+    ]
+    for cu, lens, maxq in cases:
+        out = torch.zeros_like(c["q"])
+        pkv.paged_attention_prefill(c["q"], c["kc"], c["vc"], bt,
+                                    torch.tensor(lens, dtype=torch.int32, device=cuda_device),
+                                    torch.tensor(cu, dtype=torch.int32, device=cuda_device),
+                                    maxq, 128 ** -0.5, out)
+        torch.cuda.synchronize()
+        assert pkv.pkv_device_status(reset=True) & pkv.DEV_BAD_LENGTH, cu
+        if cu[0] == 0:
+            assert np.array_equal(bits(out[:8]), bits(good[:8])), cu   # the valid sequence
+            assert torch.count_nonzero(out[8:]) == 0, cu
+        else:
+            assert torch.count_nonzero(out[:8]) == 0, cu
+            assert np.array_equal(bits(out[8:]), bits(good[8:])), cu
+
+
 def test_prefill_long_chunk_over_a_cached_prefix(cuda_device):
     """Many 128-row tiles and key tiles: a 400-token chunk after 1600 cached
     tokens, beside a whole 1200-token prompt."""
