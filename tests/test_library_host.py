@@ -48,6 +48,28 @@ def test_every_declared_symbol_is_exported(L):
         assert hasattr(L, n)
 
 
+def declared_arity():
+    """Parameter count of every function the header declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    out = {}
+    for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b([a-z_][a-z0-9_]*)\s*\(([^)]*)\)\s*;",
+                         text, flags=re.M):
+        args = m.group(2).strip()
+        out[m.group(1)] = 0 if args in ("", "void") else args.count(",") + 1
+    return out
+
+
+def test_binding_signatures_match_the_header():
+    """Every ctypes signature the binding installs has the header's parameter count."""
+    arity = declared_arity()
+    assert set(arity) == set(declared_functions())
+    for name, (argtypes, _) in pkv._SIGS.items():
+        assert name in arity, f"{name} is bound but not declared"
+        assert len(argtypes) == arity[name], (name, len(argtypes), arity[name])
+
+
 def test_version_and_status_strings(L):
     assert pkv.pkv_version() >= 100
     assert L.pkv_status_string(0) == b"ok"
@@ -157,6 +179,9 @@ def test_host_validation_before_any_cuda_call(L):
     assert L.reshape_and_cache(None, None, None, None, None, 0, 10, 8, 128, 0, None) == 0
     assert L.paged_attention_decode(None, None, None, None, 4, None, 64, 0, 16, 8, 128, 10, 0.1,
                                     None, None, 0, 0, None) == 0
+    # prefill: negative row count of q
+    assert L.paged_attention_prefill(p, p, p, p, 4, p, p, 2, 8, -1, 16, 8, 128, 10, 0.1, p, 0,
+                                     None) == 1
     # host-buffer step: staging too small
     assert L.paged_kv_decode_step_host(p, p, p, p, p, p, p, 64, p, p, 4, 64, 2, 16, 8, 128, 10,
                                        0.1, p, 1 << 20, 0, None) == 6
