@@ -148,6 +148,12 @@ def _opt(t: Optional[torch.Tensor], name: str):
     return None if t is None else _dev(t, name)
 
 
+def _check_slots(t: Optional[torch.Tensor], n: int, name: str):
+    """An optional int64 [n] slot output (the kernels write n 8-byte slots)."""
+    if t is not None and (t.dtype != torch.int64 or t.numel() != n):
+        raise ValueError(f"{name} must be int64 [{n}]")
+
+
 def _stream(stream) -> ctypes.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -168,6 +174,8 @@ def paged_kv_slot_mapping(block_tables, context_lens, num_blocks, slot_mapping=N
                           stream=None) -> torch.Tensor:
     """Slot of each sequence's token at position len-1 (int64, -1 for empty rows)."""
     B, MB = block_tables.shape
+    _check_tables(block_tables, context_lens, B)
+    _check_slots(slot_mapping, B, "slot_mapping")
     if slot_mapping is None:
         slot_mapping = torch.empty(B, dtype=torch.int64, device=block_tables.device)
     _check("paged_kv_slot_mapping", lib().paged_kv_slot_mapping(
@@ -182,6 +190,9 @@ def reshape_and_cache(k_new, v_new, k_cache, v_cache, slot_mapping, stream=None)
     NB = k_cache.shape[0]
     if tuple(k_cache.shape[1:]) != (BLOCK_SIZE, Hkv, D) or v_cache.shape != k_cache.shape:
         raise ValueError("pool shape must be [num_blocks, 16, num_kv_heads, head_dim]")
+    _check_new_rows(k_new, v_new, (T, Hkv, D), k_new.dtype)
+    if k_cache.dtype != k_new.dtype or v_cache.dtype != k_new.dtype:
+        raise ValueError("the pools must have k_new's dtype")
     if slot_mapping.dtype != torch.int64 or slot_mapping.numel() != T:
         raise ValueError("slot_mapping must be int64 [num_tokens]")
     _check("reshape_and_cache", lib().reshape_and_cache(
@@ -297,6 +308,11 @@ def paged_kv_write_new_tokens(k_new, v_new, k_cache, v_cache, block_tables, cont
     NB = k_cache.shape[0]
     if tuple(k_cache.shape[1:]) != (BLOCK_SIZE, Hkv, D) or v_cache.shape != k_cache.shape:
         raise ValueError("pool shape must be [num_blocks, 16, num_kv_heads, head_dim]")
+    _check_new_rows(k_new, v_new, (B, Hkv, D), k_new.dtype)
+    if k_cache.dtype != k_new.dtype or v_cache.dtype != k_new.dtype:
+        raise ValueError("the pools must have k_new's dtype")
+    _check_tables(block_tables, context_lens, B)
+    _check_slots(slot_mapping_out, B, "slot_mapping_out")
     _check("paged_kv_write_new_tokens", lib().paged_kv_write_new_tokens(
         _dev(k_new, "k_new"), _dev(v_new, "v_new"), _dev(k_cache, "k_cache"),
         _dev(v_cache, "v_cache"), _dev(block_tables, "block_tables"), block_tables.shape[1],
@@ -309,6 +325,7 @@ def _decode_step(fn_name, q, k_new, v_new, k_cache, v_cache, block_tables, conte
     B, Hq, Hkv, D, NB = _check_decode_shapes(q, k_cache, v_cache, block_tables, context_lens,
                                              out)
     _check_new_rows(k_new, v_new, (B, Hkv, D), q.dtype)
+    _check_slots(slot_mapping_out, B, "slot_mapping_out")
     _check(fn_name, getattr(lib(), fn_name)(
         _dev(q, "q"), _dev(k_new, "k_new"), _dev(v_new, "v_new"), _dev(k_cache, "k_cache"),
         _dev(v_cache, "v_cache"), _dev(block_tables, "block_tables"), block_tables.shape[1],
@@ -367,6 +384,7 @@ def paged_kv_decode_step_cascade(q, k_new, v_new, k_cache, v_cache, block_tables
     B, Hq, Hkv, D, NB = _check_decode_shapes(q, k_cache, v_cache, block_tables, context_lens,
                                              out)
     _check_new_rows(k_new, v_new, (B, Hkv, D), q.dtype)
+    _check_slots(slot_mapping_out, B, "slot_mapping_out")
     _check("paged_kv_decode_step_cascade", lib().paged_kv_decode_step_cascade(
         _dev(q, "q"), _dev(k_new, "k_new"), _dev(v_new, "v_new"), _dev(k_cache, "k_cache"),
         _dev(v_cache, "v_cache"), _dev(block_tables, "block_tables"), block_tables.shape[1],
@@ -481,7 +499,8 @@ def paged_kv_copy_blocks(k_cache, v_cache, src_block_ids, dst_block_ids, stream=
     NB, bs, Hkv, D = k_cache.shape
     if v_cache.shape != k_cache.shape or bs != BLOCK_SIZE:
         raise ValueError("pool shape must be [num_blocks, 16, num_kv_heads, head_dim]")
-    if src_block_ids.dtype != torch.int32 or dst_block_ids.shape != src_block_ids.shape:
+    if (src_block_ids.dtype != torch.int32 or dst_block_ids.dtype != torch.int32
+            or dst_block_ids.shape != src_block_ids.shape):
         raise ValueError("block id lists must be int32 and of equal length")
     _check("paged_kv_copy_blocks", lib().paged_kv_copy_blocks(
         _dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), _dev(src_block_ids, "src"),
