@@ -519,12 +519,17 @@ def run_prefill(args):
         step()
     torch.cuda.synchronize()
     K = max(1, min(args.steps, 200))
+    # bytes one step touches: q read, out written, the chunks' K/V read
+    touched = 2 * q.numel() * q.element_size() + \
+        2 * int(lens.sum()) * w.num_kv_heads * w.head_dim * q.element_size()
+    clocks = ClockSampler(dev.index)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(K):
         step()
     e1.record()
     torch.cuda.synchronize()
+    clk = clocks.stop()
     if pkv.pkv_device_status() != 0:
         raise SystemExit("device status flags set during the benchmark")
     ms = e0.elapsed_time(e1) / K
@@ -537,9 +542,12 @@ def run_prefill(args):
     print(json.dumps({
         "metric": "chunked-prefill attention TFLOP/s (causal, paged cache)", "value": round(tf, 2),
         "unit": "TFLOP/s", "n_gpus": 1, "steps": K, "warmup": args.warmup,
-        "ms_per_step": round(ms, 4), "higher_is_better": True, "dtype": w.dtype,
-        "data": "synthetic", "config": {"workload": w.name, "description": w.description,
-                                        "query_rows": int(qlens.sum()), "flops": flops},
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "description": w.description,
+                   "query_rows": int(qlens.sum()), "flops": flops,
+                   "l2": "inputs larger than L2: %.2f GB touched per step vs 129 MB L2, no "
+                         "flush (compute-bound)" % (touched / 1e9)},
         "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(tf / peak, 4) if peak else None,
                      "kernel": ("prefill_tma_kernel (mma.sync m16n8k16)"
@@ -547,7 +555,7 @@ def run_prefill(args):
                                 "prefill_tc_kernel (tcgen05.mma kind::f16)"),
                      "note": "causal FLOPs (4 * visible pairs * D * query heads) against the "
                              "measured cuBLAS bf16 burst peak"},
-        "gpu_launches": K}), flush=True)
+        "gpu_launches": K, "clocks": clk}), flush=True)
 
 
 def run_reference(args):
