@@ -112,6 +112,29 @@ def pin_reshape_and_cache_scatter(o):
     assert np.array_equal(gv, wv.reshape(v.shape)), "V pool differs"
 
 
+def pin_copy_blocks_whole_blocks(o):
+    """Copy-on-write's device half: after the copy each destination block holds
+    its source block's bytes in both pools, every other block is unchanged,
+    and an id outside the pool is refused."""
+    rng = np.random.default_rng(13)
+    NB, Hkv, D = 11, 2, 8
+    k = rng.integers(0, 1 << 16, size=(NB, BS, Hkv, D)).astype(np.uint16)
+    v = rng.integers(0, 1 << 16, size=(NB, BS, Hkv, D)).astype(np.uint16)
+    ids = rng.permutation(NB)
+    src, dst = ids[:3].astype(np.int32), ids[3:6].astype(np.int32)   # disjoint lists
+    gk, gv = o.copy_blocks(k, v, src, dst)
+    wk, wv = k.copy(), v.copy()
+    wk[dst], wv[dst] = k[src], v[src]
+    assert np.array_equal(gk, wk), "K pool differs"
+    assert np.array_equal(gv, wv), "V pool differs"
+    try:
+        o.copy_blocks(k, v, np.array([NB], np.int32), np.array([0], np.int32))
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("an id past the pool was accepted")
+
+
 # --- decode attention: library pin, brute force, closed forms ----------------
 
 def pin_attention_vs_sdpa(o):
@@ -283,6 +306,7 @@ ALL_PINS = [
     pin_decoders_exhaustive,
     pin_slot_mapping_enumeration,
     pin_reshape_and_cache_scatter,
+    pin_copy_blocks_whole_blocks,
     pin_attention_vs_sdpa,
     pin_attention_brute_force,
     pin_closed_forms,

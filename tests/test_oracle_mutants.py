@@ -46,6 +46,10 @@ MUTANTS = {
     "slot_position_len": ("int p = n - 1;", "int p = n;"),
     "write_padding_not_skipped": ("if (slot < 0) continue;", "if (slot < 0) slot = 0;"),
     "write_v_into_k": ("memcpy(v_cache + dst, v_new", "memcpy(k_cache + dst, v_new"),
+    "copy_v_not_copied": ("memcpy(v_cache + dst[i] * blk, v_cache + src[i] * blk",
+                          "memcpy(v_cache + src[i] * blk, v_cache + src[i] * blk"),
+    "copy_half_block": ("memcpy(k_cache + dst[i] * blk, k_cache + src[i] * blk, (size_t)blk * 2);",
+                        "memcpy(k_cache + dst[i] * blk, k_cache + src[i] * blk, (size_t)blk);"),
     "prefill_not_causal": ("int p = n - rows + r;", "int p = n - 1;"),
     "prefill_position_off_by_one": ("int p = n - rows + r;", "int p = n - rows + r - 1 + (r == 0);"),
 }
