@@ -19,6 +19,55 @@ def _run(fn):
         return ("err", e.code)
 
 
+class _ModelAllocator:
+    """The policy model behind the library allocator's Python API, so that the
+    scripted scenarios below (expectations worked out by hand) pin the model
+    as well as the library."""
+
+    def __init__(self, num_blocks):
+        self.m = PrefixCacheModel(num_blocks)
+
+    def _call(self, fn, *args):
+        try:
+            return fn(*args)
+        except ModelError as e:
+            raise pkv.PagedKVError("model", e.code) from None
+
+    def alloc(self, n):
+        return self._call(self.m.alloc, n)
+
+    def share(self, ids):
+        return self._call(self.m.share, list(ids))
+
+    def free(self, ids):
+        return self._call(self.m.free_ids, list(ids))
+
+    def num_free(self):
+        return self.m.num_free()
+
+    def refcount(self, b):
+        return self.m.refs[b] if 0 <= b < self.m.n else -1
+
+    def num_cached(self):
+        return len(self.m.hash_of)
+
+    def prefix_insert(self, b, h):
+        return self._call(self.m.insert, b, h)
+
+    def prefix_lookup(self, hashes):
+        return self._call(self.m.lookup, list(hashes))
+
+    def cow(self, b):
+        return self._call(self.m.cow, b)
+
+    def rollback(self, table, new_len):
+        return self._call(self.m.rollback, list(table), new_len)
+
+
+ALLOCATORS = pytest.mark.parametrize("make", [pkv.BlockAllocator, _ModelAllocator],
+                                     ids=["library", "oracle_model"])
+
+
 def test_differential_random_ops():
     rng = random.Random(2111)
     NB = 40
@@ -103,8 +152,9 @@ def _chain(tokens):
     return hs
 
 
-def test_prefix_reuse_release_and_eviction():
-    a = pkv.BlockAllocator(8)
+@ALLOCATORS
+def test_prefix_reuse_release_and_eviction(make):
+    a = make(8)
     prompt = list(range(48))                     # 3 full blocks
     hs = _chain(prompt)
     A = a.alloc(3)
@@ -127,8 +177,9 @@ def test_prefix_reuse_release_and_eviction():
     assert a.num_cached() == 2 and a.prefix_lookup(hs[:1]) == []
 
 
-def test_copy_on_write_and_rollback():
-    a = pkv.BlockAllocator(8)
+@ALLOCATORS
+def test_copy_on_write_and_rollback(make):
+    a = make(8)
     x = a.alloc(2)
     a.prefix_insert(x[1], 777)
     a.share(x)                                   # a second sequence forks
