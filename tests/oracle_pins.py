@@ -381,4 +381,33 @@ def pin_prefill_last_row_is_decode(o):
     assert np.array_equal(a, b)
 
 
-ALL_PINS += [pin_prefill_vs_sdpa_causal, pin_prefill_last_row_is_decode]
+def pin_prefill_large_scores(o):
+    """Scores near 1e3 overflow exp in fp64 unless the row maximum is taken out
+    first; the result must still match SDPA (which is overflow-safe)."""
+    import torch.nn.functional as F
+    rng = np.random.default_rng(67)
+    n, ql, D = 20, 6, 4
+    q = _f16(np.full((ql, 1, D), 4.0))
+    kv = rng.choice([-4.0, 4.0], size=(2, BS, 1, D))
+    kv[1, 0] = 4.0                                 # token 0: q . k = 64, the row maximum
+    k = _f16(kv)
+    v = _f16(rng.standard_normal((2, BS, 1, D)))
+    tables = np.array([[1, 0]], np.int32)
+    cu = np.array([0, ql], np.int32)
+    scale = 20.0                                   # |score| up to 20 * 64 = 1280
+    got = o.prefill_attention(F16, q, k, v, tables, np.array([n], np.int32), cu, scale)
+    kf, vf = k.reshape(-1, 1, D), v.reshape(-1, 1, D)
+    from pkv_testutil import token_slots
+    sl = np.array(token_slots(tables[0], n))
+    K = torch.from_numpy(lib_decode(kf[sl], F16)).permute(1, 0, 2)
+    V = torch.from_numpy(lib_decode(vf[sl], F16)).permute(1, 0, 2)
+    Q = torch.from_numpy(lib_decode(q, F16)).permute(1, 0, 2)
+    mask = torch.arange(n).unsqueeze(0) <= torch.arange(n - ql, n).unsqueeze(1)
+    want = F.scaled_dot_product_attention(Q, K, V, attn_mask=mask, scale=scale)
+    want = want.permute(1, 0, 2).numpy()
+    assert np.isfinite(got).all(), "non-finite output"
+    assert np.allclose(got, want, rtol=1e-11, atol=1e-12)
+
+
+ALL_PINS += [pin_prefill_vs_sdpa_causal, pin_prefill_last_row_is_decode,
+             pin_prefill_large_scores]

@@ -50,6 +50,14 @@ MUTANTS = {
                           "memcpy(v_cache + src[i] * blk, v_cache + src[i] * blk"),
     "copy_half_block": ("memcpy(k_cache + dst[i] * blk, k_cache + src[i] * blk, (size_t)blk * 2);",
                         "memcpy(k_cache + dst[i] * blk, k_cache + src[i] * blk, (size_t)blk);"),
+    "prefill_rows_not_packed": ("int64_t qrow = (int64_t)cu_q_lens[s] + r;",
+                                "int64_t qrow = (int64_t)s + r;"),
+    "prefill_gqa_head_modulo": (
+        "int h = i / group;\n                for (int d = 0; d < head_dim; ++d) { qd[d] = decode(dtype, qi[d]); o[d] = 0.0; }",
+        "int h = i % num_kv_heads;\n                for (int d = 0; d < head_dim; ++d) { qd[d] = decode(dtype, qi[d]); o[d] = 0.0; }"),
+    "prefill_max_not_subtracted": (
+        "for (int t = 0; t <= p; ++t) { z[t] = exp(z[t] - zmax); denom += z[t]; }",
+        "for (int t = 0; t <= p; ++t) { z[t] = exp(z[t]); denom += z[t]; }"),
     "prefill_not_causal": ("int p = n - rows + r;", "int p = n - 1;"),
     "prefill_position_off_by_one": ("int p = n - rows + r;", "int p = n - rows + r - 1 + (r == 0);"),
 }
