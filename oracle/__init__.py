@@ -26,7 +26,9 @@ Functions and the passages they follow (page title, section):
   rollback) in plain Python.
 
 Every function is pinned by ``tests/test_oracle_pins.py`` against something
-other than itself (library routines, brute force, closed forms, invariants).
+other than itself (library routines, brute force, closed forms, invariants);
+the policy model by the hand-worked allocator scenarios of
+``tests/test_prefix_cache.py``.
 """
 from __future__ import annotations
 
