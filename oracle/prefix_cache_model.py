@@ -74,12 +74,16 @@ class PrefixCacheModel:
         for b in ids:
             self.refs[b] += 1
 
-    def free_ids(self, ids):
+    def _check_droppable(self, ids):
+        """Every id live and named at most as often as it is referenced."""
         if not all(self._live(b) for b in ids):
             raise ModelError(4)
         for b in set(ids):
             if ids.count(b) > self.refs[b]:
                 raise ModelError(4)
+
+    def free_ids(self, ids):
+        self._check_droppable(ids)
         for b in ids:
             self._drop(b)
 
@@ -123,8 +127,7 @@ class PrefixCacheModel:
         keep = -(-new_len // BLOCK)
         if keep > len(table):
             raise ModelError(1)
-        if not all(self._live(b) for b in table[keep:]):
-            raise ModelError(4)
+        self._check_droppable(list(table[keep:]))
         for b in table[keep:]:
             self._drop(b)
         if keep and new_len % BLOCK and self.refs[table[keep - 1]] == 1:

@@ -87,6 +87,16 @@ bool all_live(const pkv_allocator* a, int n, const int32_t* ids) {
     return true;
 }
 
+// Every id live, and none named more often than it is referenced: dropping
+// one reference per entry then leaves every count >= 0.
+bool droppable(const pkv_allocator* a, int n, const int32_t* ids) {
+    if (!all_live(a, n, ids)) return false;
+    std::unordered_map<int32_t, int> seen;
+    for (int i = 0; i < n; ++i)
+        if (++seen[ids[i]] > a->refs[(size_t)ids[i]]) return false;
+    return true;
+}
+
 // splitmix64 finaliser (Steele, Lea and Flood, "Fast splittable pseudorandom
 // number generators", 2014): a bijective 64-bit mixer.
 uint64_t mix64(uint64_t z) {
@@ -139,12 +149,9 @@ pkv_status paged_kv_share(pkv_allocator* a, int n, const int32_t* block_ids) {
 
 pkv_status paged_kv_free(pkv_allocator* a, int n, const int32_t* block_ids) {
     if (!a || n < 0 || (n > 0 && !block_ids)) return PKV_ERR_INVALID_ARG;
-    if (!all_live(a, n, block_ids)) return PKV_ERR_BAD_BLOCK_ID;
     // a list that names one block more often than it is referenced would drive
     // its count below zero: refuse it as a whole
-    std::unordered_map<int32_t, int> seen;
-    for (int i = 0; i < n; ++i)
-        if (++seen[block_ids[i]] > a->refs[(size_t)block_ids[i]]) return PKV_ERR_BAD_BLOCK_ID;
+    if (!droppable(a, n, block_ids)) return PKV_ERR_BAD_BLOCK_ID;
     for (int i = 0; i < n; ++i) drop_one(a, block_ids[i]);
     return PKV_OK;
 }
@@ -219,9 +226,10 @@ pkv_status paged_kv_rollback(pkv_allocator* a, int32_t* block_table, int num_tab
     if (!a || !new_num_blocks || num_table_blocks < 0 || new_len < 0 ||
         (num_table_blocks > 0 && !block_table))
         return PKV_ERR_INVALID_ARG;
-    const int keep = (new_len + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
+    // blocks that hold new_len tokens (no overflow near INT_MAX)
+    const int keep = new_len / PKV_BLOCK_SIZE + (new_len % PKV_BLOCK_SIZE != 0 ? 1 : 0);
     if (keep > num_table_blocks) return PKV_ERR_INVALID_ARG;
-    if (!all_live(a, num_table_blocks - keep, block_table + keep)) return PKV_ERR_BAD_BLOCK_ID;
+    if (!droppable(a, num_table_blocks - keep, block_table + keep)) return PKV_ERR_BAD_BLOCK_ID;
     for (int i = keep; i < num_table_blocks; ++i) {
         drop_one(a, block_table[i]);
         block_table[i] = -1;

@@ -178,6 +178,22 @@ def test_prefix_reuse_release_and_eviction(make):
 
 
 @ALLOCATORS
+def test_rollback_refuses_a_bad_tail_whole(make):
+    """A tail naming a block more often than it is referenced, or a length past
+    the table (up to the largest int), is refused and nothing changes."""
+    a = make(6)
+    t = a.alloc(2)
+    with pytest.raises(pkv.PagedKVError) as e:
+        a.rollback(t + [t[1]], 16)                   # t[1] twice in the tail, held once
+    assert e.value.status == 4
+    assert [a.refcount(b) for b in t] == [1, 1] and a.num_free() == 4
+    with pytest.raises(pkv.PagedKVError) as e:
+        a.rollback(t, 2 ** 31 - 1)
+    assert e.value.status == 1
+    assert a.rollback(t, 16) == t[:1] and a.num_free() == 5
+
+
+@ALLOCATORS
 def test_copy_on_write_and_rollback(make):
     a = make(8)
     x = a.alloc(2)
