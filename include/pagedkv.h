@@ -116,7 +116,8 @@ pkv_status paged_kv_alloc(pkv_allocator* a, int n, int32_t* out_block_ids);
 pkv_status paged_kv_share(pkv_allocator* a, int n, const int32_t* block_ids);
 
 /* Drops one reference from each listed block; a block whose count reaches 0
- * returns to the free list.  All or nothing, as for paged_kv_share. */
+ * returns to the free list.  All or nothing: PKV_ERR_BAD_BLOCK_ID if any id
+ * is out of range or free, or is listed more often than it is referenced. */
 pkv_status paged_kv_free(pkv_allocator* a, int n, const int32_t* block_ids);
 
 int paged_kv_num_free(const pkv_allocator* a);
@@ -173,7 +174,10 @@ pkv_status paged_kv_cow(pkv_allocator* a, int32_t block_id, int32_t* out_block_i
  * num_table_blocks) (host table; those entries become -1) and returns the
  * kept block count.  A kept last block that becomes partial leaves the
  * prefix cache when the caller holds its only reference; if it is shared the
- * caller must copy-on-write before writing into it. */
+ * caller must copy-on-write before writing into it.  All or nothing:
+ * PKV_ERR_INVALID_ARG if new_len needs more blocks than the table has,
+ * PKV_ERR_BAD_BLOCK_ID if a dropped entry is out of range, free, or listed
+ * more often than it is referenced. */
 pkv_status paged_kv_rollback(pkv_allocator* a, int32_t* block_table, int num_table_blocks,
                              int new_len, int* new_num_blocks);
 
