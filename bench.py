@@ -212,7 +212,8 @@ def sample_bytes(w, lens, kv_heads, q_heads=None):
 
 def cpu_baseline(inp, w, budget_s=10.0, max_seqs=None):
     """The oracle as it stands, one thread, on whole sequences until ~budget_s
-    (or the whole batch, whichever comes first)."""
+    (or the whole batch, whichever comes first).  Returns the result and the
+    sequences it covered."""
     lens = inp["context_lens_host"]
     order = np.random.default_rng(w.seed + 99).permutation(len(lens))
     done, t_total, nbytes = [], 0.0, 0
@@ -230,7 +231,57 @@ def cpu_baseline(inp, w, budget_s=10.0, max_seqs=None):
             "kind": "oracle",
             "sample": f"{len(done)} of {len(lens)} sequences ({toks} context tokens, all "
                       f"{w.num_q_heads} query heads), write + attention, fp64, 1 thread, "
-                      f"{t_total:.1f} s"}
+                      f"{t_total:.1f} s"}, done
+
+
+def _oracle_cores_worker(hs, w, start, results):
+    """One process of the all-cores baseline: loads the oracle, waits until
+    every process is ready, then runs the oracle over its share."""
+    import oracle
+    oracle.default()
+    start.wait(timeout=300)
+    t0 = time.perf_counter()
+    for h in hs:
+        oracle_step(h, w)
+    results.put(time.perf_counter() - t0)
+
+
+def cpu_baseline_all_cores(inp, w, seq_ids, timeout_s=300.0):
+    """The same oracle, unchanged, on every host core: one spawned process per
+    core, each given whole sequences (longest first, to the least-loaded
+    process).  All start together; the time runs from that common start to
+    the last process's end, so load imbalance counts against it."""
+    import multiprocessing as mp
+    lens = inp["context_lens_host"]
+    seq_ids = [int(s) for s in seq_ids]
+    n = max(1, min(os.cpu_count() or 1, len(seq_ids)))
+    shares, load = [[] for _ in range(n)], [0] * n
+    for s in sorted(seq_ids, key=lambda s: -int(lens[s])):
+        i = load.index(min(load))
+        shares[i].append(compact_host(inp, [s]))
+        load[i] += int(lens[s])
+    ctx = mp.get_context("spawn")
+    start, results = ctx.Barrier(n + 1), ctx.Queue()
+    procs = [ctx.Process(target=_oracle_cores_worker, args=(shares[i], w, start, results),
+                         daemon=True) for i in range(n)]
+    for p in procs:
+        p.start()
+    try:
+        start.wait(timeout=timeout_s)
+        t0 = time.perf_counter()
+        busy = [results.get(timeout=timeout_s) for _ in range(n)]
+        wall = time.perf_counter() - t0
+    finally:
+        for p in procs:
+            p.join(timeout=10)
+            if p.is_alive():
+                p.terminate()
+    nbytes = sample_bytes(w, lens[seq_ids], w.num_kv_heads)
+    return {"value": round(nbytes / wall / 1e9, 4), "unit": "GB/s", "cores": n,
+            "kind": "oracle",
+            "sample": f"the same {len(seq_ids)} sequences as cpu_baseline, {n} processes "
+                      f"(whole sequences each), {wall:.2f} s wall, busiest process "
+                      f"{max(busy):.2f} s"}
 
 
 # ----------------------------------------------------------------------------- arms
@@ -466,7 +517,13 @@ def run_ours(args):
     peak, peak_kind = measured_peaks()
     value = world * step_bytes / (ms / 1e3) / 1e9
     achieved = part_bytes / (t_part / 1e3) / 1e9
-    cpu = None if args.no_cpu_baseline else cpu_baseline(inp, w)
+    cpu, cpu_all = None, None
+    if not args.no_cpu_baseline:
+        cpu, seqs = cpu_baseline(inp, w)
+        try:
+            cpu_all = cpu_baseline_all_cores(inp, w, seqs)
+        except Exception as e:  # the one-thread baseline stands on its own
+            cpu_all = {"unavailable": f"{type(e).__name__}: {e}"[:200]}
     # the committed summary's DRAM bytes are those of the default workload only
     traffic = recorded_traffic() if w.name == DEFAULT_WORKLOAD else None
     line = {
@@ -488,6 +545,7 @@ def run_ours(args):
                      "bytes_per_launch": int(part_bytes),
                      "traffic": traffic},
         "cpu_baseline": cpu,
+        "cpu_baseline_all_cores": cpu_all,
         "e2e": e2e,
         "gpu_launches": K * L * (1 + merges),
         "eager_ms_per_step": None if eager_ms is None else round(eager_ms, 5),

@@ -1,0 +1,21 @@
+"""The benchmark's CPU legs without a GPU: the one-thread oracle baseline and
+the all-cores one (spawned processes) run on the small workload's inputs built
+on the CPU, and report what the JSON line needs."""
+import os
+
+import torch
+
+from paged_kv_cache_211_gb300 import workloads as wl
+
+
+def test_cpu_baselines_one_thread_and_all_cores():
+    import bench
+    w = wl.WORKLOADS["tiny"]
+    inp = wl.make_inputs(w, device=torch.device("cpu"), num_layers=1)
+    one, seqs = bench.cpu_baseline(inp, w, budget_s=5.0)
+    assert one["cores"] == 1 and one["kind"] == "oracle" and one["value"] > 0
+    assert sorted(seqs) == list(range(w.num_seqs))          # the whole small batch
+    every = bench.cpu_baseline_all_cores(inp, w, seqs, timeout_s=120.0)
+    assert every["cores"] == min(os.cpu_count() or 1, len(seqs))
+    assert every["kind"] == "oracle" and every["unit"] == "GB/s" and every["value"] > 0
+    assert f"the same {len(seqs)} sequences" in every["sample"]
