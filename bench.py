@@ -234,19 +234,38 @@ def cpu_baseline(inp, w, budget_s=10.0, max_seqs=None):
                       f"{t_total:.1f} s"}, done
 
 
-def _oracle_cores_worker(hs, w, start, results):
-    """One process of the all-cores baseline: loads the oracle, waits until
-    every process is ready, then runs the oracle over its share."""
+def _oracle_cores_worker(hs, w, ready, go, results):
+    """One process of the all-cores baseline: loads the oracle, reports ready,
+    waits for the common start, then runs the oracle over its share."""
     import oracle
     oracle.default()
-    start.wait(timeout=300)
+    ready.put(os.getpid())
+    if not go.wait(timeout=600):
+        return
     t0 = time.perf_counter()
     for h in hs:
         oracle_step(h, w)
     results.put(time.perf_counter() - t0)
 
 
-def cpu_baseline_all_cores(inp, w, seq_ids, timeout_s=300.0):
+def _collect(q, procs, k, timeout_s):
+    """k items from q, giving up at once if a process died with an error, or
+    after timeout_s."""
+    import queue
+    got, deadline = [], time.perf_counter() + timeout_s
+    while len(got) < k:
+        try:
+            got.append(q.get(timeout=1.0))
+        except queue.Empty:
+            dead = [p.exitcode for p in procs if p.exitcode not in (None, 0)]
+            if dead:
+                raise RuntimeError(f"an oracle process exited with code {dead[0]}")
+            if time.perf_counter() > deadline:
+                raise TimeoutError(f"{len(got)} of {k} oracle processes answered")
+    return got
+
+
+def cpu_baseline_all_cores(inp, w, seq_ids, timeout_s=180.0):
     """The same oracle, unchanged, on every host core: one spawned process per
     core, each given whole sequences (longest first, to the least-loaded
     process).  All start together; the time runs from that common start to
@@ -261,17 +280,20 @@ def cpu_baseline_all_cores(inp, w, seq_ids, timeout_s=300.0):
         shares[i].append(compact_host(inp, [s]))
         load[i] += int(lens[s])
     ctx = mp.get_context("spawn")
-    start, results = ctx.Barrier(n + 1), ctx.Queue()
-    procs = [ctx.Process(target=_oracle_cores_worker, args=(shares[i], w, start, results),
-                         daemon=True) for i in range(n)]
+    ready, results, go = ctx.Queue(), ctx.Queue(), ctx.Event()
+    procs = [ctx.Process(target=_oracle_cores_worker,
+                         args=(shares[i], w, ready, go, results), daemon=True)
+             for i in range(n)]
     for p in procs:
         p.start()
     try:
-        start.wait(timeout=timeout_s)
+        _collect(ready, procs, n, timeout_s)
         t0 = time.perf_counter()
-        busy = [results.get(timeout=timeout_s) for _ in range(n)]
+        go.set()
+        busy = _collect(results, procs, n, timeout_s)
         wall = time.perf_counter() - t0
     finally:
+        go.set()
         for p in procs:
             p.join(timeout=10)
             if p.is_alive():

@@ -19,3 +19,22 @@ def test_cpu_baselines_one_thread_and_all_cores():
     assert every["cores"] == min(os.cpu_count() or 1, len(seqs))
     assert every["kind"] == "oracle" and every["unit"] == "GB/s" and every["value"] > 0
     assert f"the same {len(seqs)} sequences" in every["sample"]
+
+
+def test_all_cores_leg_gives_up_on_a_dead_or_silent_process():
+    import queue
+
+    import bench
+    import pytest
+
+    class Proc:
+        def __init__(self, code):
+            self.exitcode = code
+
+    q = queue.Queue()
+    q.put(0.5)
+    assert bench._collect(q, [Proc(None)], 1, 5.0) == [0.5]
+    with pytest.raises(RuntimeError, match="exited with code 1"):
+        bench._collect(queue.Queue(), [Proc(None), Proc(1)], 2, 60.0)
+    with pytest.raises(TimeoutError):
+        bench._collect(queue.Queue(), [Proc(None)], 1, 1.5)
