@@ -39,14 +39,17 @@
  *    never dereferenced, the affected row is skipped or zero-filled, and a
  *    bit is set in the device status word (pkv_device_status).  No kernel
  *    traps, asserts or spins without a bound.
- *  - The decode partition pass uses programmatic dependent launch.  If the
- *    kernel before it on the stream lets its dependents start early
- *    (griddepcontrol.launch_dependents; of this library's kernels only a
- *    merge pass does, after its own partition pass has finished), the pass
- *    may begin before that kernel ends.  Until that kernel completes, the
- *    pass only reads context_lens, block_tables and the K/V pools.  It reads
- *    q, k_new and v_new, and writes any output, only after the kernel
- *    completes.
+ *  - The decode partition pass, the merge pass and the host-input staging
+ *    kernel are launched as programmatic dependents of the kernel before them
+ *    on the stream, so their CTAs are scheduled while it drains.  Each waits
+ *    for that kernel to complete (griddepcontrol.wait, which also makes its
+ *    stores visible) before it reads or writes any caller memory, whatever
+ *    that kernel is.  One exception, internal to a call: in
+ *    paged_kv_decode_step_layers the partition pass of layer l > 0 reads
+ *    context_lens, block_tables and layer l's pools before that wait, since
+ *    the kernel before it is layer l - 1's, which writes none of them.  Of
+ *    this library's kernels only a merge pass lets its dependents start
+ *    before it ends, and only once its own partition pass has finished.
  */
 #ifndef PAGEDKV_H_
 #define PAGEDKV_H_
@@ -211,8 +214,12 @@ pkv_status reshape_and_cache(const void* k_new, const void* v_new, void* k_cache
  * copy-on-write): block dst_block_ids[i] receives block src_block_ids[i]
  * ([16][num_kv_heads][head_dim] of K and of V), for i < num_pairs.  Both id
  * arrays are device int32; an id outside [0, num_blocks) skips that pair and
- * sets PKV_DEV_BAD_BLOCK_ID.  No dst block may appear among the src blocks of
- * the same call.  Bit-exact copy. */
+ * sets PKV_DEV_BAD_BLOCK_ID.  The destinations must be distinct and none may
+ * be the source of another pair (a pair with src == dst copies nothing):
+ * otherwise the outcome would depend on the order in which the copies run,
+ * so every pair in such a clash is skipped, its blocks left as they were, and
+ * PKV_DEV_BAD_BLOCK_ID is set; the other pairs are copied.  num_pairs is at
+ * most 2^31 - 1.  Bit-exact copy. */
 pkv_status paged_kv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src_block_ids,
                                 const int32_t* dst_block_ids, int num_pairs, int num_blocks,
                                 int num_kv_heads, int head_dim, pkv_dtype dtype,
@@ -440,6 +447,10 @@ pkv_status paged_kv_decode_step_host(const void* q_host, const void* k_new_host,
 /* Size of the static scratch used by paged_attention_decode_noalloc (32 MiB
  * per GPU that loads the library, held until the process exits). */
 #define PKV_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/* PKV_NOALLOC_SCRATCH_BYTES as the library was built with it (for bindings
+ * that do not read this header). */
+size_t paged_attention_noalloc_scratch_bytes(void);
 
 /* paged_attention_decode for callers that cannot allocate device memory (a
  * plug-in inside a framework that owns all device memory; a runtime whose

@@ -26,8 +26,10 @@ __all__ = [
     "paged_kv_decode_step_cascade", "new_cascade_workspace", "paged_attention_prefill",
     "paged_kv_decode_step_staging_bytes", "paged_kv_decode_step_host", "pkv_device_status",
     "paged_kv_last_error", "pkv_selftest_bounded_wait",
-    "BlockAllocator", "new_workspace", "paged_kv_block_hash", "paged_kv_copy_blocks", "paged_attention_decode_noalloc",
-    "NOALLOC_SCRATCH_BYTES",
+    "BlockAllocator", "new_workspace", "paged_kv_block_hash", "paged_kv_copy_blocks",
+    "paged_attention_decode_noalloc", "paged_attention_noalloc_scratch_bytes",
+    "PKV_OK", "PKV_ERR_INVALID_ARG", "PKV_ERR_UNSUPPORTED", "PKV_ERR_NO_BLOCKS",
+    "PKV_ERR_BAD_BLOCK_ID", "PKV_ERR_CUDA", "PKV_ERR_WORKSPACE",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -35,6 +37,9 @@ LIB_PATH = os.path.join(_PKG, "libpagedkv.so")
 BLOCK_SIZE = 16
 
 PKV_F16, PKV_BF16 = 0, 1
+# pkv_status codes
+(PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_NO_BLOCKS, PKV_ERR_BAD_BLOCK_ID,
+ PKV_ERR_CUDA, PKV_ERR_WORKSPACE) = range(7)
 DEV_BAD_BLOCK_ID, DEV_BAD_LENGTH, DEV_BAD_SLOT, DEV_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 
 _STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "not enough free blocks",
@@ -104,6 +109,7 @@ _SIGS = {
     "paged_kv_copy_blocks": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp], _i),
     "paged_attention_decode_noalloc": ([_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i, _f,
                                         _vp, _i, _vp], _i),
+    "paged_attention_noalloc_scratch_bytes": ([], _sz),
 }
 
 
@@ -468,15 +474,18 @@ def paged_kv_decode_step_host(q_host, k_new_host, v_new_host, block_tables_host,
         workspace.numel() * workspace.element_size(), _dtype_code(q_host), _stream(stream)))
 
 
-NOALLOC_SCRATCH_BYTES = 32 << 20
+def paged_attention_noalloc_scratch_bytes() -> int:
+    """Bytes of the static scratch array paged_attention_decode_noalloc uses."""
+    return int(lib().paged_attention_noalloc_scratch_bytes())
 
 
 def paged_attention_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens,
                                    max_context_len, scale, out, stream=None):
     """paged_attention_decode without a workspace argument, for callers that cannot
-    allocate device memory: the partials go to a static 32 MiB array inside the
-    library.  Calls share that array, so calls overlapping on the GPU must not be
-    issued; problems needing more scratch raise (status 6)."""
+    allocate device memory: the partials go to a static array inside the library
+    (paged_attention_noalloc_scratch_bytes()).  Calls share that array, so calls
+    overlapping on the GPU must not be issued; problems needing more scratch
+    raise (PKV_ERR_WORKSPACE)."""
     B, Hq, Hkv, D, NB = _check_decode_shapes(q, k_cache, v_cache, block_tables, context_lens,
                                              out)
     _check("paged_attention_decode_noalloc", lib().paged_attention_decode_noalloc(

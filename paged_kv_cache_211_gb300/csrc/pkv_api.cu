@@ -138,6 +138,10 @@ struct StageJobs {
 };
 
 __global__ void __launch_bounds__(256) stage_inputs_kernel(const StageJobs jobs) {
+    // launched as a programmatic dependent: the previous kernel on the stream
+    // may still run (and may still read the staging buffers or write the
+    // host inputs); wait for it before touching either
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
     const size_t stride = (size_t)gridDim.x * blockDim.x;
     const size_t t0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     for (int j = 0; j < jobs.n; ++j) {
@@ -249,12 +253,10 @@ pkv_status paged_kv_decode_step_host(const void* q_host, const void* k_new_host,
         size_t total = 0;
         for (int i = 0; i < jobs.n; ++i) total += jobs.bytes[i];
         const int blocks = (int)std::min<size_t>(128, (total / 16 + 255) / 256 + 1);
-        // programmatic dependent launch: after a previous step's merge pass it
-        // may run alongside it (that merge lets dependents start only once its
-        // partition pass, the last reader of the staging buffers, has
-        // finished, and itself reads only the workspace); this kernel never
-        // lets its own dependents start early, so the partition pass sees the
-        // staged inputs complete
+        // programmatic dependent launch: the grid is scheduled while the
+        // previous kernel drains and waits for it (griddepcontrol.wait) before
+        // it reads or writes anything; it never lets its own dependents start
+        // early, and the partition pass after it waits for it as well
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)blocks);
         cfg.blockDim = dim3(256);

@@ -102,25 +102,41 @@ __global__ void decode_step_write_kernel(const uint4* __restrict__ k_new,
 }
 
 // Whole-block copies for copy-on-write: block dst[i] of both pools receives
-// block src[i] ([16][Hkv][D] each).  One thread per 16-byte vector.
-__global__ void copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
-                                   const int32_t* __restrict__ src,
-                                   const int32_t* __restrict__ dst, int num_pairs,
-                                   int num_blocks, int block_vecs, unsigned int* status) {
-    const int64_t per_pair = 2ll * block_vecs;
-    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= per_pair * num_pairs) return;
-    const int i = (int)(idx / per_pair);
-    const int r = (int)(idx - (int64_t)i * per_pair);
-    const bool is_v = r >= block_vecs;
-    const int c = is_v ? r - block_vecs : r;
+// block src[i] ([16][Hkv][D] each).  One CTA per pair.  Its threads first
+// scan the pair list for a clash: pair i's destination is another pair's
+// destination or source, or its source is another pair's destination.  Then
+// the result would depend on the order in which the CTAs run, so a pair in
+// clash is skipped (its blocks keep their contents) and flagged instead.  A
+// pair whose source is its destination copies nothing and clashes with no
+// pair on that account.  Then the CTA moves the K and V blocks, one 16-byte
+// vector per thread per step.
+__global__ void __launch_bounds__(kThreads) copy_blocks_kernel(
+    uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, const int32_t* __restrict__ src,
+    const int32_t* __restrict__ dst, int num_pairs, int num_blocks, int block_vecs,
+    unsigned int* status) {
+    const int i = blockIdx.x;
     const int32_t s = src[i], d = dst[i];
     if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
-        if (r == 0) atomicOr(status, PKV_DEV_BAD_BLOCK_ID);
+        if (threadIdx.x == 0) atomicOr(status, PKV_DEV_BAD_BLOCK_ID);
         return;
     }
-    uint4* pool = is_v ? v_cache : k_cache;
-    pool[(int64_t)d * block_vecs + c] = pool[(int64_t)s * block_vecs + c];
+    int clash = 0;
+    for (int j = threadIdx.x; j < num_pairs; j += blockDim.x) {
+        if (j == i) continue;
+        const int32_t sj = src[j], dj = dst[j];
+        if (dj == d || (sj == d && s != d) || dj == s) clash = 1;
+    }
+    if (__syncthreads_or(clash)) {
+        if (threadIdx.x == 0) atomicOr(status, PKV_DEV_BAD_BLOCK_ID);
+        return;
+    }
+    if (s == d) return;
+    for (int r = threadIdx.x; r < 2 * block_vecs; r += blockDim.x) {
+        const bool is_v = r >= block_vecs;
+        const int c = is_v ? r - block_vecs : r;
+        uint4* pool = is_v ? v_cache : k_cache;
+        pool[(int64_t)d * block_vecs + c] = pool[(int64_t)s * block_vecs + c];
+    }
 }
 
 }  // namespace
@@ -203,9 +219,8 @@ pkv_status paged_kv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src
     unsigned int* status = pkv::status_word();
     if (!status) return PKV_ERR_CUDA;
     const int block_vecs = PKV_BLOCK_SIZE * num_kv_heads * head_dim / 8;
-    const int64_t total = 2ll * block_vecs * num_pairs;
-    const int grid = (int)((total + pkv::kThreads - 1) / pkv::kThreads);
-    pkv::copy_blocks_kernel<<<grid, pkv::kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+    pkv::copy_blocks_kernel<<<num_pairs, pkv::kThreads, 0,
+                              reinterpret_cast<cudaStream_t>(stream)>>>(
         static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), src_block_ids,
         dst_block_ids, num_pairs, num_blocks, block_vecs, status);
     return pkv::cuda_status(cudaGetLastError());

@@ -131,7 +131,11 @@ struct DecodeParams {
     int min_partition_blocks;  // lower bound of the adaptive choice
     int target_items;
     int even_split;            // TMA pass: cut the (sequence, head group, block) units evenly
-    int trigger_merge;         // TMA pass: a merge pass follows (let it launch early)
+    int trigger_merge;         // a merge pass follows in this call (let it launch early)
+    int early_reads;           // TMA pass: the previous kernel on the stream is this
+                               // library's, launched in the same call, and writes none of
+                               // the lengths, tables or this layer's pools: read them
+                               // before griddepcontrol.wait
     float scale_log2;          // scale * log2(e): scores live in base 2
 };
 
@@ -361,8 +365,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
         my_blocks += (n + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
     }
     const int total_blocks = cta_sum(my_blocks, red);
-    // the merge kernel may be launched now; it waits for this grid's results
-    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    // a merge pass of this call may be launched now (it waits for this grid's
+    // results); nothing else may start early: the next call's kernels could
+    // overwrite the inputs this pass still reads
+    if (p.trigger_merge) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
     // (2) partition length: fixed, or enough items for every CTA
     int PB = p.partition_blocks;
@@ -578,16 +584,23 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
 // ============================================================================
 // Partition pass, TMA version (the default).
 //
-// One persistent CTA per SM of eight warps, each doing the arithmetic of the
-// kernel above on its share of the blocks.  Every warp feeds itself: it walks
-// its blocks twice, once to load and once to consume, and keeps a ring of
-// shared-memory stages, each holding the 16 rows x D K and V tiles of one
-// block of its KV head.  The tiles arrive by cp.async.bulk.tensor copies of
-// boxes of 16 rows x 64 elements with the 128-byte swizzle, each stage
-// tracked by a "full" mbarrier.  Lane 0 refills a stage with the block one
-// ring ahead as soon as the warp's fragments of it are in registers (read
-// with ldmatrix, .trans for V, conflict-free under the swizzle).  Every slot
-// but the one being read is therefore in flight at all times, across item
+// One persistent CTA per SM with eight consumer warps, each doing the
+// arithmetic of the kernel above on its share of the blocks.  Every consumer
+// keeps a ring of shared-memory stages, each holding the 16 rows x D K and V
+// tiles of one block of its KV head.  The tiles arrive by
+// cp.async.bulk.tensor copies of boxes of 16 rows x 64 elements with the
+// 128-byte swizzle, each stage tracked by a "full" mbarrier; the consumer
+// reads its fragments with ldmatrix (.trans for V), conflict-free under the
+// swizzle.  Two feeds fill the rings (compile-time variants):
+//  - producer warp (items of one or two KV heads: long contexts): a ninth
+//    warp walks the same items as the consumers and issues every copy, in
+//    lane-parallel batches; a consumer releases a stage through its "empty"
+//    mbarrier once its fragments are in registers;
+//  - self-feeding consumers (items of four or more heads: short contexts):
+//    no producer warp; each consumer walks its blocks twice, once to load and
+//    once to consume, and lane 0 refills a stage with the block one ring
+//    ahead as soon as the stage's fragments are in registers.
+// Either way every slot but the one being read is in flight, across item
 // boundaries.  Every mbarrier wait is bounded: on a time-out the kernel sets
 // PKV_DEV_TIMEOUT, stops issuing and waiting, lets every copy it issued land,
 // and returns.
@@ -639,10 +652,16 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
 
-    // validated lengths, partition length, partitions per sequence (all warps).
-    // This grid may start while the previous kernel of the stream (a merge
-    // pass) still runs: until the consumers' griddepcontrol.wait below it only
-    // reads the lengths, the tables and the cache, and writes shared memory.
+    // This grid is a programmatic dependent of the previous kernel on the
+    // stream and may start before it ends.  Only when that kernel is this
+    // library's own, launched by the same call on other memory (a previous
+    // layer of paged_kv_decode_step_layers), do the lengths, the tables and
+    // the cache get read before the consumers' griddepcontrol.wait below;
+    // otherwise every thread waits here first, since any earlier kernel may
+    // have written them and only the wait makes its stores visible.
+    if (!p.early_reads) asm volatile("griddepcontrol.wait;\n" ::: "memory");
+
+    // validated lengths, partition length, partitions per sequence (all warps)
     int my_blocks = 0;
     for (int s = tid; s < B; s += NT) {
         int n = p.context_lens[s];
@@ -956,8 +975,8 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
         skip_done(fs);
         fs_id = table_entry(fs);
     };
-    // the first nstages blocks: only the cache is read, so this may overlap
-    // the previous kernel
+    // the first nstages blocks (before griddepcontrol.wait only with
+    // early_reads: then the previous kernel writes nothing read here)
     if constexpr (kSelfFeed) {
         fs.c = cursor_begin();
         fs.live = next_item(fs.c, fs.it);
@@ -1508,6 +1527,7 @@ pkv_status launch_decode(const DecodeParams& prm_in, const MergeParams& mp, int 
     const long long items_upper = parts_upper * prm.num_kv_heads;
     const int grid = (int)std::max<long long>(1, std::min<long long>(items_upper, (long long)std::max(occ, 1) * sms));
     prm.target_items = grid * kItemsPerCta;
+    prm.trigger_merge = (passes & kPassMerge) && need_merge;
     if (passes & kPassPartition) {
         kern<<<grid, kThreads, smem, stream>>>(prm);
         if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
@@ -1679,8 +1699,9 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp_i
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
             return PKV_ERR_CUDA;
-        // programmatic dependent launch: the prologue and the first cache
-        // loads overlap the previous merge pass (see the kernel)
+        // programmatic dependent launch: the CTAs are scheduled while the
+        // previous kernel drains; with early_reads the prologue and the first
+        // cache loads overlap a previous layer's merge pass (see the kernel)
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)grid);
         cfg.blockDim = dim3(tma_threads(self_feed));
@@ -1731,7 +1752,7 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
                        int partition_blocks, pkv_dtype dtype, int passes,
                        cudaStream_t stream, const void* k_new = nullptr,
                        const void* v_new = nullptr, int64_t* slot_out = nullptr,
-                       int prefix_blocks = 0) {
+                       int prefix_blocks = 0, bool chained = false) {
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
         max_blocks_per_seq <= 0 || num_blocks <= 0 || max_context_len < 0 ||
         partition_blocks < 0)
@@ -1799,6 +1820,7 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
     prm.target_items = 0;
     prm.even_split = 0;
     prm.trigger_merge = 0;
+    prm.early_reads = chained ? 1 : 0;
     prm.scale_log2 = scale * kLog2e;
 
     MergeParams mp;
@@ -2013,7 +2035,8 @@ pkv_status decode_step_impl(const void* q, const void* k_new, const void* v_new,
                             int num_q_heads, int num_kv_heads, int head_dim, int num_blocks,
                             float scale, void* out, int64_t* slot_mapping_out, void* workspace,
                             size_t workspace_bytes, pkv_dtype dtype, int passes,
-                            cudaStream_t stream, int prefix_blocks = 0) {
+                            cudaStream_t stream, int prefix_blocks = 0,
+                            bool chained = false) {
     if (num_seqs < 0 || num_kv_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0 ||
         num_blocks <= 0)
         return PKV_ERR_INVALID_ARG;
@@ -2022,7 +2045,7 @@ pkv_status decode_step_impl(const void* q, const void* k_new, const void* v_new,
     return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                        max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
                        num_blocks, scale, out, workspace, workspace_bytes, 0, dtype, passes,
-                       stream, k_new, v_new, slot_mapping_out, prefix_blocks);
+                       stream, k_new, v_new, slot_mapping_out, prefix_blocks, chained);
 }
 
 }  // namespace
@@ -2069,7 +2092,8 @@ pkv_status paged_kv_decode_step_layers(const void* q, const void* k_new, const v
             context_lens, max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
             num_blocks, scale, static_cast<char*>(out) + l * q_layer, nullptr, workspace,
             workspace_bytes, dtype, pkv::kPassPartition | pkv::kPassMerge,
-            reinterpret_cast<cudaStream_t>(stream));
+            reinterpret_cast<cudaStream_t>(stream), 0,
+            /*chained=*/l > 0);  // layer l-1's kernels write only layer l-1's pools
         if (rc != PKV_OK) return rc;
     }
     return PKV_OK;

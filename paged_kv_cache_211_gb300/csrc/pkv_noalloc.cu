@@ -49,6 +49,8 @@ void* scratch_address() {
 
 extern "C" {
 
+size_t paged_attention_noalloc_scratch_bytes(void) { return kScratchBytes; }
+
 pkv_status paged_attention_decode_noalloc(const void* q, const void* k_cache,
                                           const void* v_cache, const int32_t* block_tables,
                                           int max_blocks_per_seq, const int32_t* context_lens,

@@ -2,6 +2,8 @@
 ORIGINAL inputs (never on anything the CUDA path produced)."""
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import torch
 
@@ -15,20 +17,27 @@ def dtype_code(w) -> int:
     return oracle.BF16 if w.dtype == "bf16" else oracle.F16
 
 
-def compact_oracle_step(inp: dict, seq_ids, layer: int = 0):
-    """Oracle decode step (write, then attention) for the sequences `seq_ids`.
+def _chunks(seq_ids, lens, k):
+    """Split seq_ids into at most k groups of about equal token counts (longest
+    first to the least-loaded group); each group keeps the input order."""
+    seq_ids = [int(s) for s in seq_ids]
+    k = max(1, min(k, len(seq_ids)))
+    groups, load = [[] for _ in range(k)], [0] * k
+    for s in sorted(seq_ids, key=lambda s: -int(lens[s])):
+        i = load.index(min(load))
+        groups[i].append(s)
+        load[i] += int(lens[s]) + 1
+    pos = {s: i for i, s in enumerate(seq_ids)}
+    return [sorted(g, key=pos.get) for g in groups if g]
 
-    The blocks those sequences reference are copied from the untouched
-    device pools into a compact host pool (ids remapped; attention does not
-    depend on physical ids), the oracle writes the new tokens there, then
-    computes attention.  Returns (out [len(seq_ids), Hq, D] fp64, written
-    K rows, written V rows) where the written rows are [n, Hkv, D] uint16.
-    """
-    w = inp["workload"]
+
+def _compact(inp, seq_ids, need_lens, layer):
+    """Host copies (bit patterns) of the blocks the sequences `seq_ids` use up to
+    need_lens tokens (ids remapped; attention does not depend on physical ids)
+    and their remapped tables, taken from the device pools as they are now."""
     tables = inp["block_tables_host"]
-    lens = inp["context_lens_host"]
     seq_ids = np.asarray(seq_ids)
-    need = (lens[seq_ids].astype(np.int64) + BS - 1) // BS
+    need = (need_lens[seq_ids].astype(np.int64) + BS - 1) // BS
     used = sorted({int(b) for s, n in zip(seq_ids, need) for b in tables[s, :n]})
     remap = {b: i for i, b in enumerate(used)}
     idx = torch.tensor(used, dtype=torch.long, device=inp["k_cache"].device)
@@ -37,15 +46,65 @@ def compact_oracle_step(inp: dict, seq_ids, layer: int = 0):
     tb = np.zeros((len(seq_ids), tables.shape[1]), np.int32)
     for r, (s, n) in enumerate(zip(seq_ids, need)):
         tb[r, :n] = [remap[int(b)] for b in tables[s, :n]]
-    ln = lens[seq_ids].astype(np.int32)
-    sel = torch.tensor(seq_ids, dtype=torch.long, device=inp["q"].device)
-    q = bits(inp["q"].index_select(0, sel))
-    kn = bits(inp["k_new"][layer].index_select(0, sel))
-    vn = bits(inp["v_new"][layer].index_select(0, sel))
-    slots = oracle.slot_mapping(tb, ln, BS, len(used))
-    kc2, vc2 = oracle.reshape_and_cache(kn, vn, kc, vc, slots)
-    out = oracle.decode_attention(dtype_code(w), q, kc2, vc2, tb, ln, w.scale)
-    return out, kn, vn
+    return kc, vc, tb
+
+
+def oracle_steps(inp, seq_ids, steps, layer: int = 0, workers: int | None = None):
+    """The oracle's consecutive decode steps on the sequences `seq_ids`.
+
+    steps: dicts with host arrays over ALL sequences of the workload -- q
+    [B,Hq,D], k_new / v_new [B,Hkv,D] (uint16 bit patterns) and lens [B]
+    int32 -- applied in order: each step writes its new rows at position
+    len-1, then attends with its q.  The pools are read from the device as
+    they are when this is called (before the GPU touches them).  Work is
+    split over threads by sequence (the oracle's C calls release the GIL).
+    Returns one fp64 output [len(seq_ids), Hq, D] per step.
+    """
+    from concurrent.futures import ThreadPoolExecutor
+    w = inp["workload"]
+    code = dtype_code(w)
+    seq_ids = np.asarray(seq_ids)
+    need_lens = np.max(np.stack([np.asarray(st["lens"]) for st in steps]), axis=0)
+    k = workers or max(1, min(16, os.cpu_count() or 1))
+    parts = _chunks(seq_ids, need_lens, k)
+    jobs = []
+    for part in parts:
+        kc, vc, tb = _compact(inp, part, need_lens, layer)
+        jobs.append((part, kc, vc, tb))
+
+    def run(job):
+        part, kc, vc, tb = job
+        outs = []
+        for st in steps:
+            ln = np.asarray(st["lens"])[part].astype(np.int32)
+            slots = oracle.slot_mapping(tb, ln, BS, kc.shape[0])
+            kc, vc = oracle.reshape_and_cache(st["k_new"][part], st["v_new"][part], kc, vc,
+                                              slots)
+            outs.append(oracle.decode_attention(code, st["q"][part], kc, vc, tb, ln, w.scale))
+        return outs
+
+    with ThreadPoolExecutor(max_workers=len(jobs)) as ex:
+        results = list(ex.map(run, jobs))
+    # back to the order of seq_ids
+    row = {int(s): i for i, s in enumerate(seq_ids)}
+    outs = []
+    for i in range(len(steps)):
+        o = np.empty((len(seq_ids),) + results[0][i].shape[1:], np.float64)
+        for (part, _, _, _), r in zip(jobs, results):
+            o[[row[s] for s in part]] = r[i]
+        outs.append(o)
+    return outs
+
+
+def compact_oracle_step(inp, seq_ids, layer: int = 0):
+    """Oracle decode step (write, then attention) of the workload's own step
+    (q, and layer `layer`'s new rows and pools) for the sequences `seq_ids`.  Returns (out [len(seq_ids), Hq, D] fp64,
+    written K rows, written V rows), the written rows [n, Hkv, D] uint16."""
+    seq_ids = np.asarray(seq_ids)
+    step = dict(q=bits(inp["q"]), k_new=bits(inp["k_new"][layer]),
+                v_new=bits(inp["v_new"][layer]), lens=inp["context_lens_host"])
+    out = oracle_steps(inp, seq_ids, [step], layer=layer)[0]
+    return out, step["k_new"][seq_ids], step["v_new"][seq_ids]
 
 
 def assert_attention_close(got_bits: np.ndarray, want: np.ndarray, dtype: int, what: str = ""):

@@ -236,6 +236,31 @@ def test_copy_blocks_bit_exact(cuda_device):
 
 
 @pytest.mark.gpu
+def test_copy_blocks_skips_clashing_pairs(cuda_device):
+    """Pairs whose outcome would depend on the order of the copies are skipped
+    and flagged: two pairs writing block 4, and a pair writing block 3, which
+    pair 0 reads.  A pair copying a block onto itself changes nothing.  The
+    other pairs are copied bit for bit, as the oracle copies them."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    g = torch.Generator(device=cuda_device).manual_seed(6)
+    NB, Hkv, D = 24, 4, 64
+    kc = torch.randn(NB, 16, Hkv, D, generator=g, device=cuda_device).to(torch.float16)
+    vc = torch.randn(NB, 16, Hkv, D, generator=g, device=cuda_device).to(torch.float16)
+    src = np.array([3, 7, 0, 11, 5, 9, 6, 13], np.int32)
+    dst = np.array([12, 4, 19, 1, 4, 3, 6, 20], np.int32)
+    copied = [2, 3, 7]                         # 0, 1, 4 and 5 clash; 6 is a self-copy
+    bits = lambda t: t.cpu().view(torch.int16).numpy().view(np.uint16)
+    want_k, want_v = oracle.copy_blocks(bits(kc), bits(vc), src[copied], dst[copied])
+    pkv.paged_kv_copy_blocks(kc, vc, torch.from_numpy(src).to(cuda_device),
+                             torch.from_numpy(dst).to(cuda_device))
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_status() == pkv.DEV_BAD_BLOCK_ID
+    assert np.array_equal(bits(kc), want_k) and np.array_equal(bits(vc), want_v)
+
+
+@pytest.mark.gpu
 def test_parallel_sampling_fork_with_copy_on_write(cuda_device):
     """Two sequences forked from one 40-token prompt share its 3 blocks (the
     last one partial).  Before each appends its own token, copy-on-write gives
