@@ -248,18 +248,15 @@ def make_prefill_inputs(w: Workload, chunk: int, device="cpu") -> dict:
     """A chunked-prefill step of ``w``: every sequence's last ``chunk`` tokens
     (or all of them, if shorter) are query rows.  Keys as in make_inputs for
     the pools and tables, plus q_rows [R,Hq,D], k_rows/v_rows [R,Hkv,D] (the
-    chunk's K/V), cu_q_lens [B+1] int32 and the rows' slots (int64), listed
-    by walking each table block by block."""
+    chunk's K/V), cu_q_lens [B+1] int32, and for every packed row its
+    sequence (row_seq) and position in that sequence (row_pos), int32 [R]."""
     inp = make_inputs(w, device=device, num_layers=1, poison=False)
     lens = inp["context_lens_host"]
-    tables = inp["block_tables_host"]
     qlens = np.minimum(lens, chunk).astype(np.int64)
     cu = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
-    slots = []
-    for s in range(w.num_seqs):
-        n = int(lens[s])
-        for t in range(n - int(qlens[s]), n):
-            slots.append(int(tables[s, t // BLOCK_SIZE]) * BLOCK_SIZE + t % BLOCK_SIZE)
+    row_seq = np.repeat(np.arange(w.num_seqs), qlens).astype(np.int32)
+    row_pos = np.concatenate([np.arange(int(n) - int(ql), int(n))
+                              for n, ql in zip(lens, qlens)]).astype(np.int32)
     dev = torch.device(device)
     gen = torch.Generator(device=dev)
     gen.manual_seed(w.seed * 1000 + 11)
@@ -269,7 +266,7 @@ def make_prefill_inputs(w: Workload, chunk: int, device="cpu") -> dict:
         k_rows=_randn((R, w.num_kv_heads, w.head_dim), w.torch_dtype, dev, gen),
         v_rows=_randn((R, w.num_kv_heads, w.head_dim), w.torch_dtype, dev, gen),
         cu_q_lens=torch.from_numpy(cu).to(dev), cu_q_lens_host=cu,
-        row_slots=torch.tensor(slots, dtype=torch.int64, device=dev),
+        row_seq=torch.from_numpy(row_seq).to(dev), row_pos=torch.from_numpy(row_pos).to(dev),
         max_q_len=int(qlens.max()))
     return inp
 
