@@ -47,9 +47,12 @@
  *    that kernel is.  One exception, internal to a call: in
  *    paged_kv_decode_step_layers the partition pass of layer l > 0 reads
  *    context_lens, block_tables and layer l's pools before that wait, since
- *    the kernel before it is layer l - 1's, which writes none of them.  Of
- *    this library's kernels only a merge pass lets its dependents start
- *    before it ends, and only once its own partition pass has finished.
+ *    the kernel before it is layer l - 1's, which writes none of them.  The
+ *    TMA partition pass (after its prologue) and the merge pass (once its
+ *    partition pass has finished) let the next kernel's CTAs be scheduled
+ *    before they end; a dependent of another library must then wait for
+ *    them (griddepcontrol.wait) before it reads their outputs, as
+ *    programmatic dependent launch requires of any dependent.
  */
 #ifndef PAGEDKV_H_
 #define PAGEDKV_H_

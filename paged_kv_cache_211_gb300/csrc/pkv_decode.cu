@@ -131,7 +131,8 @@ struct DecodeParams {
     int min_partition_blocks;  // lower bound of the adaptive choice
     int target_items;
     int even_split;            // TMA pass: cut the (sequence, head group, block) units evenly
-    int trigger_merge;         // a merge pass follows in this call (let it launch early)
+    int trigger_merge;         // register-pipelined pass: a merge pass follows in this call
+                               // (let it launch early)
     int early_reads;           // TMA pass: the previous kernel on the stream is this
                                // library's, launched in the same call, and writes none of
                                // the lengths, tables or this layer's pools: read them
@@ -721,9 +722,14 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
     }
     if (tid == 0) sm_off[B] = total_parts;
     __syncthreads();
-    // only a merge pass may start early: a following partition pass (of the
-    // next call) must see this pass's cache writes complete
-    if (p.trigger_merge) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    // The next kernel on the stream (the merge pass, or the next call's first
+    // kernel) may be scheduled now, so that its CTAs start as this grid's
+    // leave the SMs.  Each of this library's dependents waits for this grid
+    // (griddepcontrol.wait) before it touches what this grid reads or
+    // writes; only the next layer's partition pass of a multi-layer step
+    // reads early, and then only its own layer's pools, the lengths and the
+    // tables, which this grid never writes.
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
     const int Hq = p.num_q_heads, Hkv = p.num_kv_heads;
     const size_t row_stride = (size_t)Hkv * D;
@@ -1679,7 +1685,6 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp_i
         // per-head items: 8 per CTA; all-heads items carry Hkv heads each: 4 per CTA
         prm.target_items = grid * tma_items_per_cta(hpi);
     }
-    prm.trigger_merge = (passes & kPassMerge) && need_merge;
 
     if (passes & kPassPartition) {
         CUtensorMap tmk, tmv;
