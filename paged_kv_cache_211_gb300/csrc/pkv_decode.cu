@@ -127,12 +127,18 @@ struct DecodeParams {
     int max_blocks_per_seq, num_blocks, len_bound;
     int partition_blocks;      // > 0: fixed partition length (blocks)
     int skip_blocks;           // cascade: leading shared blocks handled by the prefix pass
-    int prefix_parts;          // cascade: workspace rows per sequence written by the prefix pass
+    int prefix_parts;          // cascade: 1 (the prefix pass writes workspace row s of
+                               // sequence s), else 0
+    int item_row0;             // first workspace row of the items (num_seqs in a cascade)
     int min_partition_blocks;  // lower bound of the adaptive choice
     int target_items;
     int even_split;            // TMA pass: cut the (sequence, head group, block) units evenly
     int trigger_merge;         // register-pipelined pass: a merge pass follows in this call
                                // (let it launch early)
+    int no_wait;               // TMA pass of a cascade: the previous kernel is this call's
+                               // prefix pass, which runs beside it on disjoint memory and
+                               // itself started after everything before it: no
+                               // griddepcontrol.wait at all
     int early_reads;           // TMA pass: the previous kernel on the stream is this
                                // library's, launched in the same call, and writes none of
                                // the lengths, tables or this layer's pools: read them
@@ -179,8 +185,8 @@ __device__ __forceinline__ int cta_exclusive_scan(int v, int* red, int* total) {
 // Partition-pass items of one sequence.  Normally its blocks in partitions
 // of pb (an empty sequence keeps one empty partition, which writes zeros).
 // In cascade mode the first `skip` blocks belong to the prefix pass, which
-// writes the sequence's first prefix_parts workspace rows; the items cover
-// the remaining blocks only, and may be none.
+// writes the sequence's prefix workspace row; the items cover the remaining
+// blocks only, and may be none.
 __device__ __forceinline__ int item_parts(int n, int pb, int skip, int prefix_parts) {
     const int nblk = (n + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
     if (prefix_parts == 0) return nblk == 0 ? 1 : (nblk + pb - 1) / pb;
@@ -396,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
     __syncthreads();
     if (blockIdx.x == 0) {
         // workspace rows of sequence s: its prefix rows, then one per item
-        for (int s = tid; s <= B; s += kThreads) p.ws_offsets[s] = sm_off[s] + p.prefix_parts * s;
+        for (int s = tid; s <= B; s += kThreads) p.ws_offsets[s] = sm_off[s];
     }
 
     const T* __restrict__ q = static_cast<const T*>(p.q);
@@ -417,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
         const int s = a;
         const int part = gp - sm_off[s];
         const int nparts = sm_off[s + 1] - sm_off[s] + p.prefix_parts;  // workspace rows of s
-        const int ws_row = gp + p.prefix_parts * (s + 1);               // this item's row
+        const int ws_row = p.item_row0 + gp;                            // this item's row
         const int n = sm_len[s];
         const int nblk = (n + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
         const int blk_lo = p.skip_blocks + part * PB;
@@ -660,7 +666,7 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
     // the cache get read before the consumers' griddepcontrol.wait below;
     // otherwise every thread waits here first, since any earlier kernel may
     // have written them and only the wait makes its stores visible.
-    if (!p.early_reads) asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    if (!p.early_reads && !p.no_wait) asm volatile("griddepcontrol.wait;\n" ::: "memory");
 
     // validated lengths, partition length, partitions per sequence (all warps)
     int my_blocks = 0;
@@ -761,7 +767,7 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
         }
         it.s = a;
         const int nparts = sm_off[a + 1] - sm_off[a] + p.prefix_parts;  // workspace rows of s
-        const int ws_row = gp + p.prefix_parts * (a + 1);               // this item's row
+        const int ws_row = p.item_row0 + gp;                            // this item's row
         it.dest = nparts == 1 ? -1 : ws_row * Hq + it.hg * HPI * g;
         it.n = sm_len[a];
         it.nblk = (it.n + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE;
@@ -993,11 +999,11 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
     }
 
     // q, k_new, v_new and every output may belong to the previous kernel:
-    // wait for it
-    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    // wait for it (a cascade's partition pass has nothing to wait for)
+    if (!p.no_wait) asm volatile("griddepcontrol.wait;\n" ::: "memory");
     if (blockIdx.x == 0) {
         for (int s = tid; s <= B; s += NC * 32)
-            p.ws_offsets[s] = sm_off[s] + p.prefix_parts * s;
+            p.ws_offsets[s] = sm_off[s];
         if (p.slot_out) {
             // no slot for an empty or invalid sequence, nor for a cascade
             // token that would land in a shared block
@@ -1238,172 +1244,6 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
 }
 
 
-// ============================================================================
-// Cascade decode: the prefix pass.
-//
-// When every sequence's first P table entries are the same P full blocks (a
-// shared prompt prefix, "从零手写 vLLM 核心：mini-vllm 项目深度解析" §2: prefix
-// cache / parallel sampling share blocks), the prefix is attended once for
-// all sharers instead of once per sequence.  A warp takes one KV head, one
-// chunk of the prefix and a tile of 8 query vectors of that KV head taken
-// across sequences (column c of the tile is query head c % g of sequence
-// c / g), and runs the same block loop as the partition pass with the 8
-// vectors as the n = 8 side of the MMA: each K/V row read serves 8 query
-// vectors of (for g < 8) several sequences.  Each column is masked by its own
-// sequence's length.  The warp leaves (m, l, o) for its columns in the
-// sequence's workspace row for the chunk; the suffix partitions and the merge
-// pass do the rest.
-// ============================================================================
-constexpr int kPrefixChunkBlocks = 8;
-
-struct PrefixParams {
-    const void* q;
-    const void* k_cache;
-    const void* v_cache;
-    const int32_t* block_tables;  // the prefix is row 0's first prefix_blocks entries
-    const int32_t* context_lens;
-    const int* ws_offsets;        // written by the partition pass before this kernel
-    float* ws_m;
-    float* ws_l;
-    float* ws_o;
-    unsigned int* status;
-    int num_seqs, num_q_heads, num_kv_heads, group, num_blocks, len_bound;
-    int prefix_blocks, prefix_parts;
-    float scale_log2;
-};
-
-template <typename T, int D>
-__global__ void __launch_bounds__(128) decode_prefix_kernel(const PrefixParams p) {
-    using E = Elem<T>;
-    constexpr int KC = BlockFrag<D>::KC;
-    constexpr int VC = BlockFrag<D>::VC;
-    constexpr int NT = D / 16;
-    const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
-    const int g = p.group, Hq = p.num_q_heads, Hkv = p.num_kv_heads;
-    const int cols = p.num_seqs * g;
-    const int tiles = (cols + 7) / 8;
-    const int unit = blockIdx.x * 4 + (threadIdx.x >> 5);
-    if (unit >= Hkv * tiles * p.prefix_parts) return;
-    const int chunk = unit % p.prefix_parts;
-    const int tile = (unit / p.prefix_parts) % tiles;
-    const int h = unit / (p.prefix_parts * tiles);
-    const int prefix_tokens = p.prefix_blocks * PKV_BLOCK_SIZE;
-
-    // query fragment: column gid is query vector tile*8 + gid
-    uint4 qf[KC];
-    {
-        const int c = tile * 8 + gid;
-        const bool live = c < cols;
-        const T* qrow = static_cast<const T*>(p.q) +
-                        ((size_t)(live ? c / g : 0) * Hq + (size_t)h * g + (live ? c % g : 0)) * D;
-#pragma unroll
-        for (int j = 0; j < KC; ++j)
-            qf[j] = live ? *reinterpret_cast<const uint4*>(qrow + (4 * j + tig) * 8)
-                         : make_uint4(0u, 0u, 0u, 0u);
-    }
-    // prefix tokens visible to this lane's two score columns 2tig, 2tig+1
-    auto visible = [&](int c) {
-        if (c >= cols) return 0;
-        int n = p.context_lens[c / g];
-        if (n < 0 || n > p.len_bound) n = 0;  // flagged by the partition pass
-        return min(n, prefix_tokens);
-    };
-    const int len0 = visible(tile * 8 + 2 * tig), len1 = visible(tile * 8 + 2 * tig + 1);
-
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    float o[NT][4];
-#pragma unroll
-    for (int i = 0; i < NT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    const size_t row_stride = (size_t)Hkv * D;
-    const T* kbase = static_cast<const T*>(p.k_cache) + (size_t)h * D;
-    const T* vbase = static_cast<const T*>(p.v_cache) + (size_t)h * D;
-    const int b_lo = chunk * kPrefixChunkBlocks;
-    const int b_hi = min(p.prefix_blocks, b_lo + kPrefixChunkBlocks);
-    for (int j = b_lo; j < b_hi; ++j) {
-        int id = p.block_tables[j];
-        if (id < 0 || id >= p.num_blocks) {
-            atomicOr(p.status, PKV_DEV_BAD_BLOCK_ID);
-            continue;  // never read
-        }
-        BlockFrag<D> f;
-        fetch_block<T, D>(f, kbase, vbase, id, row_stride, gid, tig, -1, nullptr, nullptr);
-        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int k = 0; k < KC; ++k) {
-            E::mma(sa, f.k[0][k].x, f.k[1][k].x, f.k[0][k].y, f.k[1][k].y, qf[k].x, qf[k].y);
-            E::mma(sb, f.k[0][k].z, f.k[1][k].z, f.k[0][k].w, f.k[1][k].w, qf[k].z, qf[k].w);
-        }
-        float s0 = (sa[0] + sb[0]) * p.scale_log2, s1 = (sa[1] + sb[1]) * p.scale_log2;
-        float s2 = (sa[2] + sb[2]) * p.scale_log2, s3 = (sa[3] + sb[3]) * p.scale_log2;
-        // per-column masks (prefix blocks are full, so V rows are finite data)
-        const int t0 = len0 - j * PKV_BLOCK_SIZE, t1 = len1 - j * PKV_BLOCK_SIZE;
-        if (gid >= t0) s0 = -INFINITY;
-        if (gid >= t1) s1 = -INFINITY;
-        if (gid + 8 >= t0) s2 = -INFINITY;
-        if (gid + 8 >= t1) s3 = -INFINITY;
-        float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-        }
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float ms0 = mn0 == -INFINITY ? 0.f : mn0;
-        const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float c0 = fast_exp2(m0 - ms0), c1 = fast_exp2(m1 - ms1);
-        const float p0 = fast_exp2(s0 - ms0), p1 = fast_exp2(s1 - ms1);
-        const float p2 = fast_exp2(s2 - ms0), p3 = fast_exp2(s3 - ms1);
-        l0 = l0 * c0 + p0 + p2;
-        l1 = l1 * c1 + p1 + p3;
-        m0 = mn0;
-        m1 = mn1;
-#pragma unroll
-        for (int i = 0; i < NT; ++i) {
-            o[i][0] *= c0;
-            o[i][1] *= c1;
-            o[i][2] *= c0;
-            o[i][3] *= c1;
-        }
-        const uint32_t pt = movmatrix_trans(E::pack(p0, p1));
-        const uint32_t pbt = movmatrix_trans(E::pack(p2, p3));
-#pragma unroll
-        for (int i = 0; i < NT; ++i) {
-            const int c = i >> 2, w = i & 3;
-            const uint32_t x0 = word_of(f.v[c][0], w), x1 = word_of(f.v[c][1], w);
-            const uint32_t x2 = word_of(f.v[c][2], w), x3 = word_of(f.v[c][3], w);
-            E::mma(o[i], __byte_perm(x0, x1, 0x5410), __byte_perm(x0, x1, 0x7632),
-                   __byte_perm(x2, x3, 0x5410), __byte_perm(x2, x3, 0x7632), pt, pbt);
-        }
-    }
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-    }
-    // this lane holds columns 2tig, 2tig+1 at d = 8*(gid + 8c) + e
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const int c = tile * 8 + 2 * tig + half;
-        if (c >= cols) continue;
-        const int sq = c / g, qh = h * g + c % g;
-        const size_t row = (size_t)(p.ws_offsets[sq] + chunk) * Hq + qh;
-#pragma unroll
-        for (int cc = 0; cc < VC; ++cc) {
-            float* dst = p.ws_o + row * D + 8 * (gid + 8 * cc);
-            const int e = half;
-            *reinterpret_cast<float4*>(dst) = make_float4(
-                o[4 * cc][e], o[4 * cc][e + 2], o[4 * cc + 1][e], o[4 * cc + 1][e + 2]);
-            *reinterpret_cast<float4*>(dst + 4) = make_float4(
-                o[4 * cc + 2][e], o[4 * cc + 2][e + 2], o[4 * cc + 3][e], o[4 * cc + 3][e + 2]);
-        }
-        if (gid == 0) {
-            p.ws_m[row] = half ? m1 : m0;
-            p.ws_l[row] = half ? l1 : l0;
-        }
-    }
-}
-
-
 struct MergeParams {
     const int* ws_offsets;
     const float* ws_m;
@@ -1412,6 +1252,8 @@ struct MergeParams {
     void* out;
     int num_seqs, num_q_heads;
     int min_rows;  // merge sequences with at least this many workspace rows
+    int prefix_rows;  // cascade: 1 (row s holds sequence s's prefix partials), else 0
+    int item_row0;    // first workspace row of the items
     // even split of the TMA pass (even_grid > 0): ws_offsets holds block
     // offsets, and the CTAs that covered a (sequence, group) left its partials
     // in their slots (two per CTA, even_heads query heads each)
@@ -1453,12 +1295,16 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const MergeParams p) 
         if (np < 2) return;  // one CTA covered it and wrote the output
     } else {
         const int off = p.ws_offsets[s];
-        np = p.ws_offsets[s + 1] - off;
+        np = p.ws_offsets[s + 1] - off + p.prefix_rows;
         if (np < p.min_rows) return;  // a one-row sequence was written by the partition pass
-        base = (size_t)off * Hq + qh;
+        base = ((size_t)p.item_row0 + off) * Hq + qh;
     }
     auto row_of = [&](int i) -> long long {
-        if (G == 0) return (long long)(base + (size_t)i * Hq);
+        if (G == 0) {
+            if (p.prefix_rows == 0) return (long long)(base + (size_t)i * Hq);
+            // cascade: the prefix row first, then the items
+            return i == 0 ? (long long)s * Hq + qh : (long long)(base + (size_t)(i - 1) * Hq);
+        }
         const long long c = c0 + i;
         const long long b = c * U / G;
         if (b == (c + 1) * U / G) return -1;  // a CTA with no units (U < G)
@@ -1512,10 +1358,14 @@ size_t partition_smem_bytes(int head_dim, int num_seqs) {
 
 constexpr int kPassPartition = 1;
 constexpr int kPassMerge = 2;
+// A cascade's prefix pass takes at most 1 / kCascadePrefixShare of the SMs;
+// the partition pass over the sequences' own blocks takes the rest.
+constexpr int kCascadePrefixShare = 8;
 
 template <typename T, int D>
 pkv_status launch_decode(const DecodeParams& prm_in, const MergeParams& mp, int pb_lower,
-                         int max_blocks, bool need_merge, int passes, cudaStream_t stream) {
+                         int max_blocks, bool need_merge, int passes, bool plain_merge,
+                         cudaStream_t stream) {
     DecodeParams prm = prm_in;
     auto kern = decode_partition_kernel<T, D>;
     const size_t smem = partition_smem_bytes(D, prm.num_seqs);
@@ -1551,7 +1401,7 @@ pkv_status launch_decode(const DecodeParams& prm_in, const MergeParams& mp, int 
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = plain_merge ? 0 : 1;
         if (cudaLaunchKernelEx(&cfg, decode_merge_kernel<T, D>, mp) != cudaSuccess)
             return PKV_ERR_CUDA;
     }
@@ -1645,11 +1495,12 @@ int tma_items_per_cta(int heads_per_item) {
 template <typename T, int D>
 pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp_in, int pb_lower,
                              int max_blocks, bool need_merge, int passes, int nstages,
-                             cudaStream_t stream) {
+                             int sm_cap, bool plain_merge, cudaStream_t stream) {
     DecodeParams prm = prm_in;
     MergeParams mp = mp_in;
-    const int sms = sm_count();
+    int sms = sm_count();
     if (sms <= 0) return PKV_ERR_CUDA;
+    if (sm_cap > 0) sms = std::min(sms, sm_cap);  // the other SMs run a cascade's prefix pass
     // The adaptive, non-cascade pass over long contexts splits the work
     // evenly over the CTAs (measured: CTAs of the round-robin item split
     // finished up to 17 % apart on lognormal lengths).  Short contexts (under
@@ -1731,7 +1582,7 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp_i
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = plain_merge ? 0 : 1;
         if (cudaLaunchKernelEx(&cfg, decode_merge_kernel<T, D>, mp) != cudaSuccess)
             return PKV_ERR_CUDA;
     }
@@ -1774,7 +1625,7 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
         return PKV_ERR_INVALID_ARG;
     if (prefix_blocks < 0 || prefix_blocks > max_blocks_per_seq) return PKV_ERR_INVALID_ARG;
-    const int prefix_parts = ceil_div(prefix_blocks, kPrefixChunkBlocks);  // 0 unless cascade
+    const int prefix_parts = prefix_blocks > 0 ? 1 : 0;  // the cascade's prefix row
     const WsLayout ws =
         ws_layout(num_seqs, num_q_heads, head_dim, max_context_len, prefix_parts);
     if (!workspace || workspace_bytes < ws.total ||
@@ -1821,6 +1672,8 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
     prm.partition_blocks = partition_blocks;
     prm.skip_blocks = prefix_blocks;
     prm.prefix_parts = prefix_parts;
+    prm.item_row0 = num_seqs * prefix_parts;  // rows 0 .. num_seqs - 1: the prefix partials
+    prm.no_wait = 0;
     prm.min_partition_blocks = pb_lower;
     prm.target_items = 0;
     prm.even_split = 0;
@@ -1837,6 +1690,8 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
     mp.num_seqs = num_seqs;
     mp.num_q_heads = num_q_heads;
     mp.min_rows = prefix_parts > 0 ? 1 : 2;
+    mp.prefix_rows = prefix_parts;
+    mp.item_row0 = prm.item_row0;
     mp.even_grid = 0;  // the TMA pass sets the even-split fields
     mp.even_heads = 0;
     mp.groups = 0;
@@ -1847,71 +1702,63 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
                             ? tma_stages(head_dim, num_seqs, g)
                             : 0;
     const int grid_blocks = std::max(1, max_blocks - prefix_blocks);  // blocks items can cover
-    auto run = [&](int pass_mask) -> pkv_status {
+    auto run = [&](int pass_mask, int sm_cap, bool plain_merge) -> pkv_status {
         if (nstages > 0) {
             if (dtype == PKV_BF16)
                 return head_dim == 128
                            ? launch_decode_tma<__nv_bfloat16, 128>(prm, mp, pb_lower, grid_blocks,
                                                                    need_merge, pass_mask, nstages,
-                                                                   stream)
+                                                                   sm_cap, plain_merge, stream)
                            : launch_decode_tma<__nv_bfloat16, 64>(prm, mp, pb_lower, grid_blocks,
                                                                   need_merge, pass_mask, nstages,
-                                                                  stream);
+                                                                  sm_cap, plain_merge, stream);
             return head_dim == 128
                        ? launch_decode_tma<__half, 128>(prm, mp, pb_lower, grid_blocks, need_merge,
-                                                        pass_mask, nstages, stream)
+                                                        pass_mask, nstages, sm_cap, plain_merge,
+                                                        stream)
                        : launch_decode_tma<__half, 64>(prm, mp, pb_lower, grid_blocks, need_merge,
-                                                       pass_mask, nstages, stream);
+                                                       pass_mask, nstages, sm_cap, plain_merge,
+                                                       stream);
         }
         if (dtype == PKV_BF16)
-            return head_dim == 128 ? launch_decode<__nv_bfloat16, 128>(
-                                         prm, mp, pb_lower, grid_blocks, need_merge, pass_mask, stream)
-                                   : launch_decode<__nv_bfloat16, 64>(
-                                         prm, mp, pb_lower, grid_blocks, need_merge, pass_mask, stream);
+            return head_dim == 128
+                       ? launch_decode<__nv_bfloat16, 128>(prm, mp, pb_lower, grid_blocks,
+                                                           need_merge, pass_mask, plain_merge,
+                                                           stream)
+                       : launch_decode<__nv_bfloat16, 64>(prm, mp, pb_lower, grid_blocks,
+                                                          need_merge, pass_mask, plain_merge,
+                                                          stream);
         return head_dim == 128 ? launch_decode<__half, 128>(prm, mp, pb_lower, grid_blocks,
-                                                            need_merge, pass_mask, stream)
+                                                            need_merge, pass_mask, plain_merge,
+                                                            stream)
                                : launch_decode<__half, 64>(prm, mp, pb_lower, grid_blocks,
-                                                           need_merge, pass_mask, stream);
+                                                           need_merge, pass_mask, plain_merge,
+                                                           stream);
     };
-    if (prefix_parts == 0) return run(passes);
+    if (prefix_parts == 0) return run(passes, 0, false);
 
-    // cascade: suffix partitions, then the shared prefix for all sharers, then the merge
+    // Cascade.  The shared prefix for all sharers runs first on the tensor
+    // cores, on a few SMs (an ordinary launch: it waits for everything before
+    // it).  The partition pass over the sequences' own blocks is its
+    // programmatic dependent and runs beside it on the other SMs: the two
+    // share nothing they write (prefix rows vs item rows, the new tokens
+    // land past the prefix), so the TMA pass does not wait at all.  The
+    // merge is an ordinary launch, so it waits for both.
     if (passes & kPassPartition) {
-        pkv_status rc = run(kPassPartition);
+        const int sms = sm_count();
+        if (sms <= 0) return PKV_ERR_CUDA;
+        int pgrid = 0;
+        pkv_status rc = launch_cascade_prefix(
+            q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, len_bound,
+            num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, prefix_blocks,
+            prm.scale_log2, prm.ws_m, prm.ws_l, prm.ws_o, dtype,
+            std::max(1, sms / kCascadePrefixShare), &pgrid, stream);
         if (rc != PKV_OK) return rc;
-        PrefixParams pp;
-        pp.q = q;
-        pp.k_cache = k_cache;
-        pp.v_cache = v_cache;
-        pp.block_tables = block_tables;
-        pp.context_lens = context_lens;
-        pp.ws_offsets = prm.ws_offsets;
-        pp.ws_m = prm.ws_m;
-        pp.ws_l = prm.ws_l;
-        pp.ws_o = prm.ws_o;
-        pp.status = status;
-        pp.num_seqs = num_seqs;
-        pp.num_q_heads = num_q_heads;
-        pp.num_kv_heads = num_kv_heads;
-        pp.group = g;
-        pp.num_blocks = num_blocks;
-        pp.len_bound = len_bound;
-        pp.prefix_blocks = prefix_blocks;
-        pp.prefix_parts = prefix_parts;
-        pp.scale_log2 = prm.scale_log2;
-        const long long units =
-            (long long)num_kv_heads * ((num_seqs * g + 7) / 8) * prefix_parts;
-        const unsigned grid = (unsigned)((units + 3) / 4);
-        if (dtype == PKV_BF16) {
-            if (head_dim == 128) decode_prefix_kernel<__nv_bfloat16, 128><<<grid, 128, 0, stream>>>(pp);
-            else decode_prefix_kernel<__nv_bfloat16, 64><<<grid, 128, 0, stream>>>(pp);
-        } else {
-            if (head_dim == 128) decode_prefix_kernel<__half, 128><<<grid, 128, 0, stream>>>(pp);
-            else decode_prefix_kernel<__half, 64><<<grid, 128, 0, stream>>>(pp);
-        }
-        if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+        prm.no_wait = 1;
+        rc = run(kPassPartition, std::max(1, sms - pgrid), true);
+        if (rc != PKV_OK) return rc;
     }
-    return (passes & kPassMerge) ? run(kPassMerge) : PKV_OK;
+    return (passes & kPassMerge) ? run(kPassMerge, 0, true) : PKV_OK;
 }
 
 }  // namespace
@@ -1935,7 +1782,7 @@ size_t paged_attention_cascade_workspace_bytes(int num_seqs, int num_q_heads, in
         num_prefix_blocks < 0)
         return 0;
     return pkv::ws_layout(num_seqs, num_q_heads, head_dim, max_context_len,
-                          pkv::ceil_div(num_prefix_blocks, pkv::kPrefixChunkBlocks))
+                          num_prefix_blocks > 0 ? 1 : 0)
         .total;
 }
 

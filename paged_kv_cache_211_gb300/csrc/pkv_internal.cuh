@@ -20,6 +20,21 @@ int sm_count();
 
 inline pkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
 
+// The cascade's prefix pass on the tensor cores (pkv_prefill.cu): every
+// sequence's decode query against the first prefix_blocks blocks of
+// block-table row 0, shared by all sequences; writes the unnormalised
+// partials (m, l, o, base-2 scores) of query head i of sequence s to
+// workspace row s * num_q_heads + i.  A persistent grid of at most max_ctas
+// CTAs (its size goes to *grid_out); an ordinary launch that lets the next
+// kernel on the stream start beside it.
+pkv_status launch_cascade_prefix(const void* q, const void* k_cache, const void* v_cache,
+                                 const int32_t* block_tables, int max_blocks_per_seq,
+                                 const int32_t* context_lens, int len_bound, int num_seqs,
+                                 int num_q_heads, int num_kv_heads, int head_dim, int num_blocks,
+                                 int prefix_blocks, float scale_log2, float* ws_m, float* ws_l,
+                                 float* ws_o, pkv_dtype dtype, int max_ctas, int* grid_out,
+                                 cudaStream_t stream);
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // ---------------------------------------------------------------------------

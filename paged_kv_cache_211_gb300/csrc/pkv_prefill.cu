@@ -48,6 +48,17 @@ struct PrefillParams {
     int max_q_len, num_q_rows;  // host bounds: longest chunk, rows of q and out
     int tiles_per_seq;  // ceil(max_q_len * group / kPrefillRows)
     float scale_log2;
+    // Cascade prefix mode of the tensor-core kernel (prefix_tokens > 0): the
+    // query rows are every sequence's decode query (row r of a KV head's rows:
+    // sequence r / group, query head r % group of that KV head), the keys are
+    // the shared prefix (the first prefix_tokens / 16 entries of block-table
+    // row 0), a row sees min(its length, prefix_tokens) of them, and each
+    // row's unnormalised result (m, l, o; base-2 scores) goes to workspace
+    // row sequence * num_q_heads + query head.
+    int prefix_tokens, len_bound;
+    float* ws_m;
+    float* ws_l;
+    float* ws_o;
 };
 
 // A sequence's chunk is usable if its rows lie inside q/out, it is no longer
@@ -354,7 +365,30 @@ __device__ __forceinline__ bool tc_item(const PrefillParams& p, int i, bool flag
     return true;
 }
 
-template <typename T, int D>
+// Item i of the cascade prefix mode: KV head i % num_kv_heads, tile
+// i / num_kv_heads of that head's num_seqs * group rows; every item reads all
+// prefix blocks.
+__device__ __forceinline__ bool tc_prefix_item(const PrefillParams& p, int i, TcItem& it) {
+    it.h = i % p.num_kv_heads;
+    it.row0 = (i / p.num_kv_heads) * kTcRows;
+    it.s = 0;                    // the prefix's blocks: block-table row 0
+    it.q0 = 0;                   // decode queries: row t of q is sequence t
+    it.qlen = p.num_seqs;
+    it.n = p.prefix_tokens;
+    if (it.row0 >= p.num_seqs * p.group) return false;
+    it.p_last = p.prefix_tokens - 1;
+    it.nblk = p.prefix_tokens / PKV_BLOCK_SIZE;
+    it.nkv = (it.nblk + 7) / 8;
+    return true;
+}
+
+template <bool kPrefix>
+__device__ __forceinline__ bool tc_next(const PrefillParams& p, int i, bool flag, TcItem& it) {
+    if constexpr (kPrefix) return tc_prefix_item(p, i, it);
+    return tc_item(p, i, flag, it);
+}
+
+template <typename T, int D, bool kPrefix>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v, int num_items) {
@@ -420,6 +454,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // the cascade's partition pass may be scheduled beside this grid now:
+    // the two touch disjoint memory, and the merge after them is an ordinary
+    // launch that waits for both
+    if constexpr (kPrefix) asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
     if (warp == 0 || warp == 3) {
         // ------------------------------------------------ K (warp 0) / V (warp 3) producers
@@ -432,7 +470,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         bool live = true;
         for (int i = blockIdx.x; i < num_items && live; i += gridDim.x) {
             TcItem it;
-            if (!tc_item(p, i, isk && lane == 0, it)) continue;
+            if (!tc_next<kPrefix>(p, i, isk && lane == 0, it)) continue;
             const int32_t* table = p.block_tables + (size_t)it.s * p.max_blocks_per_seq;
             for (int j = 0; j < it.nkv; ++j, ++J) {
                 const int b = J & 1, ph = (J >> 1) & 1;
@@ -471,7 +509,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int I = 0;
         for (int i = blockIdx.x; i < num_items; i += gridDim.x) {
             TcItem it;
-            if (!tc_item(p, i, false, it)) continue;
+            if (!tc_next<kPrefix>(p, i, false, it)) continue;
             const int qbuf = I & 1;
             if (!__all_sync(0xffffffffu,
                             mbar_wait(&q_empty[qbuf], ((I >> 1) & 1) ^ 1, abort_flag, p.status)))
@@ -517,7 +555,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (c.i = c.i < 0 ? (int)blockIdx.x : c.i + (int)gridDim.x; c.i < num_items;
                      c.i += gridDim.x) {
                     TcItem it;
-                    if (!tc_item(p, c.i, false, it)) continue;
+                    if (!tc_next<kPrefix>(p, c.i, false, it)) continue;
                     c.nkv = it.nkv;
                     c.j = 0;
                     ++c.I;
@@ -603,10 +641,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         bool ok = true;
         for (int i = blockIdx.x; i < num_items && ok; i += gridDim.x) {
             TcItem it;
-            if (!tc_item(p, i, false, it)) continue;
+            if (!tc_next<kPrefix>(p, i, false, it)) continue;
             const int R = it.row0 + r, t = R / g;
             const bool live_row = t < it.qlen;
-            const int pos = live_row ? it.n - it.qlen + t : -1;   // keys 0..pos are visible
+            int pos = live_row ? it.n - it.qlen + t : -1;         // keys 0..pos are visible
+            if constexpr (kPrefix) {
+                // sequence t sees the prefix up to its own length (an invalid
+                // length, flagged by the partition pass, sees nothing)
+                int n = live_row ? p.context_lens[t] : 0;
+                if (n < 0 || n > p.len_bound) n = 0;
+                pos = min(n, p.prefix_tokens) - 1;
+            }
             float m_used = -INFINITY, l = 0.f;
             for (int j = 0; j < it.nkv; ++j, ++J) {
                 const int b = J & 1, ph = (J >> 1) & 1;
@@ -744,15 +789,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             ok = __all_sync(0xffffffffu, mbar_wait(o_ready, I & 1, abort_flag, p.status));
             if (!ok) break;
             tc_fence_after();
-            T* dst = static_cast<T*>(p.out) +
-                     ((size_t)(it.q0 + (live_row ? t : 0)) * Hq + it.h * g + (R - t * g)) * D;
+            const size_t orow = (size_t)(it.q0 + (live_row ? t : 0)) * Hq + it.h * g + (R - t * g);
+            T* dst = static_cast<T*>(p.out) + orow * D;
+            if constexpr (kPrefix) {
+                // partials of this row for the cascade's merge: o relative to M
+                if (live_row) {
+                    p.ws_m[orow] = M;
+                    p.ws_l[orow] = L;
+                }
+            }
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o0[32], o1[32];
                 tc_ld32(trow + kOCol + 32 * c, o0);
                 tc_ld32(trow + kOCol + 128 + 32 * c, o1);
                 tc_wait_ld();
-                if (live_row) {
+                if constexpr (kPrefix) {
+                    if (live_row) {
+                        float4* od = reinterpret_cast<float4*>(p.ws_o + orow * D + 32 * c);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            od[e] = make_float4(
+                                __uint_as_float(o0[4 * e]) * w0 + __uint_as_float(o1[4 * e]) * w1,
+                                __uint_as_float(o0[4 * e + 1]) * w0 +
+                                    __uint_as_float(o1[4 * e + 1]) * w1,
+                                __uint_as_float(o0[4 * e + 2]) * w0 +
+                                    __uint_as_float(o1[4 * e + 2]) * w1,
+                                __uint_as_float(o0[4 * e + 3]) * w0 +
+                                    __uint_as_float(o1[4 * e + 3]) * w1);
+                    }
+                } else if (live_row) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         float v[8];
@@ -808,7 +874,7 @@ pkv_status launch_prefill(const PrefillParams& prm_in, const void* k_cache, cons
     PrefillParams prm = prm_in;
     if (use_tc_prefill()) {
         prm.tiles_per_seq = ceil_div(max_q_len * prm.group, kTcRows);
-        auto kern = prefill_tc_kernel<T, D>;
+        auto kern = prefill_tc_kernel<T, D, false>;
         const size_t smem = prefill_tc_smem<D>();
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
@@ -833,7 +899,71 @@ pkv_status launch_prefill(const PrefillParams& prm_in, const void* k_cache, cons
     return cuda_status(cudaGetLastError());
 }
 
+template <typename T, int D>
+pkv_status launch_prefix_tc(const PrefillParams& prm, const void* k_cache, const void* v_cache,
+                            int num_items, int grid, pkv_dtype dtype, cudaStream_t stream) {
+    CUtensorMap tmk, tmv;
+    if (!make_pool_map(&tmk, k_cache, prm.num_blocks, prm.num_kv_heads, D, dtype) ||
+        !make_pool_map(&tmv, v_cache, prm.num_blocks, prm.num_kv_heads, D, dtype))
+        return PKV_ERR_CUDA;
+    auto kern = prefill_tc_kernel<T, D, true>;
+    const size_t smem = prefill_tc_smem<D>();
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return PKV_ERR_CUDA;
+    kern<<<grid, kTcThreads, smem, stream>>>(prm, tmk, tmv, num_items);
+    return cuda_status(cudaGetLastError());
+}
+
 }  // namespace
+
+pkv_status launch_cascade_prefix(const void* q, const void* k_cache, const void* v_cache,
+                                 const int32_t* block_tables, int max_blocks_per_seq,
+                                 const int32_t* context_lens, int len_bound, int num_seqs,
+                                 int num_q_heads, int num_kv_heads, int head_dim, int num_blocks,
+                                 int prefix_blocks, float scale_log2, float* ws_m, float* ws_l,
+                                 float* ws_o, pkv_dtype dtype, int max_ctas, int* grid_out,
+                                 cudaStream_t stream) {
+    unsigned int* status = status_word();
+    if (!status) return PKV_ERR_CUDA;
+    const int g = num_q_heads / num_kv_heads;
+    const long long items =
+        (long long)num_kv_heads * ceil_div(num_seqs * g, kTcRows);
+    const int grid = (int)std::max<long long>(1, std::min<long long>(items, max_ctas));
+    *grid_out = grid;
+    PrefillParams prm = {};
+    prm.q = q;
+    prm.out = nullptr;
+    prm.block_tables = block_tables;
+    prm.context_lens = context_lens;
+    prm.cu_q_lens = nullptr;
+    prm.status = status;
+    prm.num_seqs = num_seqs;
+    prm.num_q_heads = num_q_heads;
+    prm.num_kv_heads = num_kv_heads;
+    prm.group = g;
+    prm.max_blocks_per_seq = max_blocks_per_seq;
+    prm.num_blocks = num_blocks;
+    prm.scale_log2 = scale_log2;
+    prm.prefix_tokens = prefix_blocks * PKV_BLOCK_SIZE;
+    prm.len_bound = len_bound;
+    prm.ws_m = ws_m;
+    prm.ws_l = ws_l;
+    prm.ws_o = ws_o;
+    if (dtype == PKV_BF16)
+        return head_dim == 128 ? launch_prefix_tc<__nv_bfloat16, 128>(prm, k_cache, v_cache,
+                                                                     (int)items, grid, dtype,
+                                                                     stream)
+                               : launch_prefix_tc<__nv_bfloat16, 64>(prm, k_cache, v_cache,
+                                                                    (int)items, grid, dtype,
+                                                                    stream);
+    return head_dim == 128
+               ? launch_prefix_tc<__half, 128>(prm, k_cache, v_cache, (int)items, grid, dtype,
+                                               stream)
+               : launch_prefix_tc<__half, 64>(prm, k_cache, v_cache, (int)items, grid, dtype,
+                                              stream);
+}
+
 }  // namespace pkv
 
 extern "C" {
@@ -877,6 +1007,9 @@ pkv_status paged_attention_prefill(const void* q, const void* k_cache, const voi
     prm.num_q_rows = num_q_rows;
     prm.tiles_per_seq = 0;  // set by the launcher for the kernel it picks
     prm.scale_log2 = scale * pkv::kLog2e;
+    prm.prefix_tokens = 0;  // prefill, not the cascade's prefix pass
+    prm.len_bound = 0;
+    prm.ws_m = prm.ws_l = prm.ws_o = nullptr;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (dtype == PKV_BF16)
         return head_dim == 128

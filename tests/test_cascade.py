@@ -10,7 +10,7 @@ import torch
 import oracle
 import paged_kv_cache_211_gb300 as pkv
 from paged_kv_cache_211_gb300 import workloads as wl
-from gpu_helpers import assert_attention_close, compact_oracle_step, dtype_code, sample_seqs
+from gpu_helpers import assert_attention_close, compact_oracle_step, dtype_code
 from pkv_testutil import bits
 
 pytestmark = pytest.mark.gpu
@@ -27,7 +27,7 @@ def test_cascade_step_on_prefix_shared_workload(cuda_device):
     w = wl.WORKLOADS["prefix_shared"]
     inp = wl.make_inputs(w, device=cuda_device, num_layers=1)
     lens = inp["context_lens_host"]
-    ids = sample_seqs(lens, 40, seed=3)
+    ids = np.arange(w.num_seqs)                 # every sequence
     want, kn_rows, _ = compact_oracle_step(inp, ids)
     max_len = int(lens.max())
     out = torch.empty_like(inp["q"])
@@ -82,11 +82,17 @@ def _shared_case(dev, dtype, lens, P, Hq, Hkv, D, seed):
             tables, np.array(lens, np.int32), kc, vc, q)
 
 
-@pytest.mark.parametrize("dtype,Hq,Hkv,D", [("bf16", 16, 8, 128), ("f16", 32, 4, 64),
-                                             ("bf16", 8, 8, 128), ("f16", 12, 4, 128)])
-def test_cascade_attention_short_and_long_sequences(dtype, Hq, Hkv, D, cuda_device):
-    P = 12                                              # 192-token prefix, two 8-block chunks
-    lens = [1, 5, 16, 100, 191, 192, 193, 250, 700, 1000, 64, 300, 2, 193]
+@pytest.mark.parametrize("dtype,Hq,Hkv,D,B", [("bf16", 16, 8, 128, 14), ("f16", 32, 4, 64, 14),
+                                               ("bf16", 8, 8, 128, 14), ("f16", 12, 4, 128, 14),
+                                               ("bf16", 24, 8, 128, 50)])
+def test_cascade_attention_short_and_long_sequences(dtype, Hq, Hkv, D, B, cuda_device):
+    """Sequences shorter than, equal to and longer than a 192-token prefix (12
+    blocks: one full and one half key tile of the prefix pass); with B = 50 and
+    3 query heads per KV head, 150 rows per KV head: two row tiles, the second
+    partly empty."""
+    P = 12
+    base = [1, 5, 16, 100, 191, 192, 193, 250, 700, 1000, 64, 300, 2, 193]
+    lens = [base[i % len(base)] + (i // len(base)) * 37 for i in range(B)]
     bt, cl, tables, ln, kc, vc, q = _shared_case(cuda_device, dtype, lens, P, Hq, Hkv, D, 17)
     code = oracle.BF16 if dtype == "bf16" else oracle.F16
     want = oracle.decode_attention(code, bits(q), bits(kc), bits(vc), tables, ln, D ** -0.5)
