@@ -846,6 +846,453 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 }
 
+// ============================================================================
+// Chunked prefill on the tensor cores, two query tiles per CTA.
+//
+// Work item: one sequence, one KV head and a pair of 128-row query tiles A
+// and B (256 consecutive (query token, query head) rows); key tiles of 128
+// tokens (8 paged blocks), the pair's key range (that of its last live row)
+// for both tiles.  A persistent CTA per SM walks the items heaviest first.
+//   warp 0   TMA-loads the K blocks of each key tile into a 2-stage ring,
+//   warp 3   the V blocks into another (and marks blocks with bad ids),
+//   warp 2   owns tensor memory and copies each tile's Q rows (cp.async) as
+//            soon as the previous item's last S of that tile is done,
+//   warp 1   (one thread) issues, per key tile J, S_A(J), S_B(J) into the
+//            tiles' score buffers and O_X += P_X(J) V(J) into their outputs
+//            in the order ... P V_A(J), S_A(J+1), P V_B(J), S_B(J+1) ..., so
+//            the tensor core works on one tile while the other's softmax runs,
+//   warps 4-7 / 8-11: the softmax of tile A / B, one thread per row holding
+//            the whole key tile: a first pass over the scores in tensor
+//            memory finds the row maximum, a second computes P and writes it
+//            as 16-bit values over the scores already read.
+// Tensor memory: S_A, S_B (128 columns each), O_A, O_B (D each).  One
+// thread issues every MMA and they run in issue order, so S_X(J) completes
+// after P V_X(J-1): when the softmax sees S_X(J), O_X holds every earlier
+// tile and may be rescaled without another wait.  O is rescaled only when a
+// row's running maximum grows by more than 2^8.  V rows no row may see (past
+// the pair's bound, in a bad block, never loaded) are zeroed before P V.
+// Every wait is bounded.
+// ============================================================================
+constexpr int kTc2Threads = 384;
+constexpr int kTc2Rows = 2 * kTcRows;   // rows per item: tiles A and B
+
+struct Tc2Item {
+    int s, h, q0, qlen, n, row0, p_last, nkv;
+};
+
+// Item i of the heaviest-first order (pairs from the end of each chunk);
+// false if it holds no rows or its sequence's lengths are invalid (flagged
+// once, by the item of pair 0, head 0).
+__device__ __forceinline__ bool tc2_item(const PrefillParams& p, int i, bool flag, Tc2Item& it) {
+    const int per_pair = p.num_seqs * p.num_kv_heads;
+    const int pair = p.tiles_per_seq - 1 - i / per_pair;
+    const int rem = i - (i / per_pair) * per_pair;
+    it.s = rem / p.num_kv_heads;
+    it.h = rem - it.s * p.num_kv_heads;
+    it.q0 = p.cu_q_lens[it.s];
+    it.qlen = p.cu_q_lens[it.s + 1] - it.q0;
+    it.n = p.context_lens[it.s];
+    if (!prefill_lengths_ok(p, it.q0, it.qlen, it.n)) {
+        if (flag && pair == 0 && it.h == 0 && it.qlen != 0) atomicOr(p.status, PKV_DEV_BAD_LENGTH);
+        return false;
+    }
+    const int g = p.group;
+    it.row0 = pair * kTc2Rows;
+    if (it.row0 >= it.qlen * g) return false;
+    const int tok_last = min(it.qlen, (it.row0 + kTc2Rows + g - 1) / g) - 1;
+    it.p_last = it.n - it.qlen + tok_last;
+    it.nkv = (it.p_last / PKV_BLOCK_SIZE + 1 + 7) / 8;
+    return true;
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kTc2Threads, 1)
+    prefill_tc2_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmap_k,
+                       const __grid_constant__ CUtensorMap tmap_v, int num_items) {
+    using E = Elem<T>;
+    constexpr int HALVES = D / 64;
+    constexpr int REG = kTcRows * 128;     // one 64-element half of 128 rows: 16 KB
+    constexpr int TILE = HALVES * REG;     // a Q tile, or one K or V key tile
+    constexpr uint32_t kCols = 512;
+    constexpr uint32_t kOCol = 2 * kTcKeys;  // O_A at kOCol, O_B at kOCol + D
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    unsigned char* sq = smem_raw + (((raw + 1023u) & ~1023u) - raw);   // Q_A, Q_B
+    unsigned char* sk = sq + 2 * TILE;      // 2 stages
+    unsigned char* sv = sk + 2 * TILE;      // 2 stages
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sv + 2 * TILE);
+    uint64_t* k_full = bars + 0;            // [stage]
+    uint64_t* k_empty = bars + 2;
+    uint64_t* v_full = bars + 4;
+    uint64_t* v_empty = bars + 6;
+    uint64_t* q_full = bars + 8;            // [tile]
+    uint64_t* q_empty = bars + 10;
+    uint64_t* s_full = bars + 12;           // [tile]: S_X(J) written
+    uint64_t* p_full = bars + 14;           // [tile]: its 4 softmax warps wrote P_X(J)
+    uint64_t* o_ready = bars + 16;          // [tile]: an item's last P V_X done
+    uint64_t* o_free = bars + 18;           // [tile]: its softmax warps read O_X
+    uint64_t* mma_idle = bars + 20;
+    int* vbad = reinterpret_cast<int*>(bars + 21);           // [2] bad-block bits per V stage
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(vbad + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = p.group, Hq = p.num_q_heads;
+
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&k_full[i], 1);
+            mbar_init(&k_empty[i], 1);
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
+            mbar_init(&q_full[i], 1);
+            mbar_init(&q_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 4);
+            mbar_init(&o_ready[i], 1);
+            mbar_init(&o_free[i], 4);
+        }
+        mbar_init(mma_idle, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    if (warp == 2) tc_alloc(tmem_slot, kCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0 || warp == 3) {
+        // ------------------------------------------------ K (warp 0) / V (warp 3) producers
+        const bool isk = warp == 0;
+        const CUtensorMap* map = isk ? &tmap_k : &tmap_v;
+        uint64_t* full = isk ? k_full : v_full;
+        uint64_t* empty = isk ? k_empty : v_empty;
+        unsigned char* ring = isk ? sk : sv;
+        int J = 0;  // key tiles issued by this CTA
+        bool live = true;
+        for (int i = blockIdx.x; i < num_items && live; i += gridDim.x) {
+            Tc2Item it;
+            if (!tc2_item(p, i, isk && lane == 0, it)) continue;
+            const int32_t* table = p.block_tables + (size_t)it.s * p.max_blocks_per_seq;
+            const int nblk = it.p_last / PKV_BLOCK_SIZE + 1;
+            for (int j = 0; j < it.nkv; ++j, ++J) {
+                const int b = J & 1, ph = (J >> 1) & 1;
+                live = __all_sync(0xffffffffu, mbar_wait(&empty[b], ph ^ 1, abort_flag, p.status));
+                if (!live) break;
+                const int nb = min(8, nblk - 8 * j);
+                int id = 0;
+                bool bad = false;
+                if (lane < nb) {
+                    id = table[8 * j + lane];
+                    bad = id < 0 || id >= p.num_blocks;
+                    if (bad) id = 0;  // fetched, then masked and zeroed
+                }
+                const unsigned badm = __ballot_sync(0xffffffffu, bad);
+                if (lane == 0) {
+                    if (isk && badm) atomicOr(p.status, PKV_DEV_BAD_BLOCK_ID);
+                    if (!isk) vbad[b] = (int)badm;
+                    mbar_arrive_expect_tx(&full[b], (uint32_t)(nb * HALVES * 2048));
+                }
+                __syncwarp();
+                if (lane < nb) {
+#pragma unroll
+                    for (int hh = 0; hh < HALVES; ++hh)
+                        tma_load_rows(ring + b * TILE + hh * REG + lane * 2048, map, &full[b],
+                                      hh * 64, it.h, id * PKV_BLOCK_SIZE);
+                }
+            }
+        }
+        // every copy issued must land before the CTA may exit
+        if (lane == 0)
+            for (int j = max(0, J - 2); j < J; ++j) mbar_drain(&full[j & 1], (j >> 1) & 1, p.status);
+    } else if (warp == 2) {
+        // ------------------------------------ Q rows of each item's two tiles (cp.async)
+        const T* qb = static_cast<const T*>(p.q);
+        constexpr int CH = D / 8;  // 16-byte chunks per row
+        int I = 0;
+        bool live = true;
+        for (int i = blockIdx.x; i < num_items && live; i += gridDim.x) {
+            Tc2Item it;
+            if (!tc2_item(p, i, false, it)) continue;
+            for (int X = 0; X < 2 && live; ++X) {
+                live = __all_sync(0xffffffffu, mbar_wait(&q_empty[X], (I & 1) ^ 1, abort_flag,
+                                                         p.status));
+                if (!live) break;
+                unsigned char* dstb = sq + X * TILE;
+                for (int x = lane; x < kTcRows * CH; x += 32) {
+                    const int r = x / CH, c = x - r * CH;
+                    const int R = it.row0 + X * kTcRows + r, t = R / g;
+                    const bool live_row = t < it.qlen;
+                    const T* src = qb + ((size_t)(it.q0 + (live_row ? t : 0)) * Hq + it.h * g +
+                                         (live_row ? R - t * g : 0)) * D + c * 8;
+                    const uint32_t dst =
+                        smem_addr(dstb + (c >> 3) * REG + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+                    // rows past the chunk are zero-filled (source size 0)
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst),
+                                 "l"(src), "r"(live_row ? 16 : 0)
+                                 : "memory");
+                }
+                asm volatile("cp.async.commit_group;\n" ::: "memory");
+                asm volatile("cp.async.wait_all;\n" ::: "memory");
+                asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&q_full[X]);
+            }
+            ++I;
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+            const uint32_t id_s = tc_idesc_f16(kBf16, kTcRows, kTcKeys, 0, 0);
+            const uint32_t id_pv = tc_idesc_f16(kBf16, kTcRows, D, 0, 1);
+            const uint32_t aq = smem_addr(sq), ak = smem_addr(sk), av = smem_addr(sv);
+            // a cursor over the key tiles of this CTA's items, in order
+            struct Cur {
+                int i, I, j, J, nkv;  // item index, items seen, key tile in item, global tile
+            };
+            auto advance = [&](Cur& c) -> bool {
+                if (c.i >= 0 && ++c.j < c.nkv) {
+                    ++c.J;
+                    return true;
+                }
+                for (c.i = c.i < 0 ? (int)blockIdx.x : c.i + (int)gridDim.x; c.i < num_items;
+                     c.i += gridDim.x) {
+                    Tc2Item it;
+                    if (!tc2_item(p, c.i, false, it)) continue;
+                    c.nkv = it.nkv;
+                    c.j = 0;
+                    ++c.I;
+                    ++c.J;
+                    return true;
+                }
+                return false;
+            };
+            // S_X(c) = Q_X K(c)^T into tile X's score buffer.  S_X(J) overwrites
+            // P_X(J-1), whose P V was issued before it by this thread (in order).
+            auto issue_s = [&](const Cur& c, int X) -> bool {
+                const int b = c.J & 1;
+                if (X == 0 && !mbar_wait(&k_full[b], (c.J >> 1) & 1, abort_flag, p.status))
+                    return false;
+                if (c.j == 0 && !mbar_wait(&q_full[X], c.I & 1, abort_flag, p.status))
+                    return false;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks)
+                    tc_mma(tmem + X * kTcKeys,
+                           tc_smem_desc(aq + X * TILE + (ks >> 2) * REG + (ks & 3) * 32, 16, 1024),
+                           tc_smem_desc(ak + b * TILE + (ks >> 2) * REG + (ks & 3) * 32, 16, 1024),
+                           id_s, ks > 0);
+                tc_commit(&s_full[X]);
+                if (X == 1) tc_commit(&k_empty[b]);                 // both tiles read K(J)
+                if (c.j == c.nkv - 1) tc_commit(&q_empty[X]);      // the item's last use of Q_X
+                return true;
+            };
+            // O_X += P_X(c) V(c): P_X over the first 64 columns of its score buffer
+            auto issue_pv = [&](const Cur& c, int X) -> bool {
+                const int b = c.J & 1;
+                if (X == 0 && !mbar_wait(&v_full[b], (c.J >> 1) & 1, abort_flag, p.status))
+                    return false;
+                // the item's first P V overwrites O_X: the last item's must have been read
+                if (c.j == 0 && c.I >= 1 &&
+                    !mbar_wait(&o_free[X], (c.I - 1) & 1, abort_flag, p.status))
+                    return false;
+                if (!mbar_wait(&p_full[X], c.J & 1, abort_flag, p.status)) return false;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kTcKeys / 16; ++kk)
+                    tc_mma_tmem_a(tmem + kOCol + X * D, tmem + X * kTcKeys + 8 * kk,
+                                  tc_smem_desc(av + b * TILE + kk * 2048, REG, 1024), id_pv,
+                                  c.j > 0 || kk > 0);
+                if (X == 1) tc_commit(&v_empty[b]);                 // both tiles read V(J)
+                if (c.j == c.nkv - 1) tc_commit(&o_ready[X]);      // O_X of the item complete
+                return true;
+            };
+            Cur cs = {-1, -1, 0, -1, 0}, cp = {-1, -1, 0, -1, 0};
+            bool live = true;
+            bool more = advance(cs);
+            if (more) live = issue_s(cs, 0) && issue_s(cs, 1);
+            while (live && advance(cp)) {
+                more = advance(cs);
+                live = issue_pv(cp, 0);
+                if (live && more) live = issue_s(cs, 0);
+                if (live) live = issue_pv(cp, 1);
+                if (live && more) live = issue_s(cs, 1);
+            }
+            // nothing of this thread's may still run when tensor memory is freed
+            tc_commit(mma_idle);
+            mbar_drain(mma_idle, 0, p.status);
+        }
+        __syncwarp();
+    } else {
+        // ---------------- softmax of tile X (warps 4-7: A, 8-11: B), one thread per row
+        const int X = (warp - 4) >> 2;
+        const int wq = warp & 3;                             // tensor-memory lane quarter
+        const int r = 32 * wq + lane;                        // row of the tile
+        const uint32_t trow = tmem + ((uint32_t)(32 * wq) << 16);
+        const uint32_t sx = trow + X * kTcKeys;              // this tile's scores / P
+        const uint32_t ox = trow + kOCol + X * D;            // this tile's O
+        const float sl2 = p.scale_log2;
+        int J = 0, I = 0;
+        bool ok = true;
+        for (int i = blockIdx.x; i < num_items && ok; i += gridDim.x) {
+            Tc2Item it;
+            if (!tc2_item(p, i, false, it)) continue;
+            const int R = it.row0 + X * kTcRows + r, t = R / g;
+            const bool live_row = t < it.qlen;
+            const int pos = live_row ? it.n - it.qlen + t : -1;   // keys 0..pos are visible
+            float m_used = -INFINITY, l = 0.f;
+            for (int j = 0; j < it.nkv; ++j, ++J) {
+                const int b = J & 1;
+                ok = __all_sync(0xffffffffu, mbar_wait(&s_full[X], J & 1, abort_flag, p.status));
+                if (!ok) break;
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(&v_full[b], (J >> 1) & 1, abort_flag, p.status));
+                if (!ok) break;
+                tc_fence_after();
+                const unsigned bad = (unsigned)vbad[b];              // 8 blocks of the tile
+                const int key0 = kTcKeys * j;
+                // tiles below every row's causal bound with no bad block need no
+                // mask: max over the raw scores, the scale goes into the exponent
+                const bool plain = __all_sync(0xffffffffu, key0 + kTcKeys - 1 <= pos) &&
+                                   bad == 0u && sl2 > 0.f;
+                const float mul = plain ? sl2 : 1.f;
+                // scaled score of key key0 + c (masked: -inf); raw for a plain tile
+                auto masked = [&](float v, int c) {
+                    const bool vis = key0 + c <= pos && !((bad >> (c >> 4)) & 1u);
+                    return vis ? v * sl2 : -INFINITY;
+                };
+                // pass 1: the row maximum of this key tile, 64 columns at a time
+                float mxp[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) mxp[e] = -INFINITY;
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    float sc[64];
+                    tc_ld32(sx + 64 * h2, reinterpret_cast<uint32_t(&)[32]>(sc[0]));
+                    tc_ld32(sx + 64 * h2 + 32, reinterpret_cast<uint32_t(&)[32]>(sc[32]));
+                    tc_wait_ld();
+                    if (plain) {
+#pragma unroll
+                        for (int c = 0; c < 64; c += 2)
+                            mxp[(c >> 1) & 7] = max3(mxp[(c >> 1) & 7], sc[c], sc[c + 1]);
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 64; ++c)
+                            mxp[c & 7] = fmaxf(mxp[c & 7], masked(sc[c], 64 * h2 + c));
+                    }
+                }
+                float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                                 fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+                if (plain) mx *= sl2;
+                const float m_new = fmaxf(m_used, mx);
+                // lazy rescale: only when the maximum grew by more than 2^kTcRescale
+                const bool grow = m_used != -INFINITY && m_new > m_used + kTcRescale;
+                const float f = grow ? fast_exp2(m_used - m_new) : 1.f;
+                if (m_used == -INFINITY || grow) m_used = m_new;
+                const float ms = m_used == -INFINITY ? 0.f : m_used;
+                if (__any_sync(0xffffffffu, grow)) {
+                    // O_X holds every earlier tile (S_X(J) completed after P V_X(J-1)):
+                    // scale it (whole warp: tensor-memory access is warp-wide)
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tc_ld32(ox + 32 * c, o);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                        tc_st32(ox + 32 * c, o);
+                    }
+                }
+                // pass 2: P, written as 16-bit pairs over the first 64 columns, 32
+                // keys at a time: P of keys 32c.. lands on columns 16c.., scores
+                // this loop has already read
+                const uint64_t mul2 = f2(mul, mul), nms2 = f2(-ms, -ms);
+                uint64_t acc2[4] = {f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f)};
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    float sc[32];
+                    tc_ld32(sx + 32 * c4, reinterpret_cast<uint32_t(&)[32]>(sc[0]));
+                    tc_wait_ld();
+                    if (!plain) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) sc[e] = masked(sc[e], 32 * c4 + e);
+                    }
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        float a0, a1;
+                        f2_split(f2_fma(f2(sc[2 * e], sc[2 * e + 1]), mul2, nms2), a0, a1);
+                        const float p0 = fast_exp2(a0), p1 = fast_exp2(a1);
+                        acc2[e & 3] = f2_add(acc2[e & 3], f2(p0, p1));
+                        pk[e] = E::pack(p0, p1);
+                    }
+                    tc_st16(sx + 16 * c4, pk);
+                }
+                float psp[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) f2_split(acc2[e], psp[2 * e], psp[2 * e + 1]);
+                const float psum = ((psp[0] + psp[1]) + (psp[2] + psp[3])) +
+                                   ((psp[4] + psp[5]) + (psp[6] + psp[7]));
+                tc_wait_st();
+                l = l * f + psum;
+                // V rows no row of the pair may see must be finite zeros before
+                // P V (0 x NaN = NaN); both tiles zero the same rows
+                if (j == it.nkv - 1 || bad) {
+                    unsigned char* vt = sv + b * TILE;
+                    for (int x = r; x < kTcKeys * 8 * HALVES; x += kTcRows) {
+                        const int kq = x / (8 * HALVES), rest = x - kq * (8 * HALVES);
+                        if (key0 + kq <= it.p_last && !((bad >> (kq >> 4)) & 1u)) continue;
+                        *reinterpret_cast<uint4*>(vt + (rest >> 3) * REG + kq * 128 +
+                                                  ((rest & 7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+                tc_fence_before();  // P and a rescaled O are ordered before the next MMA
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[X]);
+            }
+            if (!ok) break;
+            // epilogue: O_X / l for the live rows
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            ok = __all_sync(0xffffffffu, mbar_wait(&o_ready[X], I & 1, abort_flag, p.status));
+            if (!ok) break;
+            tc_fence_after();
+            T* dst = static_cast<T*>(p.out) +
+                     ((size_t)(it.q0 + (live_row ? t : 0)) * Hq + it.h * g +
+                      (live_row ? R - t * g : 0)) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tc_ld32(ox + 32 * c, o);
+                tc_wait_ld();
+                if (live_row) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float v[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) v[u] = __uint_as_float(o[8 * e + u]) * inv;
+                        *reinterpret_cast<uint4*>(dst + 32 * c + 8 * e) =
+                            make_uint4(E::pack(v[0], v[1]), E::pack(v[2], v[3]),
+                                       E::pack(v[4], v[5]), E::pack(v[6], v[7]));
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&o_free[X]);
+            ++I;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after();
+        tc_dealloc(tmem, kCols);
+    }
+}
+
 template <int D>
 size_t prefill_tc_smem() {
     // 2 Q buffers, 2 K and 2 V stages, barriers and the (m, l) hand-over
@@ -853,14 +1300,19 @@ size_t prefill_tc_smem() {
     return 1024 + (size_t)6 * (D / 64) * kTcRows * 128 + 2048;
 }
 
-// Which prefill kernel runs: the tcgen05 one unless PKV_PREFILL_KERNEL=mma
-// selects the mma.sync kernel (kept for comparison).
-bool use_tc_prefill() {
-    static const bool tc = [] {
+// Which prefill kernel runs: the tcgen05 kernel with two query tiles per CTA,
+// unless PKV_PREFILL_KERNEL selects one kept for comparison: =tc1 the
+// tcgen05 kernel with one query tile and two softmax groups per key tile
+// (also the cascade's prefix pass), =mma the mma.sync kernel.  Returns 1
+// for two tiles, 2 for one tile, 0 for mma.sync.
+int prefill_kernel_choice() {
+    static const int k = [] {
         const char* v = std::getenv("PKV_PREFILL_KERNEL");
-        return !(v && std::strcmp(v, "mma") == 0);
+        if (v && std::strcmp(v, "mma") == 0) return 0;
+        if (v && std::strcmp(v, "tc1") == 0) return 2;
+        return 1;
     }();
-    return tc;
+    return k;
 }
 
 template <typename T, int D>
@@ -872,7 +1324,23 @@ pkv_status launch_prefill(const PrefillParams& prm_in, const void* k_cache, cons
         !make_pool_map(&tmv, v_cache, num_blocks, num_kv_heads, D, dtype))
         return PKV_ERR_CUDA;
     PrefillParams prm = prm_in;
-    if (use_tc_prefill()) {
+    const int choice = prefill_kernel_choice();
+    if (choice == 1) {
+        prm.tiles_per_seq = ceil_div(max_q_len * prm.group, kTc2Rows);  // pairs of tiles
+        auto kern = prefill_tc2_kernel<T, D>;
+        const size_t smem = prefill_tc_smem<D>();
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return PKV_ERR_CUDA;
+        const long long items = (long long)prm.num_seqs * num_kv_heads * prm.tiles_per_seq;
+        if (items > 0x7fffffffll) return PKV_ERR_UNSUPPORTED;
+        const int sms = sm_count();
+        if (sms <= 0) return PKV_ERR_CUDA;
+        const int grid = (int)std::min<long long>(items, sms);  // persistent: one CTA per SM
+        kern<<<grid, kTc2Threads, smem, stream>>>(prm, tmk, tmv, (int)items);
+        return cuda_status(cudaGetLastError());
+    }
+    if (choice == 2) {
         prm.tiles_per_seq = ceil_div(max_q_len * prm.group, kTcRows);
         auto kern = prefill_tc_kernel<T, D, false>;
         const size_t smem = prefill_tc_smem<D>();

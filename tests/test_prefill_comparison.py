@@ -1,5 +1,7 @@
-"""The mma.sync prefill kernel kept for comparison (PKV_PREFILL_KERNEL=mma),
-checked against the oracle in a child process (GPU)."""
+"""The prefill kernels kept for comparison (PKV_PREFILL_KERNEL=tc1: the
+tcgen05 kernel with one query tile per CTA, which also serves the cascade's
+prefix pass; =mma: the mma.sync kernel), each checked against the oracle in a
+child process (GPU)."""
 import os
 import subprocess
 import sys
@@ -11,8 +13,9 @@ pytestmark = pytest.mark.gpu
 HERE = os.path.dirname(os.path.abspath(__file__))
 
 
-def test_prefill_comparison_kernel(cuda_device):
-    env = dict(os.environ, PKV_PREFILL_KERNEL="mma")
+@pytest.mark.parametrize("kernel", ["tc1", "mma"])
+def test_prefill_comparison_kernel(kernel, cuda_device):
+    env = dict(os.environ, PKV_PREFILL_KERNEL=kernel)
     env["PYTHONPATH"] = os.pathsep.join([HERE, os.path.dirname(HERE), env.get("PYTHONPATH", "")])
     r = subprocess.run([sys.executable, os.path.join(HERE, "prefill_case_check.py")], env=env,
                        capture_output=True, text=True, timeout=600)
