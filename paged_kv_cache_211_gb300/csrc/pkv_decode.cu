@@ -618,16 +618,20 @@ constexpr int kTmaConsumers = 8;
 __host__ __device__ constexpr int tma_threads(bool self_feed) { return (kTmaConsumers + (self_feed ? 0 : 1)) * 32; }
 constexpr int kTmaItemsPerCta = 8;
 constexpr int kTmaMaxStages = 8;
-template <typename T, int D, bool kOneHead, bool kSelfFeed>
+template <typename T, int D, bool kOneHead, bool kSelfFeed, int kHPC = 1>
 __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
     decode_partition_tma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
                                 const __grid_constant__ CUtensorMap tmap_v, int nstages,
                                 int heads_per_item) {
+    // kHPC: KV heads each consumer warp serves per block.  2 (D = 64 items of
+    // two heads, producer warp only): a stage holds both heads' tiles, so a
+    // consumer step moves 8 KB, as one head does at D = 128.
+    static_assert(kHPC == 1 || (kHPC == 2 && !kSelfFeed && !kOneHead), "two heads per consumer");
     using E = Elem<T>;
     constexpr int NC = kTmaConsumers;
     constexpr int HALVES = D / 64;
-    constexpr int TILE = 16 * D * 2;   // one K or V tile: 16 rows x D
-    constexpr int STAGE = 2 * TILE;    // K tile, then V tile
+    constexpr int TILE = 16 * D * 2;      // one K or V tile: 16 rows x D
+    constexpr int STAGE = 2 * kHPC * TILE;  // K tiles of the consumer's heads, then V tiles
     constexpr int KS = D / 16;         // k-steps of the score MMA = row tiles of O^T
     constexpr int DP = D + 4;          // padded rows of the merge buffer
     extern __shared__ unsigned char smem_raw[];
@@ -742,12 +746,13 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
     // An item is one partition of one sequence and a group of HPI KV heads
     // (HPI = 1: one head; HPI = Hkv: all heads, so a block's heads -- one
     // contiguous run of the pool -- are fetched together).  Consumer warp w
-    // serves head hg*HPI + w % HPI of the item and every CPH-th block of it,
-    // CPH = NC / HPI consumers per head.
+    // serves heads hg*HPI + (w % CPB)*kHPC + e, e < kHPC, of the item and every
+    // CPH-th block of it, CPB = HPI / kHPC, CPH = NC / CPB.
     const int HPI = kOneHead ? 1 : heads_per_item;  // a constant in the one-head build
     const int groups = Hkv / HPI;
     const int total_items = total_parts * groups;
-    const int CPH = NC / HPI;
+    const int CPB = HPI / kHPC;   // consumers per block: one per kHPC heads of the item
+    const int CPH = NC / CPB;     // a consumer takes every CPH-th block of the item
     // A work item: blocks [lo, hi) of sequence s for head group hg.  dest < 0:
     // the item is the whole of its (sequence, group) and writes the output;
     // else its partials go to workspace rows dest + (query head within group).
@@ -843,23 +848,24 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
     constexpr bool self_feed = kSelfFeed;
     if (!self_feed && warp == NC) {
         // ------------------------------------------------------------ producer
-        // Batches of BB blocks x HPI heads, lane t issuing (block jb + t / HPI,
-        // head t % HPI of the group) for consumer t % HPI + HPI * ((block - lo) % CPH).  A batch
-        // gives each consumer at most min(4, nstages) blocks, so no lane ever
-        // waits for a slot another lane of this warp has yet to fill: every
-        // wait is on a consumer warp, never on a diverged lane of this one.
+        // Batches of BB blocks x CPB consumers' heads, lane t issuing (block
+        // jb + t / CPB, heads slot t % CPB of the group) for consumer t % CPB +
+        // CPB * ((block - lo) % CPH).  A batch gives each consumer at most
+        // min(4, nstages) blocks, so no lane ever waits for a slot another lane
+        // of this warp has yet to fill: every wait is on a consumer warp, never
+        // on a diverged lane of this one.
         const int per = min(4, nstages);
         const int BB = CPH * per;               // blocks per batch (a multiple of CPH)
         // lane-constant roles (no division inside the loops)
-        const int bi = lane / HPI;              // this lane's block in a batch
-        const int hl = lane - bi * HPI;         // and head within the group
-        const int wl = hl + HPI * (bi % CPH);   // the consumer it feeds
+        const int bi = lane / CPB;              // this lane's block in a batch
+        const int hl = lane - bi * CPB;         // and heads slot within the group
+        const int wl = hl + CPB * (bi % CPH);   // the consumer it feeds
         const int uoff = bi / CPH;              // its stage offset within the batch
         int pc[NC], subv[NC];  // stages issued so far per consumer; consumer's block phase
 #pragma unroll
         for (int v = 0; v < NC; ++v) {
             pc[v] = 0;
-            subv[v] = v / HPI;
+            subv[v] = v / CPB;
         }
         // table entry of this lane's block in the batch starting at jb (-1: none / bad)
         auto lane_id = [&](const int32_t* table, int jb, int hi) {
@@ -875,7 +881,7 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
         Item it;
         while (next_item(cur, it)) {
             const int32_t* table = p.block_tables + (size_t)it.s * p.max_blocks_per_seq;
-            const int h = it.hg * HPI + hl;
+            const int h = it.hg * HPI + hl * kHPC;  // the lane's first head
             int id_cur = bi < BB ? lane_id(table, it.lo, it.hi) : -1;
             for (int jb = it.lo; jb < it.hi; jb += BB) {
                 const int cnt = min(BB, it.hi - jb);   // blocks in this batch
@@ -897,10 +903,14 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
                         unsigned char* st = ring + (size_t)k * STAGE;
                         const int row = (id < 0 ? 0 : id) * PKV_BLOCK_SIZE;
 #pragma unroll
-                        for (int hh = 0; hh < HALVES; ++hh) {
-                            tma_load_rows(st + hh * 2048, &tmap_k, &full[k], hh * 64, h, row);
-                            tma_load_rows(st + TILE + hh * 2048, &tmap_v, &full[k], hh * 64, h,
-                                          row);
+                        for (int e = 0; e < kHPC; ++e) {
+#pragma unroll
+                            for (int hh = 0; hh < HALVES; ++hh) {
+                                tma_load_rows(st + e * TILE + hh * 2048, &tmap_k, &full[k],
+                                              hh * 64, h + e, row);
+                                tma_load_rows(st + (kHPC + e) * TILE + hh * 2048, &tmap_v,
+                                              &full[k], hh * 64, h + e, row);
+                            }
                         }
                     }
                 }
@@ -935,7 +945,7 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
     // (item, block) give the blocks to fetch and the blocks to consume.
     // Otherwise the producer warp above fills the rings.
     const int w = warp;
-    const int hl = w % HPI, sub = w / HPI;  // this consumer's head in the group, block phase
+    const int hl = w % CPB, sub = w / CPB;  // this consumer's heads slot in the group, block phase
     struct Stream {
         Cursor c;
         Item it;
@@ -1029,23 +1039,30 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
     Item it;
     while (next_item(cur, it)) {
         const int s = it.s, n = it.n;
-        const int h = it.hg * HPI + hl;
-        // q fragment: column gid of the score MMA is query head h*g + gid
-        uint32_t qf[KS][2];
-        {
+        const int h = it.hg * HPI + hl * kHPC;  // this consumer's first head
+        // q fragments: column gid of head e's score MMA is query head (h+e)*g + gid
+        uint32_t qf[kHPC][KS][2];
+#pragma unroll
+        for (int e = 0; e < kHPC; ++e) {
             const bool live = gid < g;
-            const T* qrow = q + ((size_t)s * Hq + (size_t)h * g + (live ? gid : 0)) * D;
+            const T* qrow = q + ((size_t)s * Hq + (size_t)(h + e) * g + (live ? gid : 0)) * D;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
-                qf[ks][0] = live ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * tig) : 0u;
-                qf[ks][1] =
+                qf[e][ks][0] =
+                    live ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * tig) : 0u;
+                qf[e][ks][1] =
                     live ? *reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 8 + 2 * tig) : 0u;
             }
         }
-        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-        float o[KS][4];
+        float m0[kHPC], m1[kHPC], l0[kHPC], l1[kHPC];
+        float o[kHPC][KS][4];
 #pragma unroll
-        for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+        for (int e = 0; e < kHPC; ++e) {
+            m0[e] = m1[e] = -INFINITY;
+            l0[e] = l1[e] = 0.f;
+#pragma unroll
+            for (int i = 0; i < KS; ++i) o[e][i][0] = o[e][i][1] = o[e][i][2] = o[e][i][3] = 0.f;
+        }
 
         const bool writes = p.k_new != nullptr && n > 0;
         const int last_blk = writes ? it.nblk - 1 : -1;
@@ -1062,18 +1079,22 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
             const int nv = id < 0 ? 0 : min(PKV_BLOCK_SIZE, n - j * PKV_BLOCK_SIZE);
             if (j == last_blk) {
                 // this step's token: not in the cache yet; patch it into the
-                // stage from k_new / v_new and store it into its slot
+                // stage from k_new / v_new and store it into its slot (lane:
+                // head e, K or V, 16-byte chunk c)
                 if (id >= 0) {
                     constexpr int CH = D / 8;
-                    if (lane < 2 * CH) {
-                        const bool isv = lane >= CH;
-                        const int c = isv ? lane - CH : lane;
+                    static_assert(2 * CH * kHPC <= 32, "one lane per chunk");
+                    if (lane < 2 * CH * kHPC) {
+                        const int e = lane / (2 * CH), r2 = lane - e * 2 * CH;
+                        const bool isv = r2 >= CH;
+                        const int c = isv ? r2 - CH : r2;
                         const T* src = static_cast<const T*>(isv ? p.v_new : p.k_new) +
-                                       ((size_t)s * Hkv + h) * D + c * 8;
+                                       ((size_t)s * Hkv + h + e) * D + c * 8;
                         const uint4 v = *reinterpret_cast<const uint4*>(src);
-                        *reinterpret_cast<uint4*>(st + (isv ? TILE : 0) + swz(rnew, c)) = v;
+                        *reinterpret_cast<uint4*>(st + ((isv ? kHPC : 0) + e) * TILE +
+                                                  swz(rnew, c)) = v;
                         T* dst = (isv ? vbase_w : kbase_w) +
-                                 ((size_t)id * PKV_BLOCK_SIZE + rnew) * row_stride + c * 8;
+                                 ((size_t)id * PKV_BLOCK_SIZE + rnew) * row_stride + e * D + c * 8;
                         *reinterpret_cast<uint4*>(dst) = v;
                     }
                     // the stage is refilled by the async proxy after release
@@ -1083,154 +1104,167 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
                 if (p.slot_out && h == 0 && lane == 0)
                     p.slot_out[s] = id >= 0 ? (int64_t)id * PKV_BLOCK_SIZE + rnew : -1;
             }
-            uint32_t kf[KS][4], vf[KS][4];
-            if (ok) {
-                const uint32_t kt = smem_addr(st), vt = kt + TILE;
+            // head by head: its fragments into registers, then (after the last
+            // head's) the slot goes back to the producer or is refilled with the
+            // block nstages ahead (the async-proxy copy after the warp's reads)
 #pragma unroll
-                for (int ks = 0; ks < KS; ++ks) {
-                    const int row = lane & 15;
-                    ldsm_x4(kf[ks], kt + swz(row, 2 * ks + (lane >> 4)));
-                    const int mi = lane >> 3;
-                    const int tok = (lane & 7) + 8 * (mi >> 1);
-                    ldsm_x4_trans(vf[ks], vt + swz(tok, 2 * ks + (mi & 1)));
+            for (int e = 0; e < kHPC; ++e) {
+                uint32_t kf[KS][4], vf[KS][4];
+                if (ok) {
+                    const uint32_t kt = smem_addr(st) + e * TILE;
+                    const uint32_t vt = smem_addr(st) + (kHPC + e) * TILE;
+#pragma unroll
+                    for (int ks = 0; ks < KS; ++ks) {
+                        const int row = lane & 15;
+                        ldsm_x4(kf[ks], kt + swz(row, 2 * ks + (lane >> 4)));
+                        const int mi = lane >> 3;
+                        const int tok = (lane & 7) + 8 * (mi >> 1);
+                        ldsm_x4_trans(vf[ks], vt + swz(tok, 2 * ks + (mi & 1)));
+                    }
                 }
-            }
-            // the fragments are in registers: release the slot to the
-            // producer, or refill it with the block nstages ahead (the
-            // async-proxy copy after the warp's reads)
-            if constexpr (kSelfFeed) {
-                asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-                __syncwarp();
-                if (ok) fetch_next(); else feeding = false;
-            } else {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[k]);
-            }
-            if (!ok || nv == 0) continue;
+                if (e == kHPC - 1) {
+                    if constexpr (kSelfFeed) {
+                        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+                        __syncwarp();
+                        if (ok) fetch_next(); else feeding = false;
+                    } else {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&empty[k]);
+                    }
+                }
+                if (!ok || nv == 0) continue;
 
-            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+                float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int ks = 0; ks < KS; ks += 2) {
-                E::mma(sa, kf[ks][0], kf[ks][1], kf[ks][2], kf[ks][3], qf[ks][0], qf[ks][1]);
-                E::mma(sb, kf[ks + 1][0], kf[ks + 1][1], kf[ks + 1][2], kf[ks + 1][3],
-                       qf[ks + 1][0], qf[ks + 1][1]);
-            }
-            float s0 = (sa[0] + sb[0]) * p.scale_log2, s1 = (sa[1] + sb[1]) * p.scale_log2;
-            float s2 = (sa[2] + sb[2]) * p.scale_log2, s3 = (sa[3] + sb[3]) * p.scale_log2;
-            if (nv < PKV_BLOCK_SIZE) {  // partial last block: select, never weight
-                if (gid >= nv) s0 = s1 = -INFINITY;
-                if (gid + 8 >= nv) s2 = s3 = -INFINITY;
-                const uint32_t mlo = (2 * tig < nv ? 0x0000ffffu : 0u) |
-                                     (2 * tig + 1 < nv ? 0xffff0000u : 0u);
-                const uint32_t mhi = (2 * tig + 8 < nv ? 0x0000ffffu : 0u) |
-                                     (2 * tig + 9 < nv ? 0xffff0000u : 0u);
+                for (int ks = 0; ks < KS; ks += 2) {
+                    E::mma(sa, kf[ks][0], kf[ks][1], kf[ks][2], kf[ks][3], qf[e][ks][0],
+                           qf[e][ks][1]);
+                    E::mma(sb, kf[ks + 1][0], kf[ks + 1][1], kf[ks + 1][2], kf[ks + 1][3],
+                           qf[e][ks + 1][0], qf[e][ks + 1][1]);
+                }
+                float s0 = (sa[0] + sb[0]) * p.scale_log2, s1 = (sa[1] + sb[1]) * p.scale_log2;
+                float s2 = (sa[2] + sb[2]) * p.scale_log2, s3 = (sa[3] + sb[3]) * p.scale_log2;
+                if (nv < PKV_BLOCK_SIZE) {  // partial last block: select, never weight
+                    if (gid >= nv) s0 = s1 = -INFINITY;
+                    if (gid + 8 >= nv) s2 = s3 = -INFINITY;
+                    const uint32_t mlo = (2 * tig < nv ? 0x0000ffffu : 0u) |
+                                         (2 * tig + 1 < nv ? 0xffff0000u : 0u);
+                    const uint32_t mhi = (2 * tig + 8 < nv ? 0x0000ffffu : 0u) |
+                                         (2 * tig + 9 < nv ? 0xffff0000u : 0u);
+#pragma unroll
+                    for (int i = 0; i < KS; ++i) {
+                        vf[i][0] &= mlo;
+                        vf[i][1] &= mlo;
+                        vf[i][2] &= mhi;
+                        vf[i][3] &= mhi;
+                    }
+                }
+                float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                }
+                const float mn0 = fmaxf(m0[e], mx0), mn1 = fmaxf(m1[e], mx1);
+                const float ms0 = mn0 == -INFINITY ? 0.f : mn0;
+                const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
+                const float c0 = fast_exp2(m0[e] - ms0), c1 = fast_exp2(m1[e] - ms1);
+                const float p0 = fast_exp2(s0 - ms0), p1 = fast_exp2(s1 - ms1);
+                const float p2 = fast_exp2(s2 - ms0), p3 = fast_exp2(s3 - ms1);
+                l0[e] = l0[e] * c0 + p0 + p2;
+                l1[e] = l1[e] * c1 + p1 + p3;
+                m0[e] = mn0;
+                m1[e] = mn1;
 #pragma unroll
                 for (int i = 0; i < KS; ++i) {
-                    vf[i][0] &= mlo;
-                    vf[i][1] &= mlo;
-                    vf[i][2] &= mhi;
-                    vf[i][3] &= mhi;
+                    o[e][i][0] *= c0;
+                    o[e][i][1] *= c1;
+                    o[e][i][2] *= c0;
+                    o[e][i][3] *= c1;
                 }
-            }
-            float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+                const uint32_t pt = movmatrix_trans(E::pack(p0, p1));
+                const uint32_t pbt = movmatrix_trans(E::pack(p2, p3));
 #pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                for (int i = 0; i < KS; ++i)
+                    E::mma(o[e][i], vf[i][0], vf[i][1], vf[i][2], vf[i][3], pt, pbt);
             }
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float ms0 = mn0 == -INFINITY ? 0.f : mn0;
-            const float ms1 = mn1 == -INFINITY ? 0.f : mn1;
-            const float c0 = fast_exp2(m0 - ms0), c1 = fast_exp2(m1 - ms1);
-            const float p0 = fast_exp2(s0 - ms0), p1 = fast_exp2(s1 - ms1);
-            const float p2 = fast_exp2(s2 - ms0), p3 = fast_exp2(s3 - ms1);
-            l0 = l0 * c0 + p0 + p2;
-            l1 = l1 * c1 + p1 + p3;
-            m0 = mn0;
-            m1 = mn1;
-#pragma unroll
-            for (int i = 0; i < KS; ++i) {
-                o[i][0] *= c0;
-                o[i][1] *= c1;
-                o[i][2] *= c0;
-                o[i][3] *= c1;
-            }
-            const uint32_t pt = movmatrix_trans(E::pack(p0, p1));
-            const uint32_t pbt = movmatrix_trans(E::pack(p2, p3));
-#pragma unroll
-            for (int i = 0; i < KS; ++i)
-                E::mma(o[i], vf[i][0], vf[i][1], vf[i][2], vf[i][3], pt, pbt);
         }
 
-        // combine the consumer warps of this item (named barrier: consumers only)
+        // combine the consumer warps of this item (named barrier: consumers
+        // only), one round per head a consumer serves
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-        }
-        float* mo = sm_o + w * g * DP;  // rows of the g live query heads only
-        const bool live0 = 2 * tig < g, live1 = 2 * tig + 1 < g;
+        for (int e = 0; e < kHPC; ++e) {
 #pragma unroll
-        for (int i = 0; i < KS; ++i) {
-            if (live0) {
-                mo[(2 * tig) * DP + 16 * i + gid] = o[i][0];
-                mo[(2 * tig) * DP + 16 * i + 8 + gid] = o[i][2];
+            for (int off = 4; off < 32; off <<= 1) {
+                l0[e] += __shfl_xor_sync(0xffffffffu, l0[e], off);
+                l1[e] += __shfl_xor_sync(0xffffffffu, l1[e], off);
             }
-            if (live1) {
-                mo[(2 * tig + 1) * DP + 16 * i + gid] = o[i][1];
-                mo[(2 * tig + 1) * DP + 16 * i + 8 + gid] = o[i][3];
-            }
-        }
-        if (gid == 0) {
-            sm_m[w * kMaxGroup + 2 * tig] = m0;
-            sm_m[w * kMaxGroup + 2 * tig + 1] = m1;
-            sm_l[w * kMaxGroup + 2 * tig] = l0;
-            sm_l[w * kMaxGroup + 2 * tig + 1] = l1;
-        }
-        asm volatile("bar.sync 1, %0;\n" ::"r"(NC * 32) : "memory");
-        constexpr int SL = D / 8;
-        // one thread per (KV head, query head of its group, 8-wide slice of D),
-        // merging the CPH consumers of that KV head
-        for (int x = tid; x < HPI * g * SL; x += NC * 32) {
-            const int hk = x / (g * SL);  // head within the group
-            const int hh = (x / SL) % g, d0 = (x % SL) * 8;
-            float M = -INFINITY;
-            for (int c = 0; c < CPH; ++c) M = fmaxf(M, sm_m[(hk + HPI * c) * kMaxGroup + hh]);
-            const float Ms = M == -INFINITY ? 0.f : M;
-            float L = 0.f;
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            for (int c = 0; c < CPH; ++c) {
-                const int v = hk + HPI * c;
-                const float e = fast_exp2(sm_m[v * kMaxGroup + hh] - Ms);
-                L += e * sm_l[v * kMaxGroup + hh];
-                const float* src = sm_o + (v * g + hh) * DP + d0;
-                const float4 u = *reinterpret_cast<const float4*>(src);
-                const float4 u2 = *reinterpret_cast<const float4*>(src + 4);
-                acc[0] += e * u.x; acc[1] += e * u.y; acc[2] += e * u.z; acc[3] += e * u.w;
-                acc[4] += e * u2.x; acc[5] += e * u2.y; acc[6] += e * u2.z; acc[7] += e * u2.w;
-            }
-            const int qh = (it.hg * HPI + hk) * g + hh;
-            if (it.dest < 0) {
-                const float inv = L > 0.f ? 1.f / L : 0.f;
-                uint4 packed;
-                packed.x = E::pack(acc[0] * inv, acc[1] * inv);
-                packed.y = E::pack(acc[2] * inv, acc[3] * inv);
-                packed.z = E::pack(acc[4] * inv, acc[5] * inv);
-                packed.w = E::pack(acc[6] * inv, acc[7] * inv);
-                *reinterpret_cast<uint4*>(static_cast<T*>(p.out) + ((size_t)s * Hq + qh) * D +
-                                          d0) = packed;
-            } else {
-                const size_t row = (size_t)it.dest + hk * g + hh;
-                float* dst = p.ws_o + row * D + d0;
-                *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
-                if (d0 == 0) {
-                    p.ws_m[row] = M;
-                    p.ws_l[row] = L;
+            float* mo = sm_o + w * g * DP;  // rows of the g live query heads only
+            const bool live0 = 2 * tig < g, live1 = 2 * tig + 1 < g;
+#pragma unroll
+            for (int i = 0; i < KS; ++i) {
+                if (live0) {
+                    mo[(2 * tig) * DP + 16 * i + gid] = o[e][i][0];
+                    mo[(2 * tig) * DP + 16 * i + 8 + gid] = o[e][i][2];
+                }
+                if (live1) {
+                    mo[(2 * tig + 1) * DP + 16 * i + gid] = o[e][i][1];
+                    mo[(2 * tig + 1) * DP + 16 * i + 8 + gid] = o[e][i][3];
                 }
             }
+            if (gid == 0) {
+                sm_m[w * kMaxGroup + 2 * tig] = m0[e];
+                sm_m[w * kMaxGroup + 2 * tig + 1] = m1[e];
+                sm_l[w * kMaxGroup + 2 * tig] = l0[e];
+                sm_l[w * kMaxGroup + 2 * tig + 1] = l1[e];
+            }
+            asm volatile("bar.sync 1, %0;\n" ::"r"(NC * 32) : "memory");
+            constexpr int SL = D / 8;
+            // one thread per (KV head of this round, query head of its group,
+            // 8-wide slice of D), merging the CPH consumers that hold that head:
+            // consumer v holds heads hg*HPI + (v % CPB)*kHPC + e
+            for (int x = tid; x < CPB * g * SL; x += NC * 32) {
+                const int slot = x / (g * SL);  // heads slot within the group
+                const int hk = slot * kHPC + e;  // head within the group
+                const int hh = (x / SL) % g, d0 = (x % SL) * 8;
+                float M = -INFINITY;
+                for (int c = 0; c < CPH; ++c) M = fmaxf(M, sm_m[(slot + CPB * c) * kMaxGroup + hh]);
+                const float Ms = M == -INFINITY ? 0.f : M;
+                float L = 0.f;
+                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                for (int c = 0; c < CPH; ++c) {
+                    const int v = slot + CPB * c;
+                    const float ew = fast_exp2(sm_m[v * kMaxGroup + hh] - Ms);
+                    L += ew * sm_l[v * kMaxGroup + hh];
+                    const float* src = sm_o + (v * g + hh) * DP + d0;
+                    const float4 u = *reinterpret_cast<const float4*>(src);
+                    const float4 u2 = *reinterpret_cast<const float4*>(src + 4);
+                    acc[0] += ew * u.x; acc[1] += ew * u.y; acc[2] += ew * u.z; acc[3] += ew * u.w;
+                    acc[4] += ew * u2.x; acc[5] += ew * u2.y; acc[6] += ew * u2.z; acc[7] += ew * u2.w;
+                }
+                const int qh = (it.hg * HPI + hk) * g + hh;
+                if (it.dest < 0) {
+                    const float inv = L > 0.f ? 1.f / L : 0.f;
+                    uint4 packed;
+                    packed.x = E::pack(acc[0] * inv, acc[1] * inv);
+                    packed.y = E::pack(acc[2] * inv, acc[3] * inv);
+                    packed.z = E::pack(acc[4] * inv, acc[5] * inv);
+                    packed.w = E::pack(acc[6] * inv, acc[7] * inv);
+                    *reinterpret_cast<uint4*>(static_cast<T*>(p.out) + ((size_t)s * Hq + qh) * D +
+                                              d0) = packed;
+                } else {
+                    const size_t row = (size_t)it.dest + hk * g + hh;
+                    float* dst = p.ws_o + row * D + d0;
+                    *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                    *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+                    if (d0 == 0) {
+                        p.ws_m[row] = M;
+                        p.ws_l[row] = L;
+                    }
+                }
+            }
+            asm volatile("bar.sync 1, %0;\n" ::"r"(NC * 32) : "memory");
         }
-        asm volatile("bar.sync 1, %0;\n" ::"r"(NC * 32) : "memory");
     }
     // every copy this warp issued must land before the CTA may exit: wait for
     // the last use issued into each of its slots (normally already consumed)
@@ -1426,17 +1460,30 @@ size_t tma_fixed_smem(int head_dim, int num_seqs, int group) {
            (size_t)(2 * num_seqs + 1) * 4;
 }
 
-size_t tma_stage_smem(int head_dim) {
-    // one K and one V tile, two mbarriers, a block id and a use count, per consumer
-    return (size_t)kTmaConsumers * (2 * 16 * head_dim * 2 + 2 * 8 + 4 + 4);
+size_t tma_stage_smem(int head_dim, int heads_per_consumer = 1) {
+    // K and V tiles of the consumer's heads, two mbarriers, a block id and a
+    // use count, per consumer
+    return (size_t)kTmaConsumers *
+           (2 * (size_t)heads_per_consumer * 16 * head_dim * 2 + 2 * 8 + 4 + 4);
 }
 
 // Stages per consumer ring that fit in the opt-in shared memory (0 if < 2).
-int tma_stages(int head_dim, int num_seqs, int group) {
+int tma_stages(int head_dim, int num_seqs, int group, int heads_per_consumer = 1) {
     const long long room =
         (long long)smem_optin_bytes() - (long long)tma_fixed_smem(head_dim, num_seqs, group);
-    const long long ns = room / (long long)tma_stage_smem(head_dim);
+    const long long ns = room / (long long)tma_stage_smem(head_dim, heads_per_consumer);
     return ns < 2 ? 0 : (int)std::min<long long>(ns, kTmaMaxStages);
+}
+
+// Consumers serve two heads per block (kHPC = 2) for items of two D = 64 heads
+// on the producer warp, unless PKV_TWO_HEADS=0 (one head each, kept for
+// comparison runs).
+bool two_heads_per_consumer() {
+    static const bool on = [] {
+        const char* v = std::getenv("PKV_TWO_HEADS");
+        return !(v && std::strcmp(v, "0") == 0);
+    }();
+    return on;
 }
 
 // KV heads per TMA item.  One head per item keeps each consumer's share of a
@@ -1468,7 +1515,8 @@ int tma_heads_per_item(int num_seqs, int max_blocks, int num_kv_heads, int head_
     if (even) {
         // an even split walks one head group of a sequence at a time: fetch
         // at least 256 contiguous bytes of each row (one D = 64 head is 128;
-        // measured 1.17x faster with two heads per item there)
+        // measured 1.17x faster with two heads per item there; four heads, the
+        // whole row, measured no faster)
         int h = std::max(1, 128 / head_dim);
         while (h < num_kv_heads && !valid(h)) ++h;
         return valid(h) ? h : 1;
@@ -1546,12 +1594,22 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp_i
         // consumers that feed themselves measured faster with 4 or more heads
         // per item (short contexts: 28-layer steps 8 % faster), the producer
         // warp with 1 or 2 (long contexts: 10 % faster)
-        const bool self_feed = hpi >= 4;
+        // two D = 64 heads per consumer step (8 KB, as one head at D = 128),
+        // fed by the producer warp: the even split's items of two heads
+        const int ns2 = (D == 64 && even && hpi == 2 && two_heads_per_consumer())
+                            ? tma_stages(D, prm.num_seqs, prm.group, 2)
+                            : 0;
+        const int hpc = ns2 >= 2 ? 2 : 1;
+        if (hpc == 2) nstages = ns2;
+        const bool self_feed = hpi >= 4 && hpc == 1;
+        // (the two-head build exists at D = 64 only)
+        constexpr int kTwo = D == 64 ? 2 : 1;
         auto kern = self_feed  ? decode_partition_tma_kernel<T, D, false, true>
                     : hpi == 1 ? decode_partition_tma_kernel<T, D, true, false>
+                    : hpc == 2 ? decode_partition_tma_kernel<T, D, false, false, kTwo>
                                : decode_partition_tma_kernel<T, D, false, false>;
-        const size_t smem =
-            tma_fixed_smem(D, prm.num_seqs, prm.group) + (size_t)nstages * tma_stage_smem(D);
+        const size_t smem = tma_fixed_smem(D, prm.num_seqs, prm.group) +
+                            (size_t)nstages * tma_stage_smem(D, hpc);
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
             return PKV_ERR_CUDA;

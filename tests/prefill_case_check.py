@@ -19,7 +19,7 @@ def main() -> int:
     dev = torch.device("cuda", 0)
     pkv.pkv_device_status(reset=True)
     for dtype, Hq, Hkv, D in (("bf16", 32, 8, 128), ("f16", 16, 4, 64), ("bf16", 12, 4, 128)):
-        specs = [(300, 64), (33, 1), (450, 160), (17, 17), (2000, 700)]
+        specs = [(300, 64), (33, 1), (450, 160), (17, 17), (900, 300)]
         c = _case(dev, dtype, specs, Hq, Hkv, D, seed=Hq + D + 5)
         out, want, code, _, _ = _run(c, D, dev)
         assert_attention_close(bits(out), want, code, f"comparison kernel g={Hq // Hkv} D={D}")
