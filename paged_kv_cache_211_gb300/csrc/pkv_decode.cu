@@ -1489,12 +1489,13 @@ bool two_heads_per_consumer() {
 // KV heads per TMA item.  One head per item keeps each consumer's share of a
 // partition long and the partials few; several heads per item fetch more of a
 // block's contiguous run at once and keep consumers busy when contexts are
-// short.  Rule, from sweeps of 1/2/4/8 heads per item on four workloads:
+// short.  Rule, from sweeps of 1/2/4/8 heads per item on five workloads:
 // under an even split, the fewest heads that fetch 256 bytes of each row;
 // else one head when unsplit (sequence, head) items already give every SM 4
-// of them; otherwise the fewest heads that make max_blocks * heads >= 256, i.e.
-// at least 32 blocks per consumer of a longest sequence (28-layer steps with
-// 2..32-block contexts ran 1.12x faster at 8 heads per item than at 1).
+// of them, or when there are no more of them than SMs; otherwise the fewest
+// heads that make max_blocks * heads >= 256, i.e. at least 32 blocks per
+// consumer of a longest sequence (28-layer steps with 2..32-block contexts ran
+// 1.12x faster at 8 heads per item than at 1).
 // PKV_HEADS_PER_ITEM=<n> or =all overrides.
 int tma_heads_per_item(int num_seqs, int max_blocks, int num_kv_heads, int head_dim,
                        bool even) {
@@ -1522,6 +1523,10 @@ int tma_heads_per_item(int num_seqs, int max_blocks, int num_kv_heads, int head_
         return valid(h) ? h : 1;
     }
     if ((long long)num_seqs * num_kv_heads >= 4ll * sm_count()) return 1;
+    // so few (sequence, head) pairs that one head per item still leaves SMs
+    // idle: one head, so that each sequence's blocks spread over a CTA's eight
+    // consumers (4 sequences x 8 heads: 12.3 us a step against 19.5 at 8 heads)
+    if ((long long)num_seqs * num_kv_heads <= sm_count()) return 1;
     int hpi = 1;
     for (int h = 2; h <= kTmaConsumers; ++h) {
         if ((long long)max_blocks * hpi >= 32ll * kTmaConsumers) break;
