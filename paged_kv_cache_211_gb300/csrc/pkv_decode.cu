@@ -1392,9 +1392,18 @@ size_t partition_smem_bytes(int head_dim, int num_seqs) {
 
 constexpr int kPassPartition = 1;
 constexpr int kPassMerge = 2;
-// A cascade's prefix pass takes at most 1 / kCascadePrefixShare of the SMs;
-// the partition pass over the sequences' own blocks takes the rest.
+// A cascade's prefix pass takes at most 1 / kCascadePrefixShare of the SMs
+// (PKV_PREFIX_CTAS=<n> overrides, for comparison runs); the partition pass
+// over the sequences' own blocks takes the rest.
 constexpr int kCascadePrefixShare = 8;
+int cascade_prefix_ctas(int sms) {
+    static const int forced = [] {
+        const char* v = std::getenv("PKV_PREFIX_CTAS");
+        return v ? std::atoi(v) : 0;
+    }();
+    if (forced > 0) return std::min(forced, std::max(1, sms - 1));
+    return std::max(1, sms / kCascadePrefixShare);
+}
 
 template <typename T, int D>
 pkv_status launch_decode(const DecodeParams& prm_in, const MergeParams& mp, int pb_lower,
@@ -1815,7 +1824,7 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
             q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, len_bound,
             num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, prefix_blocks,
             prm.scale_log2, prm.ws_m, prm.ws_l, prm.ws_o, dtype,
-            std::max(1, sms / kCascadePrefixShare), &pgrid, stream);
+            cascade_prefix_ctas(sms), &pgrid, stream);
         if (rc != PKV_OK) return rc;
         prm.no_wait = 1;
         rc = run(kPassPartition, std::max(1, sms - pgrid), true);

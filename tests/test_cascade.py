@@ -84,12 +84,14 @@ def _shared_case(dev, dtype, lens, P, Hq, Hkv, D, seed):
 
 @pytest.mark.parametrize("dtype,Hq,Hkv,D,B", [("bf16", 16, 8, 128, 14), ("f16", 32, 4, 64, 14),
                                                ("bf16", 8, 8, 128, 14), ("f16", 12, 4, 128, 14),
-                                               ("bf16", 24, 8, 128, 50)])
+                                               ("bf16", 24, 8, 128, 50),
+                                               ("f16", 32, 16, 64, 14)])  # register-pipelined pass
 def test_cascade_attention_short_and_long_sequences(dtype, Hq, Hkv, D, B, cuda_device):
     """Sequences shorter than, equal to and longer than a 192-token prefix (12
     blocks: one full and one half key tile of the prefix pass); with B = 50 and
     3 query heads per KV head, 150 rows per KV head: two row tiles, the second
-    partly empty."""
+    partly empty.  16 KV heads take the register-pipelined partition pass,
+    which waits for the prefix pass instead of running beside it."""
     P = 12
     base = [1, 5, 16, 100, 191, 192, 193, 250, 700, 1000, 64, 300, 2, 193]
     lens = [base[i % len(base)] + (i // len(base)) * 37 for i in range(B)]
