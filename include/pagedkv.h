@@ -46,8 +46,11 @@
  *    stores visible) before it reads or writes any caller memory, whatever
  *    that kernel is.  One exception, internal to a call: in
  *    paged_kv_decode_step_layers the partition pass of layer l > 0 reads
- *    context_lens, block_tables and layer l's pools before that wait, since
- *    the kernel before it is layer l - 1's, which writes none of them.  The
+ *    context_lens, block_tables, layer l's q, k_new, v_new and pools, and
+ *    writes layer l's pools and out, before that wait: the kernel before it
+ *    is layer l - 1's, which touches none of them.  It waits before its
+ *    first workspace write (layer l - 1's merge reads the workspace) and
+ *    before it ends, so that it never completes before that kernel.  The
  *    TMA partition pass (after its prologue) and the merge pass (once its
  *    partition pass has finished) let the next kernel's CTAs be scheduled
  *    before they end; a dependent of another library must then wait for
@@ -408,6 +411,8 @@ pkv_status paged_kv_decode_step_partition_pass(
  *   q + l*[B][Hq][D], k_new / v_new + l*[B][Hkv][D], the pools' layer l
  *   (k_cache / v_cache + l*[num_blocks][16][Hkv][D]) and out + l*[B][Hq][D],
  * in order on `stream`, sharing block_tables, context_lens and the workspace.
+ * out must not overlap q, k_new, v_new or the pools (a later layer's pass
+ * runs beside the previous layer's merge).
  * The call neither allocates nor synchronises, so a caller may capture it
  * into a CUDA graph (stream capture) and replay the whole step. */
 pkv_status paged_kv_decode_step_layers(const void* q, const void* k_new, const void* v_new,

@@ -140,9 +140,10 @@ struct DecodeParams {
                                // itself started after everything before it: no
                                // griddepcontrol.wait at all
     int early_reads;           // TMA pass: the previous kernel on the stream is this
-                               // library's, launched in the same call, and writes none of
-                               // the lengths, tables or this layer's pools: read them
-                               // before griddepcontrol.wait
+                               // library's, launched in the same call, and touches none of
+                               // the lengths, tables, this layer's inputs, pools or out:
+                               // read and write them before griddepcontrol.wait (which
+                               // comes before the first workspace write)
     float scale_log2;          // scale * log2(e): scores live in base 2
 };
 
@@ -1009,11 +1010,21 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
     }
 
     // q, k_new, v_new and every output may belong to the previous kernel:
-    // wait for it (a cascade's partition pass has nothing to wait for)
-    if (!p.no_wait) asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    // wait for it (a cascade's partition pass has nothing to wait for).  A
+    // later layer of a multi-layer step (early_reads) reads nothing that the
+    // kernel before it (the previous layer's merge) writes, and writes only
+    // the shared workspace that this merge reads: it waits just before its
+    // first workspace write instead, so that its blocks up to then overlap
+    // that merge.  Every consumer thread waits before it ends, so that this
+    // grid never completes before the kernel it depends on.  (A repeated
+    // wait returns at once.)
+    // The map of workspace rows the merge pass reads is the same for every
+    // layer of a multi-layer step (same lengths, tables and launch shape), so
+    // only the first layer writes it.
+    if (!p.early_reads && !p.no_wait) asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    if (blockIdx.x == 0 && !p.early_reads)
+        for (int s = tid; s <= B; s += NC * 32) p.ws_offsets[s] = sm_off[s];
     if (blockIdx.x == 0) {
-        for (int s = tid; s <= B; s += NC * 32)
-            p.ws_offsets[s] = sm_off[s];
         if (p.slot_out) {
             // no slot for an empty or invalid sequence, nor for a cascade
             // token that would land in a shared block
@@ -1219,6 +1230,8 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
                 sm_l[w * kMaxGroup + 2 * tig + 1] = l1[e];
             }
             asm volatile("bar.sync 1, %0;\n" ::"r"(NC * 32) : "memory");
+            if (p.early_reads && it.dest >= 0)  // uniform over the consumers
+                asm volatile("griddepcontrol.wait;\n" ::: "memory");
             constexpr int SL = D / 8;
             // one thread per (KV head of this round, query head of its group,
             // 8-wide slice of D), merging the CPH consumers that hold that head:
@@ -1266,6 +1279,7 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
             asm volatile("bar.sync 1, %0;\n" ::"r"(NC * 32) : "memory");
         }
     }
+    if (p.early_reads) asm volatile("griddepcontrol.wait;\n" ::: "memory");
     // every copy this warp issued must land before the CTA may exit: wait for
     // the last use issued into each of its slots (normally already consumed)
     __syncwarp();
@@ -1277,6 +1291,8 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
     }
 }
 
+
+constexpr int kMergeThreads = 128;
 
 struct MergeParams {
     const int* ws_offsets;
@@ -1294,19 +1310,11 @@ struct MergeParams {
     int even_grid, even_heads, groups;
 };
 
-// Log-sum-exp merge of a sequence's partitions, one warp per (sequence, query head):
+// Log-sum-exp merge of one (sequence, query head)'s partitions by one warp:
 //   M = max_p m_p,  L = sum_p l_p 2^(m_p - M),  out = sum_p o_p 2^(m_p - M) / L.
 template <typename T, int D>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const MergeParams p) {
+__device__ __forceinline__ void merge_one(const MergeParams& p, int wg, int lane) {
     constexpr int PER = D / 32;
-    // launched early (programmatic dependent launch): wait for the partition
-    // pass; only then let the next grid (the next call's partition pass)
-    // start, so that it never overlaps this call's partition pass
-    asm volatile("griddepcontrol.wait;\n" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-    const int lane = threadIdx.x & 31;
-    const int wg = blockIdx.x * 4 + (threadIdx.x >> 5);
-    if (wg >= p.num_seqs * p.num_q_heads) return;
     const int Hq = p.num_q_heads;
     const int s = wg / Hq, qh = wg - s * Hq;
     // the workspace rows of (s, qh): np of them, row(i) for i < np (-1: none)
@@ -1385,6 +1393,25 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const MergeParams p) 
     }
 }
 
+// The merge pass: warp w of the grid merges (sequence, query head) pairs w,
+// w + 4 * gridDim.x, ...  The grid may be smaller than one warp per pair, so
+// that every CTA fits beside a partition CTA on its SM (see merge_grid_cap).
+template <typename T, int D>
+__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const MergeParams p) {
+    // launched early (programmatic dependent launch).  The next grid may be
+    // scheduled at once: its CTAs take the SMs the partition pass leaves
+    // (the next layer's partition pass of a multi-layer step starts on its
+    // own layer there; any other dependent waits for this grid first).
+    // Then wait for the partition pass.
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    constexpr int WPC = kMergeThreads / 32;
+    const int lane = threadIdx.x & 31;
+    const int pairs = p.num_seqs * p.num_q_heads;
+    for (int wg = blockIdx.x * WPC + (threadIdx.x >> 5); wg < pairs; wg += gridDim.x * WPC)
+        merge_one<T, D>(p, wg, lane);
+}
+
 size_t partition_smem_bytes(int head_dim, int num_seqs) {
     return (size_t)kWarps * kMaxGroup * head_dim * 4 + 2 * kWarps * kMaxGroup * 4 +
            (size_t)(2 * num_seqs + 1) * 4;
@@ -1434,10 +1461,11 @@ pkv_status launch_decode(const DecodeParams& prm_in, const MergeParams& mp, int 
     if ((passes & kPassMerge) && need_merge) {
         // programmatic dependent launch: the merge grid is scheduled while the
         // partition grid drains and waits (griddepcontrol.wait) for its results
-        const int warps = prm.num_seqs * prm.num_q_heads;
+        constexpr int WPC = kMergeThreads / 32;
+        const int pairs = prm.num_seqs * prm.num_q_heads;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)((warps + 3) / 4));
-        cfg.blockDim = dim3(128);
+        cfg.gridDim = dim3((unsigned)((pairs + WPC - 1) / WPC));
+        cfg.blockDim = dim3(kMergeThreads);
         cfg.dynamicSmemBytes = 0;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
@@ -1461,6 +1489,57 @@ int smem_optin_bytes() {
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return 0;
     return v;
+}
+
+// Registers a kernel's CTA of `threads` holds (allocated per warp in units of
+// 256), cached per kernel.
+int cta_registers(const void* fn, int threads) {
+    static std::mutex mu;
+    static const void* keys[16];
+    static int regs[16];
+    static int n = 0;
+    std::lock_guard<std::mutex> lk(mu);
+    int r = -1;
+    for (int i = 0; i < n; ++i)
+        if (keys[i] == fn) r = regs[i];
+    if (r < 0) {
+        cudaFuncAttributes a;
+        if (cudaFuncGetAttributes(&a, fn) != cudaSuccess) return -1;
+        r = a.numRegs;
+        if (n < 16) {
+            keys[n] = fn;
+            regs[n++] = r;
+        }
+    }
+    return (r * 32 + 255) / 256 * 256 * ((threads + 31) / 32);
+}
+
+// Merge CTAs that fit on one SM beside one partition CTA (registers, shared
+// memory and threads; at least 1).  The merge pass is launched while its
+// partition pass runs; capped at this many CTAs per SM, every merge CTA is
+// resident from the start, and none lands on an SM the partition pass leaves,
+// where it would keep out the next layer's partition CTA.
+int merge_ctas_beside(const void* part, int part_threads, size_t part_smem, const void* merge) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    int regs_sm = 0, smem_sm = 0, smem_res = 0, threads_sm = 0;
+    if (cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&smem_res, cudaDevAttrReservedSharedMemoryPerBlock, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&threads_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev) !=
+            cudaSuccess)
+        return 1;
+    const long long pr = cta_registers(part, part_threads);
+    const long long mr = cta_registers(merge, kMergeThreads);
+    if (pr <= 0 || mr <= 0) return 1;
+    long long k = (regs_sm - pr) / mr;
+    k = std::min<long long>(
+        k, ((long long)smem_sm - (long long)part_smem - 2ll * smem_res) / std::max(1, smem_res));
+    k = std::min<long long>(k, (threads_sm - part_threads) / kMergeThreads);
+    return (int)std::max<long long>(1, k);
 }
 
 size_t tma_fixed_smem(int head_dim, int num_seqs, int group) {
@@ -1557,7 +1636,8 @@ int tma_items_per_cta(int heads_per_item) {
 template <typename T, int D>
 pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp_in, int pb_lower,
                              int max_blocks, bool need_merge, int passes, int nstages,
-                             int sm_cap, bool plain_merge, cudaStream_t stream) {
+                             int sm_cap, bool plain_merge, cudaStream_t stream,
+                             bool feeds_next = false) {
     DecodeParams prm = prm_in;
     MergeParams mp = mp_in;
     int sms = sm_count();
@@ -1599,6 +1679,7 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp_i
         prm.target_items = grid * tma_items_per_cta(hpi);
     }
 
+    int merge_cap = 0;  // merge CTAs that fit beside this pass's partition CTAs
     if (passes & kPassPartition) {
         CUtensorMap tmk, tmv;
         const pkv_dtype dt = std::is_same<T, __nv_bfloat16>::value ? PKV_BF16 : PKV_F16;
@@ -1642,12 +1723,25 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp_i
         cfg.numAttrs = 1;
         if (cudaLaunchKernelEx(&cfg, kern, prm, tmk, tmv, nstages, hpi) != cudaSuccess)
             return PKV_ERR_CUDA;
+        merge_cap = sms * merge_ctas_beside(reinterpret_cast<const void*>(kern),
+                                            tma_threads(self_feed), smem,
+                                            reinterpret_cast<const void*>(
+                                                decode_merge_kernel<T, D>));
     }
     if ((passes & kPassMerge) && need_merge) {
-        const int warps = prm.num_seqs * prm.num_q_heads;
+        constexpr int WPC = kMergeThreads / 32;
+        const int pairs = prm.num_seqs * prm.num_q_heads;
+        int mgrid = (pairs + WPC - 1) / WPC;
+        // When the next kernel is the next layer's partition pass, the merge
+        // fits beside a partition CTA on every SM (else its CTAs, landing on
+        // the SMs this pass leaves, would hold that layer's CTAs off them
+        // until the merge ends: 1.3x slower 28-layer steps).  Otherwise it
+        // takes as many CTAs as it has pairs / 4 (capped, 8192 pairs of
+        // D = 64 merged 8 % slower).
+        if (feeds_next && !plain_merge && merge_cap > 0) mgrid = std::min(mgrid, merge_cap);
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)((warps + 3) / 4));
-        cfg.blockDim = dim3(128);
+        cfg.gridDim = dim3((unsigned)mgrid);
+        cfg.blockDim = dim3(kMergeThreads);
         cfg.dynamicSmemBytes = 0;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
@@ -1680,7 +1774,7 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
                        int partition_blocks, pkv_dtype dtype, int passes,
                        cudaStream_t stream, const void* k_new = nullptr,
                        const void* v_new = nullptr, int64_t* slot_out = nullptr,
-                       int prefix_blocks = 0, bool chained = false) {
+                       int prefix_blocks = 0, bool chained = false, bool feeds_next = false) {
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
         max_blocks_per_seq <= 0 || num_blocks <= 0 || max_context_len < 0 ||
         partition_blocks < 0)
@@ -1780,17 +1874,19 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
                 return head_dim == 128
                            ? launch_decode_tma<__nv_bfloat16, 128>(prm, mp, pb_lower, grid_blocks,
                                                                    need_merge, pass_mask, nstages,
-                                                                   sm_cap, plain_merge, stream)
+                                                                   sm_cap, plain_merge, stream,
+                                                                   feeds_next)
                            : launch_decode_tma<__nv_bfloat16, 64>(prm, mp, pb_lower, grid_blocks,
                                                                   need_merge, pass_mask, nstages,
-                                                                  sm_cap, plain_merge, stream);
+                                                                  sm_cap, plain_merge, stream,
+                                                                  feeds_next);
             return head_dim == 128
                        ? launch_decode_tma<__half, 128>(prm, mp, pb_lower, grid_blocks, need_merge,
                                                         pass_mask, nstages, sm_cap, plain_merge,
-                                                        stream)
+                                                        stream, feeds_next)
                        : launch_decode_tma<__half, 64>(prm, mp, pb_lower, grid_blocks, need_merge,
                                                        pass_mask, nstages, sm_cap, plain_merge,
-                                                       stream);
+                                                       stream, feeds_next);
         }
         if (dtype == PKV_BF16)
             return head_dim == 128
@@ -1960,7 +2056,7 @@ pkv_status decode_step_impl(const void* q, const void* k_new, const void* v_new,
                             float scale, void* out, int64_t* slot_mapping_out, void* workspace,
                             size_t workspace_bytes, pkv_dtype dtype, int passes,
                             cudaStream_t stream, int prefix_blocks = 0,
-                            bool chained = false) {
+                            bool chained = false, bool feeds_next = false) {
     if (num_seqs < 0 || num_kv_heads <= 0 || head_dim <= 0 || max_blocks_per_seq <= 0 ||
         num_blocks <= 0)
         return PKV_ERR_INVALID_ARG;
@@ -1969,7 +2065,8 @@ pkv_status decode_step_impl(const void* q, const void* k_new, const void* v_new,
     return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                        max_context_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
                        num_blocks, scale, out, workspace, workspace_bytes, 0, dtype, passes,
-                       stream, k_new, v_new, slot_mapping_out, prefix_blocks, chained);
+                       stream, k_new, v_new, slot_mapping_out, prefix_blocks, chained,
+                       feeds_next);
 }
 
 }  // namespace
@@ -2017,7 +2114,8 @@ pkv_status paged_kv_decode_step_layers(const void* q, const void* k_new, const v
             num_blocks, scale, static_cast<char*>(out) + l * q_layer, nullptr, workspace,
             workspace_bytes, dtype, pkv::kPassPartition | pkv::kPassMerge,
             reinterpret_cast<cudaStream_t>(stream), 0,
-            /*chained=*/l > 0);  // layer l-1's kernels write only layer l-1's pools
+            /*chained=*/l > 0,   // layer l-1's kernels write only layer l-1's pools
+            /*feeds_next=*/l + 1 < num_layers);
         if (rc != PKV_OK) return rc;
     }
     return PKV_OK;

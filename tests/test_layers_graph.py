@@ -24,11 +24,22 @@ def _oracle_layer(inp, layer):
     return oracle.decode_attention(dtype_code(w), h_q, kc, vc, tb, ln, w.scale)
 
 
-def test_layers_step_eager_and_graph(cuda_device):
+# Each later layer's partition pass runs beside the previous layer's merge
+# and waits for it only before its first workspace write: short contexts
+# (items of whole or cut sequences) and long ones (the even split, at D = 128
+# and at D = 64 with two heads per consumer).
+CASES = [
+    ("qwen3_0p6b", 4, {}),
+    ("llama7b_long", 3, dict(num_seqs=4, num_blocks=8200)),
+    ("tinyllama_1p1b", 3, dict(num_seqs=24, num_blocks=3200)),
+]
+
+
+@pytest.mark.parametrize("name,L,kw", CASES, ids=[c[0] for c in CASES])
+def test_layers_step_eager_and_graph(cuda_device, name, L, kw):
     import __graft_entry__
     __graft_entry__.build()
-    L = 4
-    w = wl.WORKLOADS["qwen3_0p6b"]
+    w = wl.WORKLOADS[name].with_(**kw)
     inp = wl.make_inputs(w, device=cuda_device, num_layers=L)
     want = [_oracle_layer(inp, l) for l in range(L)]        # before the GPU writes anything
     max_len = int(inp["context_lens_host"].max())
