@@ -1353,34 +1353,68 @@ __device__ __forceinline__ void merge_one(const MergeParams& p, int wg, int lane
         const long long slot = (i == 0 && b < start) ? 2 * c + 1 : 2 * c;
         return slot * p.even_heads + lq;
     };
-    float M = -INFINITY;
-    for (int i = lane; i < np; i += 32) {
+    // Two dependent rounds of loads after the offsets: the first kPre rows'
+    // partial outputs (every lane its slice) and, in lane i, row i's m and l,
+    // all at once; then M, the weights and the sums (rows past kPre, and
+    // rows past 32 for m and l, in further rounds).
+    using V = typename std::conditional<PER == 4, float4, float2>::type;
+    constexpr int kPre = 4;
+    V pre[kPre];
+#pragma unroll
+    for (int k = 0; k < kPre; ++k) {
+        const long long r = k < np ? row_of(k) : -1;
+        if (r >= 0) pre[k] = *reinterpret_cast<const V*>(p.ws_o + (size_t)r * D + lane * PER);
+    }
+    float mi = -INFINITY, li = 0.f;  // lane i: row i (i < 32)
+    {
+        const long long r = lane < np ? row_of(lane) : -1;
+        if (r >= 0) {
+            mi = p.ws_m[r];
+            li = p.ws_l[r];
+        }
+    }
+    float M = mi;
+    for (int i = lane + 32; i < np; i += 32) {
         const long long r = row_of(i);
         if (r >= 0) M = fmaxf(M, p.ws_m[r]);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     const float Ms = M == -INFINITY ? 0.f : M;
-    float L = 0.f;
+    const float wi = mi == -INFINITY ? 0.f : fast_exp2(mi - Ms);  // lane i: row i's weight
+    float L = wi * li;
     float acc[PER];
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-#pragma unroll 4
-    for (int i = 0; i < np; ++i) {
+    auto add = [&](float w, const V& u) {
+        if constexpr (PER == 4) {
+            acc[0] += w * u.x; acc[1] += w * u.y; acc[2] += w * u.z; acc[3] += w * u.w;
+        } else {
+            acc[0] += w * u.x; acc[1] += w * u.y;
+        }
+    };
+#pragma unroll
+    for (int k = 0; k < kPre; ++k) {
+        const float w = __shfl_sync(0xffffffffu, wi, k);
+        // rows past np, and rows with no units, carry weight 0 and a load
+        // never issued: select, never multiply an unset register
+        if (k < np && w != 0.f) add(w, pre[k]);
+    }
+    for (int i = kPre; i < np; ++i) {
         const long long rr = row_of(i);
         if (rr < 0) continue;
         const size_t r = (size_t)rr;
-        const float w = fast_exp2(p.ws_m[r] - Ms);
-        L += w * p.ws_l[r];
-        const float* src = p.ws_o + r * D + lane * PER;
-        if constexpr (PER == 4) {
-            const float4 u = *reinterpret_cast<const float4*>(src);
-            acc[0] += w * u.x; acc[1] += w * u.y; acc[2] += w * u.z; acc[3] += w * u.w;
+        float w;
+        if (i < 32) {
+            w = __shfl_sync(0xffffffffu, wi, i);
         } else {
-            const float2 u = *reinterpret_cast<const float2*>(src);
-            acc[0] += w * u.x; acc[1] += w * u.y;
+            w = fast_exp2(p.ws_m[r] - Ms);
+            if (lane == 0) L += w * p.ws_l[r];
         }
+        add(w, *reinterpret_cast<const V*>(p.ws_o + r * D + lane * PER));
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
     const float inv = L > 0.f ? 1.f / L : 0.f;
     T* dst = static_cast<T*>(p.out) + ((size_t)s * Hq + qh) * D + lane * PER;
     if constexpr (PER == 4) {
@@ -1397,7 +1431,7 @@ __device__ __forceinline__ void merge_one(const MergeParams& p, int wg, int lane
 // w + 4 * gridDim.x, ...  The grid may be smaller than one warp per pair, so
 // that every CTA fits beside a partition CTA on its SM (see merge_grid_cap).
 template <typename T, int D>
-__global__ void __launch_bounds__(kMergeThreads) decode_merge_kernel(const MergeParams p) {
+__global__ void __launch_bounds__(kMergeThreads, 8) decode_merge_kernel(const MergeParams p) {
     // launched early (programmatic dependent launch).  The next grid may be
     // scheduled at once: its CTAs take the SMs the partition pass leaves
     // (the next layer's partition pass of a multi-layer step starts on its
