@@ -608,6 +608,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
 //    no producer warp; each consumer walks its blocks twice, once to load and
 //    once to consume, and lane 0 refills a stage with the block one ring
 //    ahead as soon as the stage's fragments are in registers.
+// With warp items (many short one-head items: a cascade's suffixes, large
+// batches of short contexts) each self-feeding consumer warp takes whole
+// items of its own, every block of its item's head, and writes the item's
+// result alone: no combine across the consumers and no CTA-wide barrier.
 // Either way every slot but the one being read is in flight, across item
 // boundaries.  Every mbarrier wait is bounded: on a time-out the kernel sets
 // PKV_DEV_TIMEOUT, stops issuing and waiting, lets every copy it issued land,
@@ -619,7 +623,7 @@ constexpr int kTmaConsumers = 8;
 __host__ __device__ constexpr int tma_threads(bool self_feed) { return (kTmaConsumers + (self_feed ? 0 : 1)) * 32; }
 constexpr int kTmaItemsPerCta = 8;
 constexpr int kTmaMaxStages = 8;
-template <typename T, int D, bool kOneHead, bool kSelfFeed, int kHPC = 1>
+template <typename T, int D, bool kOneHead, bool kSelfFeed, int kHPC = 1, bool kWarpItems = false>
 __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
     decode_partition_tma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
                                 const __grid_constant__ CUtensorMap tmap_v, int nstages,
@@ -628,6 +632,9 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
     // two heads, producer warp only): a stage holds both heads' tiles, so a
     // consumer step moves 8 KB, as one head does at D = 128.
     static_assert(kHPC == 1 || (kHPC == 2 && !kSelfFeed && !kOneHead), "two heads per consumer");
+    // kWarpItems: consumer warp w of CTA c takes items c * 8 + w, then every
+    // (8 * gridDim.x)-th item after it (item mode only, one head per item)
+    static_assert(!kWarpItems || (kSelfFeed && kOneHead && kHPC == 1), "warp items");
     using E = Elem<T>;
     constexpr int NC = kTmaConsumers;
     constexpr int HALVES = D / 64;
@@ -692,7 +699,7 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
     int PB = p.partition_blocks;
     if (!even && PB <= 0) {
         const int groups0 = p.num_kv_heads / (kOneHead ? 1 : heads_per_item);
-        if ((long long)B * groups0 >= 4ll * gridDim.x) {
+        if ((long long)B * groups0 >= 4ll * gridDim.x * (kWarpItems ? NC : 1)) {
             // enough items without splitting: one partition per sequence
             int my_max = 0;
             for (int s = tid; s < B; s += NT) {
@@ -752,8 +759,10 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
     const int HPI = kOneHead ? 1 : heads_per_item;  // a constant in the one-head build
     const int groups = Hkv / HPI;
     const int total_items = total_parts * groups;
-    const int CPB = HPI / kHPC;   // consumers per block: one per kHPC heads of the item
-    const int CPH = NC / CPB;     // a consumer takes every CPH-th block of the item
+    // consumers per block: one per kHPC heads of the item (warp items: the
+    // item's one consumer), and a consumer takes every CPH-th block of it
+    const int CPB = kWarpItems ? 1 : HPI / kHPC;
+    const int CPH = kWarpItems ? 1 : NC / CPB;
     // A work item: blocks [lo, hi) of sequence s for head group hg.  dest < 0:
     // the item is the whole of its (sequence, group) and writes the output;
     // else its partials go to workspace rows dest + (query head within group).
@@ -800,7 +809,7 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
     };
     auto cursor_begin = [&]() {
         Cursor c;
-        c.item = blockIdx.x;
+        c.item = kWarpItems ? (int)blockIdx.x * NC + warp : (int)blockIdx.x;
         c.u = u_begin;
         c.s = 0;
         if (even && u_begin < u_end) {  // the sequence holding unit u_begin
@@ -817,7 +826,7 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
         if (!even) {
             if (c.item >= total_items) return false;
             it = item_of(c.item);
-            c.item += gridDim.x;
+            c.item += kWarpItems ? (int)gridDim.x * NC : (int)gridDim.x;
             return true;
         }
         if (c.u >= u_end) return false;
@@ -946,7 +955,8 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
     // (item, block) give the blocks to fetch and the blocks to consume.
     // Otherwise the producer warp above fills the rings.
     const int w = warp;
-    const int hl = w % CPB, sub = w / CPB;  // this consumer's heads slot in the group, block phase
+    // this consumer's heads slot in the group, and block phase
+    const int hl = w % CPB, sub = kWarpItems ? 0 : w / CPB;
     struct Stream {
         Cursor c;
         Item it;
@@ -962,21 +972,28 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
             if (st.live) st.j = st.it.lo + sub;
         }
     };
-    // lane 0 loads the table entry of the next block to fetch one fetch early,
-    // so that no refill waits on a global load
-    auto table_entry = [&](const Stream& st) {
-        return st.live && lane == 0
-                   ? p.block_tables[(size_t)st.it.s * p.max_blocks_per_seq + st.j]
-                   : 0;
+    // lane t holds the table entry of the fetch walk's block t steps (of CPH
+    // blocks) on within its item, from one parallel load per item (or per 32
+    // steps): a refill never waits on a table load issued by the refill before
+    // it (a chain of one dependent global load per stage held long walks to
+    // 1.5 us a stage)
+    int fs_tab = 0;  // this lane's entry
+    int fs_t = 0;    // the lane holding the next block's entry
+    auto load_tab = [&]() {  // whole warp
+        const int jl = fs.j + lane * CPH;
+        fs_tab = fs.live && jl < fs.it.hi
+                     ? p.block_tables[(size_t)fs.it.s * p.max_blocks_per_seq + jl]
+                     : 0;
+        fs_t = 0;
     };
-    int fs_id = 0;
     int nfetch = 0;        // stages issued by this warp
+    int fslot = 0;         // its ring slot (nfetch mod nstages, kept without a division)
     bool feeding = true;   // false after a wait gave up: issue nothing more
     auto fetch_next = [&]() {  // whole warp; lane 0 issues
         if (!fs.live || !feeding) return;
-        const int k = w * nstages + nfetch % nstages;
+        const int k = w * nstages + fslot;
+        int id = __shfl_sync(0xffffffffu, fs_tab, fs_t);
         if (lane == 0) {
-            int id = fs_id;
             if (id < 0 || id >= p.num_blocks) {
                 atomicOr(p.status, PKV_DEV_BAD_BLOCK_ID);
                 id = -1;  // block 0 is fetched and fully masked
@@ -994,9 +1011,14 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
             }
         }
         ++nfetch;
+        if (++fslot == nstages) fslot = 0;
         fs.j += CPH;
-        skip_done(fs);
-        fs_id = table_entry(fs);
+        if (fs.j >= fs.it.hi) {  // on to the next item this warp has a block in
+            skip_done(fs);
+            load_tab();
+        } else if (++fs_t == 32) {
+            load_tab();
+        }
     };
     // the first nstages blocks (before griddepcontrol.wait only with
     // early_reads: then the previous kernel writes nothing read here)
@@ -1005,7 +1027,7 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
         fs.live = next_item(fs.c, fs.it);
         fs.j = fs.live ? fs.it.lo + sub : 0;
         skip_done(fs);
-        fs_id = table_entry(fs);
+        load_tab();
         for (int t = 0; t < nstages; ++t) fetch_next();
     }
 
@@ -1045,7 +1067,13 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
     }
     const int gid = lane >> 2, tig = lane & 3;
     const T* __restrict__ q = static_cast<const T*>(p.q);
-    int ncons = 0;  // stages this warp has consumed
+    // the ring slot this warp consumes next and its phase parity (the stage
+    // count mod nstages and the parity of its quotient, kept without a
+    // division: two integer divisions a stage by the runtime ring depth cost
+    // more than the score MMAs)
+    int cslot = 0;
+    uint32_t cphase = 0;
+    const int kbase = w * nstages;
     Cursor cur = cursor_begin();
     Item it;
     while (next_item(cur, it)) {
@@ -1081,10 +1109,15 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
         T* kbase_w = static_cast<T*>(p.k_cache_w) + (size_t)h * D;
         T* vbase_w = static_cast<T*>(p.v_cache_w) + (size_t)h * D;
 
-        for (int j = it.lo + sub; j < it.hi; j += CPH, ++ncons) {
-            const int k = w * nstages + ncons % nstages;
+        for (int j = it.lo + sub; j < it.hi; j += CPH) {
+            const int k = kbase + cslot;
+            const uint32_t parity = cphase;
+            if (++cslot == nstages) {
+                cslot = 0;
+                cphase ^= 1u;
+            }
             const bool ok = __all_sync(
-                0xffffffffu, mbar_wait(&full[k], (ncons / nstages) & 1, abort_flag, p.status));
+                0xffffffffu, mbar_wait(&full[k], parity, abort_flag, p.status));
             unsigned char* st = ring + (size_t)k * STAGE;
             const int id = ok ? stage_id[k] : -1;
             const int nv = id < 0 ? 0 : min(PKV_BLOCK_SIZE, n - j * PKV_BLOCK_SIZE);
@@ -1229,24 +1262,28 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
                 sm_l[w * kMaxGroup + 2 * tig] = l0[e];
                 sm_l[w * kMaxGroup + 2 * tig + 1] = l1[e];
             }
-            asm volatile("bar.sync 1, %0;\n" ::"r"(NC * 32) : "memory");
-            if (p.early_reads && it.dest >= 0)  // uniform over the consumers
+            if constexpr (kWarpItems) __syncwarp();
+            else asm volatile("bar.sync 1, %0;\n" ::"r"(NC * 32) : "memory");
+            if (p.early_reads && it.dest >= 0)  // uniform over the item's consumers
                 asm volatile("griddepcontrol.wait;\n" ::: "memory");
             constexpr int SL = D / 8;
             // one thread per (KV head of this round, query head of its group,
             // 8-wide slice of D), merging the CPH consumers that hold that head:
-            // consumer v holds heads hg*HPI + (v % CPB)*kHPC + e
-            for (int x = tid; x < CPB * g * SL; x += NC * 32) {
+            // consumer v holds heads hg*HPI + (v % CPB)*kHPC + e (warp items:
+            // the lanes of the item's one consumer, w)
+            constexpr int XS = kWarpItems ? 32 : NC * 32;
+            for (int x = kWarpItems ? lane : tid; x < CPB * g * SL; x += XS) {
                 const int slot = x / (g * SL);  // heads slot within the group
                 const int hk = slot * kHPC + e;  // head within the group
                 const int hh = (x / SL) % g, d0 = (x % SL) * 8;
+                auto holder = [&](int c) { return kWarpItems ? w : slot + CPB * c; };
                 float M = -INFINITY;
-                for (int c = 0; c < CPH; ++c) M = fmaxf(M, sm_m[(slot + CPB * c) * kMaxGroup + hh]);
+                for (int c = 0; c < CPH; ++c) M = fmaxf(M, sm_m[holder(c) * kMaxGroup + hh]);
                 const float Ms = M == -INFINITY ? 0.f : M;
                 float L = 0.f;
                 float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
                 for (int c = 0; c < CPH; ++c) {
-                    const int v = slot + CPB * c;
+                    const int v = holder(c);
                     const float ew = fast_exp2(sm_m[v * kMaxGroup + hh] - Ms);
                     L += ew * sm_l[v * kMaxGroup + hh];
                     const float* src = sm_o + (v * g + hh) * DP + d0;
@@ -1276,7 +1313,8 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
                     }
                 }
             }
-            asm volatile("bar.sync 1, %0;\n" ::"r"(NC * 32) : "memory");
+            if constexpr (kWarpItems) __syncwarp();
+            else asm volatile("bar.sync 1, %0;\n" ::"r"(NC * 32) : "memory");
         }
     }
     if (p.early_reads) asm volatile("griddepcontrol.wait;\n" ::: "memory");
@@ -1657,6 +1695,17 @@ int tma_heads_per_item(int num_seqs, int max_blocks, int num_kv_heads, int head_
     return hpi;
 }
 
+// Consumer warps take whole one-head items of their own (warp items) when
+// the (sequence, KV head) pairs give every consumer warp of the grid half an
+// item or more, unless PKV_WARP_ITEMS=0 (kept for comparison runs).
+bool warp_items_enabled() {
+    static const bool on = [] {
+        const char* v = std::getenv("PKV_WARP_ITEMS");
+        return !(v && std::strcmp(v, "0") == 0);
+    }();
+    return on;
+}
+
 // Adaptive partitioning aims at this many items per CTA (PKV_TMA_ITEMS overrides).
 int tma_items_per_cta(int heads_per_item) {
     static const int forced = [] {
@@ -1712,6 +1761,10 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp_i
         // per-head items: 8 per CTA; all-heads items carry Hkv heads each: 4 per CTA
         prm.target_items = grid * tma_items_per_cta(hpi);
     }
+    const bool warp_items = !even && hpi == 1 && warp_items_enabled() &&
+                            (long long)prm.num_seqs * prm.num_kv_heads >=
+                                (long long)kTmaConsumers * sms / 2;
+    if (warp_items) prm.target_items = grid * kTmaConsumers * 2;  // two items per warp
 
     int merge_cap = 0;  // merge CTAs that fit beside this pass's partition CTAs
     if (passes & kPassPartition) {
@@ -1730,11 +1783,12 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp_i
                             : 0;
         const int hpc = ns2 >= 2 ? 2 : 1;
         if (hpc == 2) nstages = ns2;
-        const bool self_feed = hpi >= 4 && hpc == 1;
+        const bool self_feed = (hpi >= 4 && hpc == 1) || warp_items;
         // (the two-head build exists at D = 64 only)
         constexpr int kTwo = D == 64 ? 2 : 1;
-        auto kern = self_feed  ? decode_partition_tma_kernel<T, D, false, true>
-                    : hpi == 1 ? decode_partition_tma_kernel<T, D, true, false>
+        auto kern = warp_items  ? decode_partition_tma_kernel<T, D, true, true, 1, true>
+                    : self_feed ? decode_partition_tma_kernel<T, D, false, true>
+                    : hpi == 1  ? decode_partition_tma_kernel<T, D, true, false>
                     : hpc == 2 ? decode_partition_tma_kernel<T, D, false, false, kTwo>
                                : decode_partition_tma_kernel<T, D, false, false>;
         const size_t smem = tma_fixed_smem(D, prm.num_seqs, prm.group) +

@@ -174,6 +174,27 @@ def test_group_sizes_and_ragged_lengths(dtype, Hq, Hkv, D, cuda_device):
     assert_attention_close(bits(out), want, dtype_code(w), f"g={Hq // Hkv} D={D}")
 
 
+@pytest.mark.parametrize("dtype,Hq,Hkv,D,B", [("bf16", 32, 8, 128, 160), ("f16", 32, 4, 64, 200),
+                                               ("bf16", 8, 8, 128, 96)])
+def test_warp_items(dtype, Hq, Hkv, D, B, cuda_device):
+    """Many short one-head items (at least half an item per consumer warp of
+    the grid, contexts under 64 blocks): each consumer warp takes whole items
+    of its own.  Lengths span empty, one token, block boundaries and 1000
+    tokens, so some sequences stay whole and others are cut and merged."""
+    rng = np.random.default_rng(1000 + B)
+    lens = rng.integers(1, 1001, size=B)
+    lens[:6] = [0, 1, 16, 17, 1000, 999]
+    w, inp = _custom(cuda_device, dtype, [int(n) for n in lens], Hq, Hkv, D,
+                     int((lens + 15).sum() // 16) + 64, seed=B)
+    keep = np.flatnonzero(lens > 0)
+    want, _, _ = compact_oracle_step(inp, keep)
+    out, slots = _run_step(inp, cuda_device)
+    assert pkv.pkv_device_status() == 0
+    assert int(slots[0]) == -1
+    assert torch.count_nonzero(out[0]) == 0
+    assert_attention_close(bits(out)[keep], want, dtype_code(w), f"B={B} g={Hq // Hkv} D={D}")
+
+
 def test_length_one_returns_v_exactly(cuda_device):
     w, inp = _custom(cuda_device, "bf16", [1, 1, 1], 8, 2, 128, 8, seed=5)
     out, _ = _run_step(inp, cuda_device)

@@ -26,16 +26,19 @@ def _oracle_layer(inp, layer):
 
 # Each later layer's partition pass runs beside the previous layer's merge
 # and waits for it only before its first workspace write: short contexts
-# (items of whole or cut sequences) and long ones (the even split, at D = 128
-# and at D = 64 with two heads per consumer).
+# (items of whole or cut sequences, shared by the consumer warps or, with many
+# sequences, taken whole by one warp each) and long ones (the even split, at
+# D = 128 and at D = 64 with two heads per consumer).
 CASES = [
     ("qwen3_0p6b", 4, {}),
     ("llama7b_long", 3, dict(num_seqs=4, num_blocks=8200)),
     ("tinyllama_1p1b", 3, dict(num_seqs=24, num_blocks=3200)),
+    ("qwen3_0p6b", 3, dict(num_seqs=160)),   # consumer warps take whole items
 ]
 
 
-@pytest.mark.parametrize("name,L,kw", CASES, ids=[c[0] for c in CASES])
+@pytest.mark.parametrize("name,L,kw", CASES,
+                         ids=[c[0] + ("_b%d" % c[2]["num_seqs"] if c[2] else "") for c in CASES])
 def test_layers_step_eager_and_graph(cuda_device, name, L, kw):
     import __graft_entry__
     __graft_entry__.build()
