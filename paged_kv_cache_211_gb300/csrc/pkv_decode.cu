@@ -75,6 +75,7 @@ int min_partition_blocks(int max_context_len) {
 
 struct WsLayout {
     size_t offsets, m, l, o, total;
+    size_t rows;  // partial rows (m, l and o of one query head) it holds
 };
 
 // Largest grid of the even-split partition pass; its workspace holds two rows
@@ -97,6 +98,7 @@ WsLayout ws_layout(int num_seqs, int num_q_heads, int head_dim, int max_context_
     if (extra_rows_per_seq == 0 && mb >= kEvenMinBlocks)
         rows = std::max(rows, (size_t)2 * kMaxEvenGrid * std::min(num_q_heads, kEvenMaxHeads));
     WsLayout w;
+    w.rows = rows;
     w.offsets = 0;
     w.m = align256((size_t)(num_seqs + 1) * 4);
     w.l = w.m + align256(rows * 4);
@@ -130,6 +132,9 @@ struct DecodeParams {
     int prefix_parts;          // cascade: 1 (the prefix pass writes workspace row s of
                                // sequence s), else 0
     int item_row0;             // first workspace row of the items (num_seqs in a cascade)
+    int even_row0;             // TMA pass, even split: first workspace row of the slots
+                               // (a cascade's whole suffixes keep rows item_row0 + s)
+    long long ws_rows;         // host: partial rows the workspace holds
     int min_partition_blocks;  // lower bound of the adaptive choice
     int target_items;
     int even_split;            // TMA pass: cut the (sequence, head group, block) units evenly
@@ -726,8 +731,8 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
     const int chunk = (B + NT - 1) / NT;
     const int s_lo = min(B, tid * chunk), s_hi = min(B, s_lo + chunk);
     // item mode: partitions per sequence; even split: blocks per sequence
-    auto units_of = [&](int s) {
-        return even ? (sm_len[s] + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE
+    auto units_of = [&](int s) {  // (a cascade's shared prefix is not the items')
+        return even ? max((sm_len[s] + PKV_BLOCK_SIZE - 1) / PKV_BLOCK_SIZE - p.skip_blocks, 0)
                     : item_parts(sm_len[s], PB, p.skip_blocks, p.prefix_parts);
     };
     int mine = 0;
@@ -796,13 +801,18 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
         return it;
     };
     // Even split: the U = groups * (total blocks) units, ordered (sequence,
-    // group, block), are cut into gridDim.x ranges of equal size; this CTA's
-    // range is a run of segments, each a whole (sequence, group) written
-    // straight to the output except possibly the first and the last, which
-    // leave partials in workspace slots 2c and 2c + 1 (c = this CTA).
+    // group, block), are cut into one range of equal size per worker (a CTA;
+    // with warp items, a consumer warp: worker c * 8 + w); a worker's range is
+    // a run of segments, each a whole (sequence, group) written straight to
+    // the output except possibly the first and the last, which leave partials
+    // in workspace slots 2c and 2c + 1 (c = the worker; rows from even_row0).
+    // In a cascade the blocks are those past the shared prefix, and a whole
+    // segment leaves its partials in row item_row0 + s instead, for the merge.
     const long long U = even ? (long long)groups * sm_off[B] : 0;
-    const long long u_begin = U * blockIdx.x / gridDim.x;
-    const long long u_end = U * (blockIdx.x + 1) / gridDim.x;
+    const int worker = kWarpItems ? (int)blockIdx.x * NC + warp : (int)blockIdx.x;
+    const int workers = kWarpItems ? (int)gridDim.x * NC : (int)gridDim.x;
+    const long long u_begin = U * worker / workers;
+    const long long u_end = U * (worker + 1) / workers;
     struct Cursor {
         int item, s;
         long long u;
@@ -840,12 +850,13 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
         it.s = s;
         it.hg = hg;
         it.n = sm_len[s];
-        it.nblk = nb;
-        it.lo = b0;
-        it.hi = b0 + len;
-        it.dest = (b0 == 0 && len == nb)
-                      ? -1
-                      : (2 * (int)blockIdx.x + (c.u == u_begin ? 0 : 1)) * (HPI * g);
+        it.nblk = p.skip_blocks + nb;  // blocks of the sequence (the last holds the new token)
+        it.lo = p.skip_blocks + b0;
+        it.hi = p.skip_blocks + b0 + len;
+        if (b0 == 0 && len == nb)
+            it.dest = p.prefix_parts ? (p.item_row0 + s) * Hq + hg * HPI * g : -1;
+        else
+            it.dest = p.even_row0 + (2 * worker + (c.u == u_begin ? 0 : 1)) * (HPI * g);
         c.u += len;
         if (b0 + len == nb && hg == groups - 1) {  // on to the next sequence with blocks
             int t = s + 1;
@@ -1057,8 +1068,9 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
             }
         }
     }
-    if (even) {
+    if (even && !p.prefix_parts) {
         // empty (or invalid) sequences have no units: their rows are zeros
+        // (a cascade's merge writes every row)
         for (int s = blockIdx.x; s < B; s += gridDim.x) {
             if (sm_len[s] != 0) continue;
             uint4* o = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + (size_t)s * Hq * D);
@@ -1342,6 +1354,7 @@ struct MergeParams {
     int min_rows;  // merge sequences with at least this many workspace rows
     int prefix_rows;  // cascade: 1 (row s holds sequence s's prefix partials), else 0
     int item_row0;    // first workspace row of the items
+    int even_row0;    // first workspace row of the even split's slots
     // even split of the TMA pass (even_grid > 0): ws_offsets holds block
     // offsets, and the CTAs that covered a (sequence, group) left its partials
     // in their slots (two per CTA, even_heads query heads each)
@@ -1360,60 +1373,70 @@ __device__ __forceinline__ void merge_one(const MergeParams& p, int wg, int lane
     size_t base = 0;
     int c0 = 0, lq = 0;
     long long U = 0, start = 0;
-    const long long G = p.even_grid;
+    const long long G = p.even_grid;  // even split: its workers (CTAs or consumer warps)
+    int ne = 0;                       // even split: workers that covered (s, qh)'s group
     if (G > 0) {
         const int nb = p.ws_offsets[s + 1] - p.ws_offsets[s];
-        if (nb == 0) return;  // zeros, written by the partition pass
-        U = (long long)p.groups * p.ws_offsets[p.num_seqs];
-        const int hg = qh / p.even_heads;
-        lq = qh - hg * p.even_heads;
-        start = (long long)p.groups * p.ws_offsets[s] + (long long)hg * nb;
-        // CTA holding unit u: the largest c with floor(c * U / G) <= u
-        auto cta_of = [&](long long u) { return (int)(((u + 1) * G + U - 1) / U - 1); };
-        c0 = cta_of(start);
-        np = cta_of(start + nb - 1) - c0 + 1;
-        if (np < 2) return;  // one CTA covered it and wrote the output
+        if (nb > 0) {
+            U = (long long)p.groups * p.ws_offsets[p.num_seqs];
+            const int hg = qh / p.even_heads;
+            lq = qh - hg * p.even_heads;
+            start = (long long)p.groups * p.ws_offsets[s] + (long long)hg * nb;
+            // worker holding unit u: the largest c with floor(c * U / G) <= u
+            auto cta_of = [&](long long u) { return (int)(((u + 1) * G + U - 1) / U - 1); };
+            c0 = cta_of(start);
+            ne = cta_of(start + nb - 1) - c0 + 1;
+        }
+        // no blocks (zeros) or one worker: the partition pass wrote the
+        // output, unless a cascade's prefix row is still to be merged
+        if (ne < 2 && p.prefix_rows == 0) return;
+        np = ne + p.prefix_rows;
     } else {
         const int off = p.ws_offsets[s];
         np = p.ws_offsets[s + 1] - off + p.prefix_rows;
         if (np < p.min_rows) return;  // a one-row sequence was written by the partition pass
         base = ((size_t)p.item_row0 + off) * Hq + qh;
     }
-    auto row_of = [&](int i) -> long long {
+    // row i of (s, qh), -1 for none (rows fit in 32 bits: the workspace is
+    // sized from int arguments)
+    auto row_of = [&](int i) -> int {
         if (G == 0) {
-            if (p.prefix_rows == 0) return (long long)(base + (size_t)i * Hq);
+            if (p.prefix_rows == 0) return (int)(base + (size_t)i * Hq);
             // cascade: the prefix row first, then the items
-            return i == 0 ? (long long)s * Hq + qh : (long long)(base + (size_t)(i - 1) * Hq);
+            return i == 0 ? s * Hq + qh : (int)(base + (size_t)(i - 1) * Hq);
+        }
+        if (p.prefix_rows) {  // cascade: the prefix row first, then the suffix's rows
+            if (i == 0) return s * Hq + qh;
+            --i;
+            if (ne == 1) return (p.item_row0 + s) * Hq + qh;  // a whole suffix
         }
         const long long c = c0 + i;
         const long long b = c * U / G;
-        if (b == (c + 1) * U / G) return -1;  // a CTA with no units (U < G)
+        if (b == (c + 1) * U / G) return -1;  // a worker with no units (U < G)
         const long long slot = (i == 0 && b < start) ? 2 * c + 1 : 2 * c;
-        return slot * p.even_heads + lq;
+        return (int)(p.even_row0 + slot * p.even_heads + lq);
     };
-    // Two dependent rounds of loads after the offsets: the first kPre rows'
-    // partial outputs (every lane its slice) and, in lane i, row i's m and l,
-    // all at once; then M, the weights and the sums (rows past kPre, and
-    // rows past 32 for m and l, in further rounds).
+    // Two dependent rounds of loads after the offsets: lane i finds row i and
+    // loads its m and l while every lane loads its slice of the first kPre
+    // rows' partial outputs (row numbers passed by shuffle); then M, the
+    // weights and the sums (rows past kPre, and past 32, in further rounds).
     using V = typename std::conditional<PER == 4, float4, float2>::type;
     constexpr int kPre = 4;
+    const int rl = lane < np ? row_of(lane) : -1;  // lane i: row i (i < 32)
     V pre[kPre];
 #pragma unroll
     for (int k = 0; k < kPre; ++k) {
-        const long long r = k < np ? row_of(k) : -1;
+        const int r = __shfl_sync(0xffffffffu, rl, k);
         if (r >= 0) pre[k] = *reinterpret_cast<const V*>(p.ws_o + (size_t)r * D + lane * PER);
     }
-    float mi = -INFINITY, li = 0.f;  // lane i: row i (i < 32)
-    {
-        const long long r = lane < np ? row_of(lane) : -1;
-        if (r >= 0) {
-            mi = p.ws_m[r];
-            li = p.ws_l[r];
-        }
+    float mi = -INFINITY, li = 0.f;
+    if (rl >= 0) {
+        mi = p.ws_m[rl];
+        li = p.ws_l[rl];
     }
     float M = mi;
     for (int i = lane + 32; i < np; i += 32) {
-        const long long r = row_of(i);
+        const int r = row_of(i);
         if (r >= 0) M = fmaxf(M, p.ws_m[r]);
     }
 #pragma unroll
@@ -1436,12 +1459,11 @@ __device__ __forceinline__ void merge_one(const MergeParams& p, int wg, int lane
         const float w = __shfl_sync(0xffffffffu, wi, k);
         // rows past np, and rows with no units, carry weight 0 and a load
         // never issued: select, never multiply an unset register
-        if (k < np && w != 0.f) add(w, pre[k]);
+        if (w != 0.f) add(w, pre[k]);
     }
     for (int i = kPre; i < np; ++i) {
-        const long long rr = row_of(i);
-        if (rr < 0) continue;
-        const size_t r = (size_t)rr;
+        const int r = i < 32 ? __shfl_sync(0xffffffffu, rl, i) : row_of(i);
+        if (r < 0) continue;
         float w;
         if (i < 32) {
             w = __shfl_sync(0xffffffffu, wi, i);
@@ -1449,7 +1471,7 @@ __device__ __forceinline__ void merge_one(const MergeParams& p, int wg, int lane
             w = fast_exp2(p.ws_m[r] - Ms);
             if (lane == 0) L += w * p.ws_l[r];
         }
-        add(w, *reinterpret_cast<const V*>(p.ws_o + r * D + lane * PER));
+        add(w, *reinterpret_cast<const V*>(p.ws_o + (size_t)r * D + lane * PER));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
@@ -1743,17 +1765,41 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp_i
         even = false;
         hpi = tma_heads_per_item(prm.num_seqs, max_blocks, prm.num_kv_heads, D, false);
     }
+    // A cascade's suffixes (each sequence is merged with its prefix row
+    // anyway) are split evenly over the grid's consumer warps: each warp
+    // streams an equal run of (sequence, KV head, block) units.  A warp's
+    // time is set by its blocks (a stage costs a third of a copy's round
+    // trip), and items dealt whole left the longest suffix's warp running
+    // alone at the end (cascade step 56.8 -> see the measurements).  Needs
+    // 2 B Hq rows (prefix, whole suffixes) plus two slots of g rows per warp.
+    bool warp_even = false;
+    if (prm.prefix_parts > 0 && prm.partition_blocks <= 0 && warp_items_enabled() &&
+        prm.group <= kEvenMaxHeads) {
+        const long long rows = 2ll * prm.num_seqs * prm.num_q_heads +
+                               2ll * sms * kTmaConsumers * prm.group;
+        warp_even = rows <= prm.ws_rows;
+    }
+    if (warp_even) {
+        even = true;
+        hpi = 1;
+    }
     const int groups = prm.num_kv_heads / hpi;
     int grid;
     if (even) {
         const long long units_upper = (long long)prm.num_seqs * groups * std::max(1, max_blocks);
         grid = (int)std::max<long long>(1, std::min<long long>(units_upper,
                                                               std::min(sms, kMaxEvenGrid)));
+        if (warp_even) grid = std::min(sms, kMaxEvenGrid);
         prm.even_split = 1;
-        mp.even_grid = grid;
+        mp.even_grid = warp_even ? grid * kTmaConsumers : grid;  // workers
         mp.even_heads = hpi * prm.group;
         mp.groups = groups;
-        need_merge = max_blocks > 1;  // a one-block (sequence, group) is never cut
+        if (warp_even) {
+            prm.even_row0 = 2 * prm.num_seqs * prm.num_q_heads;
+            mp.even_row0 = prm.even_row0;
+        } else {
+            need_merge = max_blocks > 1;  // a one-block (sequence, group) is never cut
+        }
     } else {
         const long long items_upper =
             (long long)prm.num_seqs * std::max(1, ceil_div(max_blocks, pb_lower)) * groups;
@@ -1761,10 +1807,10 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp_i
         // per-head items: 8 per CTA; all-heads items carry Hkv heads each: 4 per CTA
         prm.target_items = grid * tma_items_per_cta(hpi);
     }
-    const bool warp_items = !even && hpi == 1 && warp_items_enabled() &&
-                            (long long)prm.num_seqs * prm.num_kv_heads >=
-                                (long long)kTmaConsumers * sms / 2;
-    if (warp_items) prm.target_items = grid * kTmaConsumers * 2;  // two items per warp
+    const bool warp_items = warp_even || (!even && hpi == 1 && warp_items_enabled() &&
+                                          (long long)prm.num_seqs * prm.num_kv_heads >=
+                                              (long long)kTmaConsumers * sms / 2);
+    if (warp_items && !even) prm.target_items = grid * kTmaConsumers * 2;  // two items per warp
 
     int merge_cap = 0;  // merge CTAs that fit beside this pass's partition CTAs
     if (passes & kPassPartition) {
@@ -1927,6 +1973,8 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
     prm.skip_blocks = prefix_blocks;
     prm.prefix_parts = prefix_parts;
     prm.item_row0 = num_seqs * prefix_parts;  // rows 0 .. num_seqs - 1: the prefix partials
+    prm.even_row0 = 0;
+    prm.ws_rows = (long long)ws.rows;
     prm.no_wait = 0;
     prm.min_partition_blocks = pb_lower;
     prm.target_items = 0;
@@ -1946,6 +1994,7 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
     mp.min_rows = prefix_parts > 0 ? 1 : 2;
     mp.prefix_rows = prefix_parts;
     mp.item_row0 = prm.item_row0;
+    mp.even_row0 = 0;
     mp.even_grid = 0;  // the TMA pass sets the even-split fields
     mp.even_heads = 0;
     mp.groups = 0;
@@ -2000,21 +2049,25 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
     // share nothing they write (prefix rows vs item rows, the new tokens
     // land past the prefix), so the TMA pass does not wait at all.  The
     // merge is an ordinary launch, so it waits for both.
+    // The suffix pass runs on the SMs the prefix pass leaves; its merge is
+    // planned for the same SM count (an even split's workers).
+    const int sms = sm_count();
+    if (sms <= 0) return PKV_ERR_CUDA;
+    const int prefix_ctas = cascade_prefix_ctas(sms);
+    const int suffix_sms =
+        std::max(1, sms - cascade_prefix_grid(num_seqs, num_q_heads, num_kv_heads, prefix_ctas));
     if (passes & kPassPartition) {
-        const int sms = sm_count();
-        if (sms <= 0) return PKV_ERR_CUDA;
         int pgrid = 0;
         pkv_status rc = launch_cascade_prefix(
             q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, len_bound,
             num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, prefix_blocks,
-            prm.scale_log2, prm.ws_m, prm.ws_l, prm.ws_o, dtype,
-            cascade_prefix_ctas(sms), &pgrid, stream);
+            prm.scale_log2, prm.ws_m, prm.ws_l, prm.ws_o, dtype, prefix_ctas, &pgrid, stream);
         if (rc != PKV_OK) return rc;
         prm.no_wait = 1;
-        rc = run(kPassPartition, std::max(1, sms - pgrid), true);
+        rc = run(kPassPartition, suffix_sms, true);
         if (rc != PKV_OK) return rc;
     }
-    return (passes & kPassMerge) ? run(kPassMerge, 0, true) : PKV_OK;
+    return (passes & kPassMerge) ? run(kPassMerge, suffix_sms, true) : PKV_OK;
 }
 
 }  // namespace

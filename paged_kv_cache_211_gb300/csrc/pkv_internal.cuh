@@ -27,6 +27,8 @@ inline pkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK 
 // workspace row s * num_q_heads + i.  A persistent grid of at most max_ctas
 // CTAs (its size goes to *grid_out); an ordinary launch that lets the next
 // kernel on the stream start beside it.
+// CTAs of a cascade's prefix pass for these shapes, at most max_ctas.
+int cascade_prefix_grid(int num_seqs, int num_q_heads, int num_kv_heads, int max_ctas);
 pkv_status launch_cascade_prefix(const void* q, const void* k_cache, const void* v_cache,
                                  const int32_t* block_tables, int max_blocks_per_seq,
                                  const int32_t* context_lens, int len_bound, int num_seqs,

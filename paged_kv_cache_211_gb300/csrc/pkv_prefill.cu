@@ -1385,6 +1385,13 @@ pkv_status launch_prefix_tc(const PrefillParams& prm, const void* k_cache, const
 
 }  // namespace
 
+int cascade_prefix_grid(int num_seqs, int num_q_heads, int num_kv_heads, int max_ctas) {
+    // one CTA per (KV head, row tile of the sharers' query rows), at most max_ctas
+    const long long items =
+        (long long)num_kv_heads * ceil_div(num_seqs * (num_q_heads / num_kv_heads), kTcRows);
+    return (int)std::max<long long>(1, std::min<long long>(items, max_ctas));
+}
+
 pkv_status launch_cascade_prefix(const void* q, const void* k_cache, const void* v_cache,
                                  const int32_t* block_tables, int max_blocks_per_seq,
                                  const int32_t* context_lens, int len_bound, int num_seqs,
@@ -1395,9 +1402,8 @@ pkv_status launch_cascade_prefix(const void* q, const void* k_cache, const void*
     unsigned int* status = status_word();
     if (!status) return PKV_ERR_CUDA;
     const int g = num_q_heads / num_kv_heads;
-    const long long items =
-        (long long)num_kv_heads * ceil_div(num_seqs * g, kTcRows);
-    const int grid = (int)std::max<long long>(1, std::min<long long>(items, max_ctas));
+    const long long items = (long long)num_kv_heads * ceil_div(num_seqs * g, kTcRows);
+    const int grid = cascade_prefix_grid(num_seqs, num_q_heads, num_kv_heads, max_ctas);
     *grid_out = grid;
     PrefillParams prm = {};
     prm.q = q;

@@ -3,6 +3,10 @@
 The oracle knows nothing of the cascade: it attends each sequence's whole
 context through its block table, so these tests check that reading the
 shared prefix once for all sharers changes nothing but the reads."""
+import os
+import subprocess
+import sys
+
 import numpy as np
 import pytest
 import torch
@@ -14,6 +18,8 @@ from gpu_helpers import assert_attention_close, compact_oracle_step, dtype_code
 from pkv_testutil import bits
 
 pytestmark = pytest.mark.gpu
+
+HERE = os.path.dirname(os.path.abspath(__file__))
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -123,3 +129,17 @@ def test_cascade_step_refuses_a_token_inside_the_prefix(cuda_device):
     assert int(slots[0]) == -1
     assert torch.equal(kc[tables[0, 3]].view(torch.int16), k_before[tables[0, 3]].view(torch.int16))
     assert int(slots[1]) == int(tables[1, 4]) * 16 and int(slots[2]) >= 0
+
+
+@pytest.mark.parametrize("split", ["0", "1"])
+def test_cascade_suffix_splits_in_child(split, cuda_device):
+    """The suffix pass split evenly over the consumer warps (the default when
+    the workspace holds the slots) and dealt as items (PKV_WARP_ITEMS=0), on
+    the same cases: 128 and 50 sequences, lengths inside, at and past the
+    prefix."""
+    env = dict(os.environ, PKV_WARP_ITEMS=split)
+    env["PYTHONPATH"] = os.pathsep.join([HERE, os.path.dirname(HERE), env.get("PYTHONPATH", "")])
+    r = subprocess.run([sys.executable, os.path.join(HERE, "cascade_case_check.py")], env=env,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-2000:]
+    assert "ok" in r.stdout
