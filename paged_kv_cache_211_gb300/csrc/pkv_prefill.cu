@@ -875,6 +875,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // ============================================================================
 constexpr int kTc2Threads = 384;
 constexpr int kTc2Rows = 2 * kTcRows;   // rows per item: tiles A and B
+// Registers a thread: the block is launched at kTc2LaunchRegs (the host
+// checks the build); the load / MMA warpgroup then gives up registers and the
+// two softmax warpgroups take them (setmaxnreg), so that a softmax thread
+// holds a whole 128-key row of scores.  The shares add up to the launch total.
+constexpr int kTc2LaunchRegs = 168;
+constexpr int kTc2OtherRegs = 88;
+constexpr int kTc2SoftmaxRegs = 208;
+static_assert(128 * kTc2OtherRegs + 256 * kTc2SoftmaxRegs <= kTc2Threads * kTc2LaunchRegs,
+              "register shares exceed the launch total");
 
 struct Tc2Item {
     int s, h, q0, qlen, n, row0, p_last, nkv;
@@ -961,7 +970,9 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-
+    // whole warpgroups: warps 0-3 release registers, 4-11 take them
+    if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kTc2OtherRegs));
     if (warp == 0 || warp == 3) {
         // ------------------------------------------------ K (warp 0) / V (warp 3) producers
         const bool isk = warp == 0;
@@ -1125,7 +1136,9 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
             mbar_drain(mma_idle, 0, p.status);
         }
         __syncwarp();
+    }
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kTc2SoftmaxRegs));
         // ---------------- softmax of tile X (warps 4-7: A, 8-11: B), one thread per row
         const int X = (warp - 4) >> 2;
         const int wq = warp & 3;                             // tensor-memory lane quarter
@@ -1163,24 +1176,25 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
                     const bool vis = key0 + c <= pos && !((bad >> (c >> 4)) & 1u);
                     return vis ? v * sl2 : -INFINITY;
                 };
-                // pass 1: the row maximum of this key tile, 64 columns at a time
+                // the whole 128-key row of scores in registers: one round trip
+                // to tensor memory per key tile
+                float sc[kTcKeys];
+#pragma unroll
+                for (int q4 = 0; q4 < kTcKeys / 32; ++q4)
+                    tc_ld32(sx + 32 * q4, reinterpret_cast<uint32_t(&)[32]>(sc[32 * q4]));
+                tc_wait_ld();
                 float mxp[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) mxp[e] = -INFINITY;
+                if (plain) {
 #pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    float sc[64];
-                    tc_ld32(sx + 64 * h2, reinterpret_cast<uint32_t(&)[32]>(sc[0]));
-                    tc_ld32(sx + 64 * h2 + 32, reinterpret_cast<uint32_t(&)[32]>(sc[32]));
-                    tc_wait_ld();
-                    if (plain) {
+                    for (int c = 0; c < kTcKeys; c += 2)
+                        mxp[(c >> 1) & 7] = max3(mxp[(c >> 1) & 7], sc[c], sc[c + 1]);
+                } else {
 #pragma unroll
-                        for (int c = 0; c < 64; c += 2)
-                            mxp[(c >> 1) & 7] = max3(mxp[(c >> 1) & 7], sc[c], sc[c + 1]);
-                    } else {
-#pragma unroll
-                        for (int c = 0; c < 64; ++c)
-                            mxp[c & 7] = fmaxf(mxp[c & 7], masked(sc[c], 64 * h2 + c));
+                    for (int c = 0; c < kTcKeys; ++c) {
+                        sc[c] = masked(sc[c], c);
+                        mxp[c & 7] = fmaxf(mxp[c & 7], sc[c]);
                     }
                 }
                 float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
@@ -1205,25 +1219,19 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
                         tc_st32(ox + 32 * c, o);
                     }
                 }
-                // pass 2: P, written as 16-bit pairs over the first 64 columns, 32
-                // keys at a time: P of keys 32c.. lands on columns 16c.., scores
-                // this loop has already read
+                // P, written as 16-bit pairs over the first 64 columns: P of keys
+                // 32c.. lands on columns 16c.. (every score is in registers)
                 const uint64_t mul2 = f2(mul, mul), nms2 = f2(-ms, -ms);
                 uint64_t acc2[4] = {f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    float sc[32];
-                    tc_ld32(sx + 32 * c4, reinterpret_cast<uint32_t(&)[32]>(sc[0]));
-                    tc_wait_ld();
-                    if (!plain) {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) sc[e] = masked(sc[e], 32 * c4 + e);
-                    }
+                for (int c4 = 0; c4 < kTcKeys / 32; ++c4) {
                     uint32_t pk[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         float a0, a1;
-                        f2_split(f2_fma(f2(sc[2 * e], sc[2 * e + 1]), mul2, nms2), a0, a1);
+                        f2_split(f2_fma(f2(sc[32 * c4 + 2 * e], sc[32 * c4 + 2 * e + 1]), mul2,
+                                        nms2),
+                                 a0, a1);
                         const float p0 = fast_exp2(a0), p1 = fast_exp2(a1);
                         acc2[e & 3] = f2_add(acc2[e & 3], f2(p0, p1));
                         pk[e] = E::pack(p0, p1);
@@ -1324,7 +1332,15 @@ pkv_status launch_prefill(const PrefillParams& prm_in, const void* k_cache, cons
         !make_pool_map(&tmv, v_cache, num_blocks, num_kv_heads, D, dtype))
         return PKV_ERR_CUDA;
     PrefillParams prm = prm_in;
-    const int choice = prefill_kernel_choice();
+    int choice = prefill_kernel_choice();
+    // the two-tile kernel's register shares assume its launch count; any other
+    // build takes the one-tile kernel
+    static const bool tc2_regs_ok = [] {
+        cudaFuncAttributes a;
+        return cudaFuncGetAttributes(&a, prefill_tc2_kernel<T, D>) == cudaSuccess &&
+               a.numRegs == kTc2LaunchRegs;
+    }();
+    if (choice == 1 && !tc2_regs_ok) choice = 2;
     if (choice == 1) {
         prm.tiles_per_seq = ceil_div(max_q_len * prm.group, kTc2Rows);  // pairs of tiles
         auto kern = prefill_tc2_kernel<T, D>;
