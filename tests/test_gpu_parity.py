@@ -161,6 +161,20 @@ def test_even_split_edge_cases(dtype, Hkv, D, cuda_device):
         assert_attention_close(bits(out)[keep], want, dtype_code(w), f"case {k}")
 
 
+@pytest.mark.parametrize("dtype,Hq,Hkv,D,lens", [("bf16", 8, 2, 128, [32768]),
+                                                  ("f16", 4, 1, 64, [30000, 100])])
+def test_even_split_segment_over_many_ctas(dtype, Hq, Hkv, D, lens, cuda_device):
+    """A (sequence, head group) cut across far more than 32 CTAs (76 and about
+    150 pieces): the merge reads row i < 32 in lane i and the rest in further
+    rounds."""
+    NB = sum((n + 15) // 16 for n in lens) + 8
+    w, inp = _custom(cuda_device, dtype, lens, Hq, Hkv, D, NB, seed=len(lens) + Hkv)
+    want, _, _ = compact_oracle_step(inp, np.arange(len(lens)))
+    out, _ = _run_step(inp, cuda_device)
+    assert pkv.pkv_device_status() == 0
+    assert_attention_close(bits(out), want, dtype_code(w), f"{lens[0]} tokens, Hkv={Hkv}")
+
+
 @pytest.mark.parametrize("dtype,Hq,Hkv,D", [("bf16", 8, 8, 128), ("f16", 8, 1, 64),
                                              ("bf16", 16, 4, 64), ("f16", 6, 3, 128),
                                              ("bf16", 14, 2, 128)])

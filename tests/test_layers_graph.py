@@ -34,11 +34,15 @@ CASES = [
     ("llama7b_long", 3, dict(num_seqs=4, num_blocks=8200)),
     ("tinyllama_1p1b", 3, dict(num_seqs=24, num_blocks=3200)),
     ("qwen3_0p6b", 3, dict(num_seqs=160)),   # consumer warps take whole items
+    # 16 KV heads: the register-pipelined pass, which waits for the previous
+    # layer's merge before it reads anything
+    ("qwen3_0p6b", 3, dict(num_seqs=24, num_q_heads=32, num_kv_heads=16)),
 ]
 
 
 @pytest.mark.parametrize("name,L,kw", CASES,
-                         ids=[c[0] + ("_b%d" % c[2]["num_seqs"] if c[2] else "") for c in CASES])
+                         ids=[c[0] + "".join("_%s%d" % (k[4] if k.startswith("num_") else k[0], v)
+                                             for k, v in c[2].items()) for c in CASES])
 def test_layers_step_eager_and_graph(cuda_device, name, L, kw):
     import __graft_entry__
     __graft_entry__.build()
