@@ -1329,7 +1329,10 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
             else asm volatile("bar.sync 1, %0;\n" ::"r"(NC * 32) : "memory");
         }
     }
-    if (p.early_reads) asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    // A cascade's suffix pass (no_wait) waits here for the prefix pass it ran
+    // beside, so that its merge, a programmatic dependent of this grid, sees
+    // both passes complete once this grid is
+    if (p.early_reads || p.no_wait) asm volatile("griddepcontrol.wait;\n" ::: "memory");
     // every copy this warp issued must land before the CTA may exit: wait for
     // the last use issued into each of its slots (normally already consumed)
     __syncwarp();
@@ -2047,10 +2050,12 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
     // it).  The partition pass over the sequences' own blocks is its
     // programmatic dependent and runs beside it on the other SMs: the two
     // share nothing they write (prefix rows vs item rows, the new tokens
-    // land past the prefix), so the TMA pass does not wait at all.  The
-    // merge is an ordinary launch, so it waits for both.
+    // land past the prefix), so the TMA pass waits for it only before it
+    // ends (the register-pipelined pass waits at its start).
     // The suffix pass runs on the SMs the prefix pass leaves; its merge is
-    // planned for the same SM count (an even split's workers).
+    // planned for the same SM count (an even split's workers).  The merge is
+    // the suffix pass's programmatic dependent: the suffix pass's threads wait
+    // for the prefix pass before they end, so the merge's wait covers both.
     const int sms = sm_count();
     if (sms <= 0) return PKV_ERR_CUDA;
     const int prefix_ctas = cascade_prefix_ctas(sms);
@@ -2067,7 +2072,8 @@ pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache,
         rc = run(kPassPartition, suffix_sms, true);
         if (rc != PKV_OK) return rc;
     }
-    return (passes & kPassMerge) ? run(kPassMerge, suffix_sms, true) : PKV_OK;
+    return (passes & kPassMerge) ? run(kPassMerge, suffix_sms, !(passes & kPassPartition))
+                                 : PKV_OK;
 }
 
 }  // namespace
