@@ -613,10 +613,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
 //    no producer warp; each consumer walks its blocks twice, once to load and
 //    once to consume, and lane 0 refills a stage with the block one ring
 //    ahead as soon as the stage's fragments are in registers.
-// With warp items (many short one-head items: a cascade's suffixes, large
-// batches of short contexts) each self-feeding consumer warp takes whole
-// items of its own, every block of its item's head, and writes the item's
-// result alone: no combine across the consumers and no CTA-wide barrier.
+// With warp items each self-feeding consumer warp works alone, every block of
+// its piece's head, and writes the piece's result itself: no combine across
+// the consumers and no CTA-wide barrier.  Its pieces are whole one-head items
+// (many short items: large batches of short contexts) or, for a cascade's
+// suffixes, an equal run of the (sequence, KV head, block) units.
 // Either way every slot but the one being read is in flight, across item
 // boundaries.  Every mbarrier wait is bounded: on a time-out the kernel sets
 // PKV_DEV_TIMEOUT, stops issuing and waiting, lets every copy it issued land,
