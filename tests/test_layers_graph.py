@@ -31,6 +31,7 @@ def _oracle_layer(inp, layer):
 # D = 128 and at D = 64 with two heads per consumer).
 CASES = [
     ("qwen3_0p6b", 4, {}),
+    ("tiny", 3, {}),   # no merge: each layer's pass follows the previous layer's pass
     ("llama7b_long", 3, dict(num_seqs=4, num_blocks=8200)),
     ("tinyllama_1p1b", 3, dict(num_seqs=24, num_blocks=3200)),
     ("qwen3_0p6b", 3, dict(num_seqs=160)),   # consumer warps take whole items
