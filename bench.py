@@ -608,6 +608,82 @@ def prefill_measure(pkv, wl, dev, K, warmup):
     return res
 
 
+def cow_measure(pkv, dev, stream, peak):
+    """The prefix cache's copy-on-write: its device half (paged_kv_copy_blocks)
+    on a Llama-7B-shaped layer pool, 2048 (source, destination) block pairs per
+    call, and the host allocator's operations through the Python binding."""
+    NB, Hkv, D, pairs = 65536, 8, 128, 2048
+    g = torch.Generator(device=dev).manual_seed(2116)
+    kc = torch.randn(NB, 16, Hkv, D, generator=g, device=dev).to(torch.bfloat16)
+    vc = torch.randn(NB, 16, Hkv, D, generator=g, device=dev).to(torch.bfloat16)
+    perm = torch.from_numpy(np.random.default_rng(2116).permutation(NB)[:2 * pairs]
+                            .astype(np.int32)).to(dev)
+    src, dst = perm[:pairs].contiguous(), perm[pairs:].contiguous()
+
+    def step():
+        pkv.paged_kv_copy_blocks(kc, vc, src, dst, stream=stream)
+
+    for _ in range(5):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index)
+    K = 200
+    ms = time_loop(step, K, stream)
+    clk = clocks.stop()
+    if pkv.pkv_device_status() != 0:
+        raise SystemExit("device status flags set during the copy-on-write benchmark")
+    block_bytes = 16 * Hkv * D * 2
+    moved = pairs * 2 * 2 * block_bytes  # K and V, read and written
+    gbs = moved / (ms / 1e3) / 1e9
+    del kc, vc
+    torch.cuda.empty_cache()
+
+    # host allocator: each operation timed over many calls (CPU wall clock)
+    alloc = pkv.BlockAllocator(NB)
+    ops = {}
+
+    def timed(name, fn, n):
+        t0 = time.perf_counter()
+        for i in range(n):
+            fn(i)
+        ops[name] = round((time.perf_counter() - t0) / n * 1e6, 3)
+
+    held = []
+    timed("alloc_1_us", lambda i: held.append(alloc.alloc(1)[0]), 20000)
+    timed("share_1_us", lambda i: alloc.share([held[i]]), 20000)
+    timed("free_1_us", lambda i: alloc.free([held[i]]), 20000)   # drops the shared ref
+    hashes = [pkv.paged_kv_block_hash(0 if i == 0 else i, list(range(16 * i, 16 * i + 16)))
+              for i in range(64)]
+    for i, h in enumerate(hashes):
+        alloc.prefix_insert(held[i], h)
+    timed("prefix_lookup_64_blocks_us",
+          lambda i: alloc.free(alloc.prefix_lookup(hashes)), 2000)
+
+    def share_cow_free(i):  # a writer moved off a shared block, then its copy freed
+        b = held[100 + i % 1000]
+        alloc.share([b])
+        moved_to, _ = alloc.cow(b)
+        alloc.free([moved_to])
+
+    timed("share_cow_free_us", share_cow_free, 10000)
+    alloc.close()
+    return {
+        "description": "copy-on-write of 2048 random blocks of a Llama-7B-shaped layer "
+                       "(16 x 8 KV heads x 128, bf16, K and V) in a 65536-block pool; host "
+                       "allocator operations",
+        "step_us": round(ms * 1e3, 2), "steps": K, "value": round(gbs, 2), "unit": "GB/s",
+        "frac_of_measured_hbm": round(gbs / peak, 4),
+        "bytes_per_step": moved,
+        "bytes_formula": "pairs * 2 (K, V) * 2 (read, write) * 16 * Hkv * D * 2",
+        "gpu_launches_per_step": 1, "api": "paged_kv_copy_blocks",
+        "l2": "256 MB moved per call from random blocks of 4.3 GB of pools, no flush",
+        "host_allocator_us_per_op": ops,
+        "host_note": "BlockAllocator through the Python binding (ctypes call included), "
+                     "CPU wall clock",
+        "clocks": clk,
+    }
+
+
 def prefill_kernel_name() -> str:
     return ("prefill_tma_kernel (mma.sync m16n8k16)"
             if os.environ.get("PKV_PREFILL_KERNEL") == "mma" else
@@ -744,6 +820,7 @@ def run_ours(args):
             "l2": "inputs larger than L2: %.2f GB touched per step, no flush (compute-bound)"
                   % (pf["touched"] / 1e9),
             "api": "paged_attention_prefill", "clocks": pf["clocks"]}
+        workloads["prefix_cache_cow"] = cow_measure(pkv, dev, stream, peak)
 
     if rank != 0:
         return
