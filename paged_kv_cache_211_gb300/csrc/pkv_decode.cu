@@ -629,6 +629,18 @@ constexpr int kTmaConsumers = 8;
 __host__ __device__ constexpr int tma_threads(bool self_feed) { return (kTmaConsumers + (self_feed ? 0 : 1)) * 32; }
 constexpr int kTmaItemsPerCta = 8;
 constexpr int kTmaMaxStages = 8;
+// The ring's full / empty barriers (one arrival each) and use counts, one
+// slot per thread side by side (a separate function: inlined, it changed how
+// the kernel's registers are allocated).
+__device__ __noinline__ void init_ring(uint64_t* full, uint64_t* empty, int* last_use, int n) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        mbar_init(&full[i], 1);
+        mbar_init(&empty[i], 1);
+        last_use[i] = -1;
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+}
+
 template <typename T, int D, bool kOneHead, bool kSelfFeed, int kHPC = 1, bool kWarpItems = false>
 __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
     decode_partition_tma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
@@ -667,15 +679,8 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
     int* sm_off = sm_len + B;                                          // [B + 1]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) {
-        for (int i = 0; i < NC * nstages; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
-            last_use[i] = -1;
-        }
-        *abort_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    }
+    init_ring(full, empty, last_use, NC * nstages);
+    if (tid == 0) *abort_flag = 0;
 
     // This grid is a programmatic dependent of the previous kernel on the
     // stream and may start before it ends.  Only when that kernel is this
@@ -722,11 +727,13 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
             PB = max(mx, p.min_partition_blocks);
         } else {
             // items cover heads_per_item KV heads of their blocks: aim at target_items
-            const long long want =
-                ((long long)total_blocks * groups0 + p.target_items - 1) / p.target_items;
-            const long long lo = p.min_partition_blocks;
-            const long long hi = kAdaptiveMaxBlocks > lo ? kAdaptiveMaxBlocks : lo;
-            PB = (int)(want < lo ? lo : (want > hi ? hi : want));
+            // 32-bit: blocks x groups stays below 2^31 (8192 sequences, a table
+            // of int32 entries, at most 8 groups)
+            const unsigned want =
+                ((unsigned)total_blocks * groups0 + p.target_items - 1) / (unsigned)p.target_items;
+            const int lo = p.min_partition_blocks;
+            const int hi = kAdaptiveMaxBlocks > lo ? kAdaptiveMaxBlocks : lo;
+            PB = (int)want < lo ? lo : ((int)want > hi ? hi : (int)want);
         }
     }
     const int chunk = (B + NT - 1) / NT;
