@@ -917,7 +917,8 @@ __device__ __forceinline__ bool tc2_item(const PrefillParams& p, int i, bool fla
 template <typename T, int D>
 __global__ void __launch_bounds__(kTc2Threads, 1)
     prefill_tc2_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmap_k,
-                       const __grid_constant__ CUtensorMap tmap_v, int num_items) {
+                       const __grid_constant__ CUtensorMap tmap_v,
+                       const __grid_constant__ CUtensorMap tmap_q, int q_tma, int num_items) {
     using E = Elem<T>;
     constexpr int HALVES = D / 64;
     constexpr int REG = kTcRows * 128;     // one 64-element half of 128 rows: 16 KB
@@ -1017,6 +1018,52 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
         // every copy issued must land before the CTA may exit
         if (lane == 0)
             for (int j = max(0, J - 2); j < J; ++j) mbar_drain(&full[j & 1], (j >> 1) & 1, p.status);
+    } else if (warp == 2 && q_tma) {
+        // ------------------------- Q tiles of each item by tensor copies (lane 0)
+        // Tile X of an item is rows row0 + 128 X .. of the chunk: 128 / g
+        // tokens x the g query heads of KV head h, one box per 64-element
+        // half.  Rows past the chunk belong to the next chunk (or read as
+        // zeros past q): their rows see no key and are never stored.  The
+        // CTA's next item's tiles are fetched into L2 meanwhile, so that
+        // the copy at the item boundary finds them there.
+        if (lane == 0) {
+            const int g = p.group;
+            int I = 0;
+            int issued[2] = {0, 0};  // copies issued into Q_X
+            for (int i = blockIdx.x; i < num_items; i += gridDim.x) {
+                Tc2Item it;
+                if (!tc2_item(p, i, false, it)) continue;
+                bool live = true;
+                for (int X = 0; X < 2 && live; ++X) {
+                    live = mbar_wait(&q_empty[X], (I & 1) ^ 1, abort_flag, p.status);
+                    if (!live) break;
+                    ++issued[X];
+                    mbar_arrive_expect_tx(&q_full[X], (uint32_t)TILE);
+                    const int row = it.q0 + (it.row0 + X * kTcRows) / g;
+#pragma unroll
+                    for (int hh = 0; hh < HALVES; ++hh)
+                        tma_load_rows(sq + X * TILE + hh * REG, &tmap_q, &q_full[X], hh * 64,
+                                      it.h * g, row);
+                }
+                if (!live) break;
+                for (int i2 = i + gridDim.x; i2 < num_items; i2 += gridDim.x) {
+                    Tc2Item nx;
+                    if (!tc2_item(p, i2, false, nx)) continue;
+#pragma unroll
+                    for (int X = 0; X < 2; ++X)
+#pragma unroll
+                        for (int hh = 0; hh < HALVES; ++hh)
+                            tma_prefetch_rows(&tmap_q, hh * 64, nx.h * g,
+                                              nx.q0 + (nx.row0 + X * kTcRows) / g);
+                    break;
+                }
+                ++I;
+            }
+            // every copy issued must land before the CTA may exit
+            for (int X = 0; X < 2; ++X)
+                if (issued[X] > 0) mbar_drain(&q_full[X], (issued[X] - 1) & 1, p.status);
+        }
+        __syncwarp();
     } else if (warp == 2) {
         // ------------------------------------ Q rows of each item's two tiles (cp.async)
         const T* qb = static_cast<const T*>(p.q);
@@ -1353,7 +1400,14 @@ pkv_status launch_prefill(const PrefillParams& prm_in, const void* k_cache, cons
         const int sms = sm_count();
         if (sms <= 0) return PKV_ERR_CUDA;
         const int grid = (int)std::min<long long>(items, sms);  // persistent: one CTA per SM
-        kern<<<grid, kTc2Threads, smem, stream>>>(prm, tmk, tmv, (int)items);
+        // Q tiles by tensor copies when the group divides the tile's 128 rows
+        CUtensorMap tmq = tmk;
+        const int q_tma =
+            make_q_tile_map(&tmq, prm.q, prm.num_q_rows, prm.num_q_heads, D, prm.group, dtype)
+                ? 1
+                : 0;
+        if (!q_tma) tmq = tmk;  // unused
+        kern<<<grid, kTc2Threads, smem, stream>>>(prm, tmk, tmv, tmq, q_tma, (int)items);
         return cuda_status(cudaGetLastError());
     }
     if (choice == 2) {

@@ -83,6 +83,15 @@ __device__ __forceinline__ void tma_load_rows(void* dst, const CUtensorMap* map,
         : "memory");
 }
 
+// Fetch the same box into L2 only (no shared memory, no barrier): a later
+// tma_load_rows of it then finds the rows in L2.
+__device__ __forceinline__ void tma_prefetch_rows(const CUtensorMap* map, int x, int head, int row) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];\n" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(head), "r"(row)
+                 : "memory");
+}
+
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -143,6 +152,30 @@ inline bool make_pool_map(CUtensorMap* map, const void* pool, int num_blocks, in
     const CUtensorMapDataType dt =
         dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     return enc(map, dt, 3, const_cast<void*>(pool), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+// Query rows [num_rows][num_q_heads][D] viewed as (element, head, row) with
+// boxes of 64 elements x `group` heads x (128 / group) rows and the 128-byte
+// swizzle: one box is one 64-element half of a 128-row tile whose row r is
+// (row r / group, head r % group), the layout the tensor-core kernels read.
+// Rows past num_rows read as zeros.  Needs group to divide 128.
+inline bool make_q_tile_map(CUtensorMap* map, const void* q, int num_rows, int num_q_heads,
+                            int head_dim, int group, pkv_dtype dtype) {
+    if (group <= 0 || 128 % group != 0 || num_rows <= 0) return false;
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_q_heads,
+                                (cuuint64_t)num_rows};
+    const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2,
+                                   (cuuint64_t)num_q_heads * head_dim * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)group, (cuuint32_t)(128 / group)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapDataType dt =
+        dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    return enc(map, dt, 3, const_cast<void*>(q), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
            CUDA_SUCCESS;
