@@ -1213,10 +1213,12 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
                 tc_fence_after();
                 const unsigned bad = (unsigned)vbad[b];              // 8 blocks of the tile
                 const int key0 = kTcKeys * j;
-                // tiles below every row's causal bound with no bad block need no
-                // mask: max over the raw scores, the scale goes into the exponent
-                const bool plain = __all_sync(0xffffffffu, key0 + kTcKeys - 1 <= pos) &&
-                                   bad == 0u && sl2 > 0.f;
+                // tiles with no bad block keep the raw scores (the scale goes into
+                // the exponent); at the causal bound the keys past a row's
+                // position read as -inf (a select); tiles below every row's
+                // bound need no mask at all
+                const bool plain = bad == 0u && sl2 > 0.f;
+                const bool whole = __all_sync(0xffffffffu, key0 + kTcKeys - 1 <= pos);
                 const float mul = plain ? sl2 : 1.f;
                 // scaled score of key key0 + c (masked: -inf); raw for a plain tile
                 auto masked = [&](float v, int c) {
@@ -1234,6 +1236,11 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) mxp[e] = -INFINITY;
                 if (plain) {
+                    if (!whole) {
+                        const int lim = pos - key0;  // keys 0..lim of the tile are visible
+#pragma unroll
+                        for (int c = 0; c < kTcKeys; ++c) sc[c] = c <= lim ? sc[c] : -INFINITY;
+                    }
 #pragma unroll
                     for (int c = 0; c < kTcKeys; c += 2)
                         mxp[(c >> 1) & 7] = max3(mxp[(c >> 1) & 7], sc[c], sc[c + 1]);
