@@ -391,7 +391,8 @@ __device__ __forceinline__ bool tc_next(const PrefillParams& p, int i, bool flag
 template <typename T, int D, bool kPrefix>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmap_k,
-                      const __grid_constant__ CUtensorMap tmap_v, int num_items) {
+                      const __grid_constant__ CUtensorMap tmap_v,
+                      const __grid_constant__ CUtensorMap tmap_q, int q_tma, int num_items) {
     using E = Elem<T>;
     constexpr int HALVES = D / 64;
     constexpr int REG = kTcRows * 128;     // one 64-element half of 128 rows: 16 KB
@@ -502,6 +503,43 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // every copy issued must land before the CTA may exit
         if (lane == 0)
             for (int j = max(0, J - 2); j < J; ++j) mbar_drain(&full[j & 1], (j >> 1) & 1, p.status);
+    } else if (warp == 2 && q_tma) {
+        // ----------------------- Q tile of each item by tensor copies (lane 0)
+        // Rows row0.. of an item are 128 / g query rows (tokens of its chunk,
+        // or sequences in the prefix mode) x the g query heads of KV head h,
+        // one box per 64-element half; rows past q read as zeros, rows of
+        // the next chunk see no key and are never stored.  The CTA's next
+        // item's tile is fetched into L2 meanwhile.
+        if (lane == 0) {
+            int I = 0;
+            for (int i = blockIdx.x; i < num_items; i += gridDim.x) {
+                TcItem it;
+                if (!tc_next<kPrefix>(p, i, false, it)) continue;
+                const int qbuf = I & 1;
+                if (!mbar_wait(&q_empty[qbuf], ((I >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+                mbar_arrive_expect_tx(&q_full[qbuf], (uint32_t)TILE);
+#pragma unroll
+                for (int hh = 0; hh < HALVES; ++hh)
+                    tma_load_rows(sq + qbuf * TILE + hh * REG, &tmap_q, &q_full[qbuf], hh * 64,
+                                  it.h * g, it.q0 + it.row0 / g);
+                for (int i2 = i + gridDim.x; i2 < num_items; i2 += gridDim.x) {
+                    TcItem nx;
+                    if (!tc_next<kPrefix>(p, i2, false, nx)) continue;
+#pragma unroll
+                    for (int hh = 0; hh < HALVES; ++hh)
+                        tma_prefetch_rows(&tmap_q, hh * 64, nx.h * g, nx.q0 + nx.row0 / g);
+                    break;
+                }
+                ++I;
+            }
+            // every copy issued must land before the CTA may exit: the last
+            // tile issued into each buffer
+            for (int b2 = 0; b2 < 2; ++b2) {
+                const int uses = (I - b2 + 1) / 2;
+                if (uses > 0) mbar_drain(&q_full[b2], (uses - 1) & 1, p.status);
+            }
+        }
+        __syncwarp();
     } else if (warp == 2) {
         // --------------------------------------- Q rows of each item (cp.async)
         const T* qb = static_cast<const T*>(p.q);
@@ -1443,7 +1481,13 @@ pkv_status launch_prefill(const PrefillParams& prm_in, const void* k_cache, cons
         const int sms = sm_count();
         if (sms <= 0) return PKV_ERR_CUDA;
         const int grid = (int)std::min<long long>(items, sms);  // persistent: one CTA per SM
-        kern<<<grid, kTcThreads, smem, stream>>>(prm, tmk, tmv, (int)items);
+        CUtensorMap tmq = tmk;
+        const int q_tma =
+            make_q_tile_map(&tmq, prm.q, prm.num_q_rows, prm.num_q_heads, D, prm.group, dtype)
+                ? 1
+                : 0;
+        if (!q_tma) tmq = tmk;  // unused
+        kern<<<grid, kTcThreads, smem, stream>>>(prm, tmk, tmv, tmq, q_tma, (int)items);
         return cuda_status(cudaGetLastError());
     }
     prm.tiles_per_seq = ceil_div(max_q_len * prm.group, kPrefillRows);
@@ -1470,7 +1514,12 @@ pkv_status launch_prefix_tc(const PrefillParams& prm, const void* k_cache, const
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return PKV_ERR_CUDA;
-    kern<<<grid, kTcThreads, smem, stream>>>(prm, tmk, tmv, num_items);
+    // decode queries [num_seqs][Hq][D]: row t of a KV head's rows is sequence t / g
+    CUtensorMap tmq = tmk;
+    const int q_tma =
+        make_q_tile_map(&tmq, prm.q, prm.num_seqs, prm.num_q_heads, D, prm.group, dtype) ? 1 : 0;
+    if (!q_tma) tmq = tmk;  // unused
+    kern<<<grid, kTcThreads, smem, stream>>>(prm, tmk, tmv, tmq, q_tma, num_items);
     return cuda_status(cudaGetLastError());
 }
 
