@@ -626,7 +626,16 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
 constexpr int kTmaConsumers = 8;
 // threads of the TMA partition kernel: 8 consumer warps, plus the producer
 // warp unless the consumers feed themselves
-__host__ __device__ constexpr int tma_threads(bool self_feed) { return (kTmaConsumers + (self_feed ? 0 : 1)) * 32; }
+__host__ __device__ constexpr int tma_threads(bool self_feed, bool stream = false) {
+    return stream ? 12 * 32 : (kTmaConsumers + (self_feed ? 0 : 1)) * 32;
+}
+// Register shares of the stream-producer build (12 warps launched at 168):
+// warps 8-11 (the producer warp and three that leave) and the consumers.
+constexpr int kStreamLaunchRegs = 168;
+constexpr int kStreamProducerRegs = 72;
+constexpr int kStreamConsumerRegs = 216;
+static_assert(128 * kStreamProducerRegs + 256 * kStreamConsumerRegs <= 384 * kStreamLaunchRegs,
+              "register shares exceed the launch total");
 constexpr int kTmaItemsPerCta = 8;
 constexpr int kTmaMaxStages = 8;
 // The ring's full / empty barriers (one arrival each) and use counts, one
@@ -641,8 +650,9 @@ __device__ __noinline__ void init_ring(uint64_t* full, uint64_t* empty, int* las
     }
 }
 
-template <typename T, int D, bool kOneHead, bool kSelfFeed, int kHPC = 1, bool kWarpItems = false>
-__global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
+template <typename T, int D, bool kOneHead, bool kSelfFeed, int kHPC = 1, bool kWarpItems = false,
+          bool kStream = false>
+__global__ void __launch_bounds__(tma_threads(kSelfFeed, kStream), 1)
     decode_partition_tma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
                                 const __grid_constant__ CUtensorMap tmap_v, int nstages,
                                 int heads_per_item) {
@@ -652,7 +662,10 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
     static_assert(kHPC == 1 || (kHPC == 2 && !kSelfFeed && !kOneHead), "two heads per consumer");
     // kWarpItems: consumer warp w of CTA c takes items c * 8 + w, then every
     // (8 * gridDim.x)-th item after it (item mode only, one head per item)
-    static_assert(!kWarpItems || (kSelfFeed && kOneHead && kHPC == 1), "warp items");
+    static_assert(!kWarpItems || ((kSelfFeed || kStream) && kOneHead && kHPC == 1), "warp items");
+    // kStream: warp items fed by a producer warp whose lane v walks consumer
+    // v's stream (the consumers do not issue their own copies)
+    static_assert(!kStream || (kWarpItems && !kSelfFeed), "stream producer");
     using E = Elem<T>;
     constexpr int NC = kTmaConsumers;
     constexpr int HALVES = D / 64;
@@ -672,9 +685,9 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
     float* sm_o = reinterpret_cast<float*>(last_use + NC * nstages);   // [NC][g][DP]
     float* sm_m = sm_o + NC * g * DP;                                  // [NC][8]
     float* sm_l = sm_m + NC * kMaxGroup;                               // [NC][8]
-    constexpr int NT = tma_threads(kSelfFeed), NW = NT / 32;  // threads, warps
+    constexpr int NT = tma_threads(kSelfFeed, kStream), NW = NT / 32;  // threads, warps
     int* red = reinterpret_cast<int*>(sm_l + NC * kMaxGroup);          // [NC + 1]
-    volatile int* abort_flag = red + NC + 1;
+    volatile int* abort_flag = red + 2 * NC + 1;                       // red: up to 2 NC + 1 warps
     int* sm_len = red + NC + 2 + NC;                                   // [B]
     int* sm_off = sm_len + B;                                          // [B + 1]
 
@@ -817,7 +830,11 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
     // In a cascade the blocks are those past the shared prefix, and a whole
     // segment leaves its partials in row item_row0 + s instead, for the merge.
     const long long U = even ? (long long)groups * sm_off[B] : 0;
-    const int worker = kWarpItems ? (int)blockIdx.x * NC + warp : (int)blockIdx.x;
+    // this thread's worker: its CTA, or with warp items its consumer warp (a
+    // stream producer's lane v walks consumer v's range)
+    const int worker =
+        kWarpItems ? (int)blockIdx.x * NC + ((kStream && warp >= NC) ? (lane < NC ? lane : 0) : warp)
+                   : (int)blockIdx.x;
     const int workers = kWarpItems ? (int)gridDim.x * NC : (int)gridDim.x;
     const long long u_begin = U * worker / workers;
     const long long u_end = U * (worker + 1) / workers;
@@ -827,7 +844,7 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
     };
     auto cursor_begin = [&]() {
         Cursor c;
-        c.item = kWarpItems ? (int)blockIdx.x * NC + warp : (int)blockIdx.x;
+        c.item = worker;
         c.u = u_begin;
         c.s = 0;
         if (even && u_begin < u_end) {  // the sequence holding unit u_begin
@@ -873,6 +890,90 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed), 1)
         }
         return true;
     };
+
+    if constexpr (kStream) {
+        if (warp >= NC) {
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kStreamProducerRegs));
+            if (warp == NC) {
+                // ------------------------------------------------ stream producer
+                // Lane v (< 8) walks consumer v's stream of (item, block) in the
+                // consumer's order and refills each of its ring slots as soon as
+                // the consumer releases it (one non-blocking poll per lane and
+                // pass): the consumers only wait, read their fragments and
+                // release.  (A self-feeding consumer spent ~750 cycles of a
+                // ~3000-cycle stage issuing its own refill.)
+                const bool mine = lane < NC;
+                Cursor pc = cursor_begin();
+                Item pit;
+                bool live = mine && next_item(pc, pit);
+                int pj = live ? pit.lo : 0;
+                while (live && pj >= pit.hi) {  // pieces with no block
+                    live = next_item(pc, pit);
+                    if (live) pj = pit.lo;
+                }
+                // the table entry of the next refill, loaded one refill ahead
+                auto entry = [&]() {
+                    return live ? p.block_tables[(size_t)pit.s * p.max_blocks_per_seq + pj] : 0;
+                };
+                int id_next = entry();
+                int nf = 0, slot = 0;
+                uint32_t ph = 1u;  // parity of the empty phase the next refill waits for
+                long long t_last = clock64();
+                while (__any_sync(0xffffffffu, live)) {
+                    if (!live) continue;
+                    if (*abort_flag) {
+                        live = false;
+                        continue;
+                    }
+                    const int k = lane * nstages + slot;
+                    if (!mbar_test_wait(&empty[k], ph)) {
+                        if (clock64() - t_last > kWaitCycles) {
+                            *abort_flag = 1;
+                            atomicOr(p.status, PKV_DEV_TIMEOUT);
+                            live = false;
+                        }
+                        continue;
+                    }
+                    int id = id_next;
+                    if (id < 0 || id >= p.num_blocks) {
+                        atomicOr(p.status, PKV_DEV_BAD_BLOCK_ID);
+                        id = -1;  // block 0 is fetched and fully masked
+                    }
+                    stage_id[k] = id;
+                    last_use[k] = nf;
+                    mbar_arrive_expect_tx(&full[k], STAGE);
+                    unsigned char* st = ring + (size_t)k * STAGE;
+                    const int row = (id < 0 ? 0 : id) * PKV_BLOCK_SIZE;
+#pragma unroll
+                    for (int hh = 0; hh < HALVES; ++hh) {
+                        tma_load_rows(st + hh * 2048, &tmap_k, &full[k], hh * 64, pit.hg, row);
+                        tma_load_rows(st + TILE + hh * 2048, &tmap_v, &full[k], hh * 64, pit.hg,
+                                      row);
+                    }
+                    ++nf;
+                    if (++slot == nstages) {
+                        slot = 0;
+                        ph ^= 1u;
+                    }
+                    ++pj;
+                    while (live && pj >= pit.hi) {
+                        live = next_item(pc, pit);
+                        if (live) pj = pit.lo;
+                    }
+                    id_next = entry();
+                    t_last = clock64();
+                }
+                // every copy issued must land before the CTA may exit
+                __syncwarp();
+                for (int k = lane; k < NC * nstages; k += 32) {
+                    const int use = last_use[k];
+                    if (use >= 0) mbar_drain(&full[k], (use / nstages) & 1, p.status);
+                }
+            }
+            return;
+        }
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kStreamConsumerRegs));
+    }
 
     constexpr bool self_feed = kSelfFeed;
     if (!self_feed && warp == NC) {
@@ -1749,6 +1850,28 @@ int tma_items_per_cta(int heads_per_item) {
     return heads_per_item == 1 ? kTmaItemsPerCta : kTmaItemsPerCta / 2;
 }
 
+// The stream-producer build feeds a cascade's suffix pass unless
+// PKV_STREAM_FEED=0 (the self-feeding warps, kept for comparison runs).
+bool stream_feed_enabled() {
+    static const bool on = [] {
+        const char* v = std::getenv("PKV_STREAM_FEED");
+        return !(v && std::strcmp(v, "0") == 0);
+    }();
+    return on;
+}
+
+// Its register shares (setmaxnreg) add up only at its 168-register launch.
+template <typename T, int D>
+bool stream_regs_ok() {
+    static const bool ok = [] {
+        cudaFuncAttributes a;
+        return cudaFuncGetAttributes(&a, decode_partition_tma_kernel<T, D, true, false, 1, true,
+                                                                     true>) == cudaSuccess &&
+               a.numRegs == kStreamLaunchRegs;
+    }();
+    return ok;
+}
+
 template <typename T, int D>
 pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp_in, int pb_lower,
                              int max_blocks, bool need_merge, int passes, int nstages,
@@ -1840,10 +1963,15 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp_i
                             : 0;
         const int hpc = ns2 >= 2 ? 2 : 1;
         if (hpc == 2) nstages = ns2;
-        const bool self_feed = (hpi >= 4 && hpc == 1) || warp_items;
+        // a cascade's suffixes split over the consumer warps: their rings are
+        // filled by a stream-producer warp (unless PKV_STREAM_FEED=0, or the
+        // build does not launch at the register count its shares assume)
+        const bool stream_feed = warp_even && stream_feed_enabled() && stream_regs_ok<T, D>();
+        const bool self_feed = !stream_feed && ((hpi >= 4 && hpc == 1) || warp_items);
         // (the two-head build exists at D = 64 only)
         constexpr int kTwo = D == 64 ? 2 : 1;
-        auto kern = warp_items  ? decode_partition_tma_kernel<T, D, true, true, 1, true>
+        auto kern = stream_feed ? decode_partition_tma_kernel<T, D, true, false, 1, true, true>
+                    : warp_items ? decode_partition_tma_kernel<T, D, true, true, 1, true>
                     : self_feed ? decode_partition_tma_kernel<T, D, false, true>
                     : hpi == 1  ? decode_partition_tma_kernel<T, D, true, false>
                     : hpc == 2 ? decode_partition_tma_kernel<T, D, false, false, kTwo>
@@ -1858,7 +1986,7 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp_i
         // cache loads overlap a previous layer's merge pass (see the kernel)
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)grid);
-        cfg.blockDim = dim3(tma_threads(self_feed));
+        cfg.blockDim = dim3(tma_threads(self_feed, stream_feed));
         cfg.dynamicSmemBytes = smem;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
@@ -1869,7 +1997,7 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp_i
         if (cudaLaunchKernelEx(&cfg, kern, prm, tmk, tmv, nstages, hpi) != cudaSuccess)
             return PKV_ERR_CUDA;
         merge_cap = sms * merge_ctas_beside(reinterpret_cast<const void*>(kern),
-                                            tma_threads(self_feed), smem,
+                                            tma_threads(self_feed, stream_feed), smem,
                                             reinterpret_cast<const void*>(
                                                 decode_merge_kernel<T, D>));
     }

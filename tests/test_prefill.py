@@ -89,6 +89,25 @@ def test_prefill_matches_oracle(dtype, Hq, Hkv, D, cuda_device):
     assert torch.allclose(dec.float(), out[last].float(), atol=1e-2, rtol=1e-2)
 
 
+@pytest.mark.parametrize("dtype,Hq,Hkv,D", [("bf16", 32, 8, 128), ("f16", 16, 16, 64),
+                                             ("bf16", 32, 2, 128), ("f16", 12, 4, 128)])
+def test_prefill_rows_past_the_last_chunk_are_never_used(dtype, Hq, Hkv, D, cuda_device):
+    """q and out hold more rows than the chunks, NaN past them.  A query tile
+    of 128 / g tokens that runs past its chunk loads the rows after it (by
+    tensor copies when g divides 128, zero-filled by cp.async otherwise):
+    those rows see no key and are never stored, so the chunks match the
+    oracle and the extra output rows stay as they were."""
+    specs = [(300, 70), (190, 45)]          # chunks that end inside a tile
+    c = _case(cuda_device, dtype, specs, Hq, Hkv, D, seed=53 + Hq)
+    R = c["q"].shape[0]
+    q = torch.full((R + 37, Hq, D), float("nan"), dtype=c["q"].dtype, device=cuda_device)
+    q[:R] = c["q"]
+    c["q"] = q
+    out, want, code, _, _ = _run(c, D, cuda_device)
+    assert_attention_close(bits(out[:R]), want[:R], code, f"rows past the chunks g={Hq // Hkv}")
+    assert torch.isnan(out[R:].float()).all()
+
+
 def test_prefill_flags_a_chunk_longer_than_its_context(cuda_device):
     c = _case(cuda_device, "bf16", [(40, 8), (30, 30)], 8, 2, 128, seed=3)
     _run(c, 128, cuda_device)                       # valid first
