@@ -604,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
 // cp.async.bulk.tensor copies of boxes of 16 rows x 64 elements with the
 // 128-byte swizzle, each stage tracked by a "full" mbarrier; the consumer
 // reads its fragments with ldmatrix (.trans for V), conflict-free under the
-// swizzle.  Two feeds fill the rings (compile-time variants):
+// swizzle.  Three feeds fill the rings (compile-time variants):
 //  - producer warp (items of one or two KV heads: long contexts): a ninth
 //    warp walks the same items as the consumers and issues every copy, in
 //    lane-parallel batches; a consumer releases a stage through its "empty"
@@ -612,12 +612,16 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
 //  - self-feeding consumers (items of four or more heads: short contexts):
 //    no producer warp; each consumer walks its blocks twice, once to load and
 //    once to consume, and lane 0 refills a stage with the block one ring
-//    ahead as soon as the stage's fragments are in registers.
-// With warp items each self-feeding consumer warp works alone, every block of
-// its piece's head, and writes the piece's result itself: no combine across
-// the consumers and no CTA-wide barrier.  Its pieces are whole one-head items
-// (many short items: large batches of short contexts) or, for a cascade's
-// suffixes, an equal run of the (sequence, KV head, block) units.
+//    ahead as soon as the stage's fragments are in registers;
+//  - stream producer (a cascade's suffixes, split over the consumer warps):
+//    12 warps; lane v of the producer warp walks consumer v's own stream and
+//    refills each of its slots once released, and setmaxnreg moves registers
+//    from the producer's warpgroup to the consumers.
+// With warp items each consumer warp works alone, every block of its piece's
+// head, and writes the piece's result itself: no combine across the
+// consumers and no CTA-wide barrier.  Its pieces are whole one-head items
+// (many short items: large batches of short contexts, self-feeding) or, for
+// a cascade's suffixes, an equal run of the (sequence, KV head, block) units.
 // Either way every slot but the one being read is in flight, across item
 // boundaries.  Every mbarrier wait is bounded: on a time-out the kernel sets
 // PKV_DEV_TIMEOUT, stops issuing and waiting, lets every copy it issued land,
@@ -625,7 +629,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
 // ============================================================================
 constexpr int kTmaConsumers = 8;
 // threads of the TMA partition kernel: 8 consumer warps, plus the producer
-// warp unless the consumers feed themselves
+// warp unless the consumers feed themselves; the stream-producer build has
+// 12 (the producer warp's warpgroup gives its registers to the consumers)
 __host__ __device__ constexpr int tma_threads(bool self_feed, bool stream = false) {
     return stream ? 12 * 32 : (kTmaConsumers + (self_feed ? 0 : 1)) * 32;
 }
