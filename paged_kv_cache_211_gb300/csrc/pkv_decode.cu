@@ -608,7 +608,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
 //  - producer warp (items of one or two KV heads: long contexts): a ninth
 //    warp walks the same items as the consumers and issues every copy, in
 //    lane-parallel batches; a consumer releases a stage through its "empty"
-//    mbarrier once its fragments are in registers;
+//    mbarrier once its fragments are in registers.  With one head per item
+//    the CTA has 12 warps and setmaxnreg moves the producer warpgroup's
+//    registers to the consumers (which spilled at nine warps' 168);
 //  - self-feeding consumers (items of four or more heads: short contexts):
 //    no producer warp; each consumer walks its blocks twice, once to load and
 //    once to consume, and lane 0 refills a stage with the block one ring
@@ -629,10 +631,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_partition_kernel(const Dec
 // ============================================================================
 constexpr int kTmaConsumers = 8;
 // threads of the TMA partition kernel: 8 consumer warps, plus the producer
-// warp unless the consumers feed themselves; the stream-producer build has
-// 12 (the producer warp's warpgroup gives its registers to the consumers)
-__host__ __device__ constexpr int tma_threads(bool self_feed, bool stream = false) {
-    return stream ? 12 * 32 : (kTmaConsumers + (self_feed ? 0 : 1)) * 32;
+// warp unless the consumers feed themselves; the stream-producer and wide
+// producer builds have 12 (the producer warp's warpgroup gives its registers
+// to the consumers)
+__host__ __device__ constexpr int tma_threads(bool self_feed, bool stream = false,
+                                              bool wide = false) {
+    return stream || wide ? 12 * 32 : (kTmaConsumers + (self_feed ? 0 : 1)) * 32;
 }
 // Register shares of the stream-producer build (12 warps launched at 168):
 // warps 8-11 (the producer warp and three that leave) and the consumers.
@@ -656,8 +660,8 @@ __device__ __noinline__ void init_ring(uint64_t* full, uint64_t* empty, int* las
 }
 
 template <typename T, int D, bool kOneHead, bool kSelfFeed, int kHPC = 1, bool kWarpItems = false,
-          bool kStream = false>
-__global__ void __launch_bounds__(tma_threads(kSelfFeed, kStream), 1)
+          bool kStream = false, bool kWide = false>
+__global__ void __launch_bounds__(tma_threads(kSelfFeed, kStream, kWide), 1)
     decode_partition_tma_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
                                 const __grid_constant__ CUtensorMap tmap_v, int nstages,
                                 int heads_per_item) {
@@ -671,6 +675,11 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed, kStream), 1)
     // kStream: warp items fed by a producer warp whose lane v walks consumer
     // v's stream (the consumers do not issue their own copies)
     static_assert(!kStream || (kWarpItems && !kSelfFeed), "stream producer");
+    // kWide: the producer warp (one head per item) in a CTA of 12 warps, whose
+    // warpgroup gives its registers to the consumers (setmaxnreg), as the
+    // stream producer's does: the consumers no longer spill
+    static_assert(!kWide || (kOneHead && kHPC == 1 && !kSelfFeed && !kStream && !kWarpItems),
+                  "wide producer");
     using E = Elem<T>;
     constexpr int NC = kTmaConsumers;
     constexpr int HALVES = D / 64;
@@ -690,7 +699,7 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed, kStream), 1)
     float* sm_o = reinterpret_cast<float*>(last_use + NC * nstages);   // [NC][g][DP]
     float* sm_m = sm_o + NC * g * DP;                                  // [NC][8]
     float* sm_l = sm_m + NC * kMaxGroup;                               // [NC][8]
-    constexpr int NT = tma_threads(kSelfFeed, kStream), NW = NT / 32;  // threads, warps
+    constexpr int NT = tma_threads(kSelfFeed, kStream, kWide), NW = NT / 32;  // threads, warps
     int* red = reinterpret_cast<int*>(sm_l + NC * kMaxGroup);          // [NC + 1]
     volatile int* abort_flag = red + 2 * NC + 1;                       // red: up to 2 NC + 1 warps
     int* sm_len = red + NC + 2 + NC;                                   // [B]
@@ -981,7 +990,7 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed, kStream), 1)
     }
 
     constexpr bool self_feed = kSelfFeed;
-    if (!self_feed && warp == NC) {
+    auto lockstep_producer = [&]() {
         // ------------------------------------------------------------ producer
         // Batches of BB blocks x CPB consumers' heads, lane t issuing (block
         // jb + t / CPB, heads slot t % CPB of the group) for consumer t % CPB +
@@ -1068,6 +1077,16 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed, kStream), 1)
             const int use = last_use[k];
             if (use >= 0) mbar_drain(&full[k], (use / nstages) & 1, p.status);
         }
+    };
+    if constexpr (kWide) {
+        if (warp >= NC) {
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kStreamProducerRegs));
+            if (warp == NC) lockstep_producer();
+            return;
+        }
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kStreamConsumerRegs));
+    } else if (!self_feed && warp == NC) {
+        lockstep_producer();
         return;
     }
 
@@ -1274,46 +1293,10 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed, kStream), 1)
                 if (p.slot_out && h == 0 && lane == 0)
                     p.slot_out[s] = id >= 0 ? (int64_t)id * PKV_BLOCK_SIZE + rnew : -1;
             }
-            // head by head: its fragments into registers, then (after the last
-            // head's) the slot goes back to the producer or is refilled with the
-            // block nstages ahead (the async-proxy copy after the warp's reads)
-#pragma unroll
-            for (int e = 0; e < kHPC; ++e) {
-                uint32_t kf[KS][4], vf[KS][4];
-                if (ok) {
-                    const uint32_t kt = smem_addr(st) + e * TILE;
-                    const uint32_t vt = smem_addr(st) + (kHPC + e) * TILE;
-#pragma unroll
-                    for (int ks = 0; ks < KS; ++ks) {
-                        const int row = lane & 15;
-                        ldsm_x4(kf[ks], kt + swz(row, 2 * ks + (lane >> 4)));
-                        const int mi = lane >> 3;
-                        const int tok = (lane & 7) + 8 * (mi >> 1);
-                        ldsm_x4_trans(vf[ks], vt + swz(tok, 2 * ks + (mi & 1)));
-                    }
-                }
-                if (e == kHPC - 1) {
-                    if constexpr (kSelfFeed) {
-                        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-                        __syncwarp();
-                        if (ok) fetch_next(); else feeding = false;
-                    } else {
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&empty[k]);
-                    }
-                }
-                if (!ok || nv == 0) continue;
-
-                float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int ks = 0; ks < KS; ks += 2) {
-                    E::mma(sa, kf[ks][0], kf[ks][1], kf[ks][2], kf[ks][3], qf[e][ks][0],
-                           qf[e][ks][1]);
-                    E::mma(sb, kf[ks + 1][0], kf[ks + 1][1], kf[ks + 1][2], kf[ks + 1][3],
-                           qf[e][ks + 1][0], qf[e][ks + 1][1]);
-                }
-                float s0 = (sa[0] + sb[0]) * p.scale_log2, s1 = (sa[1] + sb[1]) * p.scale_log2;
-                float s2 = (sa[2] + sb[2]) * p.scale_log2, s3 = (sa[3] + sb[3]) * p.scale_log2;
+            // the softmax and P V of head e from its scaled scores s0..s3 and
+            // its V fragments
+            auto head_tail = [&](int e, float s0, float s1, float s2, float s3,
+                                 uint32_t (&vf)[KS][4]) {
                 if (nv < PKV_BLOCK_SIZE) {  // partial last block: select, never weight
                     if (gid >= nv) s0 = s1 = -INFINITY;
                     if (gid + 8 >= nv) s2 = s3 = -INFINITY;
@@ -1357,6 +1340,48 @@ __global__ void __launch_bounds__(tma_threads(kSelfFeed, kStream), 1)
 #pragma unroll
                 for (int i = 0; i < KS; ++i)
                     E::mma(o[e][i], vf[i][0], vf[i][1], vf[i][2], vf[i][3], pt, pbt);
+            };
+            // head by head: its fragments into registers, then (after the last
+            // head's) the slot goes back to the producer or is refilled with the
+            // block nstages ahead (the async-proxy copy after the warp's reads)
+#pragma unroll
+            for (int e = 0; e < kHPC; ++e) {
+                uint32_t kf[KS][4], vf[KS][4];
+                if (ok) {
+                    const uint32_t kt = smem_addr(st) + e * TILE;
+                    const uint32_t vt = smem_addr(st) + (kHPC + e) * TILE;
+#pragma unroll
+                    for (int ks = 0; ks < KS; ++ks) {
+                        const int row = lane & 15;
+                        ldsm_x4(kf[ks], kt + swz(row, 2 * ks + (lane >> 4)));
+                        const int mi = lane >> 3;
+                        const int tok = (lane & 7) + 8 * (mi >> 1);
+                        ldsm_x4_trans(vf[ks], vt + swz(tok, 2 * ks + (mi & 1)));
+                    }
+                }
+                if (e == kHPC - 1) {
+                    if constexpr (kSelfFeed) {
+                        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+                        __syncwarp();
+                        if (ok) fetch_next(); else feeding = false;
+                    } else {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&empty[k]);
+                    }
+                }
+                if (!ok || nv == 0) continue;
+
+                float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < KS; ks += 2) {
+                    E::mma(sa, kf[ks][0], kf[ks][1], kf[ks][2], kf[ks][3], qf[e][ks][0],
+                           qf[e][ks][1]);
+                    E::mma(sb, kf[ks + 1][0], kf[ks + 1][1], kf[ks + 1][2], kf[ks + 1][3],
+                           qf[e][ks + 1][0], qf[e][ks + 1][1]);
+                }
+                float s0 = (sa[0] + sb[0]) * p.scale_log2, s1 = (sa[1] + sb[1]) * p.scale_log2;
+                float s2 = (sa[2] + sb[2]) * p.scale_log2, s3 = (sa[3] + sb[3]) * p.scale_log2;
+                head_tail(e, s0, s1, s2, s3, vf);
             }
         }
 
@@ -1865,6 +1890,29 @@ bool stream_feed_enabled() {
     return on;
 }
 
+// One-head items on the producer warp run the 12-warp build unless
+// PKV_WIDE=0 (the 9-warp build, kept for comparison runs).
+bool wide_enabled() {
+    static const bool on = [] {
+        const char* v = std::getenv("PKV_WIDE");
+        return !(v && std::strcmp(v, "0") == 0);
+    }();
+    return on;
+}
+
+// Its register shares (setmaxnreg) add up only at its 168-register launch.
+template <typename T, int D>
+bool wide_regs_ok() {
+    static const bool ok = [] {
+        cudaFuncAttributes a;
+        return cudaFuncGetAttributes(&a, decode_partition_tma_kernel<T, D, true, false, 1, false,
+                                                                     false, true>) ==
+                   cudaSuccess &&
+               a.numRegs == kStreamLaunchRegs;
+    }();
+    return ok;
+}
+
 // Its register shares (setmaxnreg) add up only at its 168-register launch.
 template <typename T, int D>
 bool stream_regs_ok() {
@@ -1975,10 +2023,17 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp_i
         const bool self_feed = !stream_feed && ((hpi >= 4 && hpc == 1) || warp_items);
         // (the two-head build exists at D = 64 only)
         constexpr int kTwo = D == 64 ? 2 : 1;
+        // one-head items on the producer warp run in 12 warps, their consumers
+        // given more registers (long-context step 172.5 -> 171.9 us; two-head
+        // items measured no faster)
+        const bool wide = !stream_feed && !self_feed && hpi == 1 && wide_enabled() &&
+                          wide_regs_ok<T, D>();
         auto kern = stream_feed ? decode_partition_tma_kernel<T, D, true, false, 1, true, true>
                     : warp_items ? decode_partition_tma_kernel<T, D, true, true, 1, true>
                     : self_feed ? decode_partition_tma_kernel<T, D, false, true>
-                    : hpi == 1  ? decode_partition_tma_kernel<T, D, true, false>
+                    : hpi == 1  ? (wide ? decode_partition_tma_kernel<T, D, true, false, 1, false,
+                                                                       false, true>
+                                        : decode_partition_tma_kernel<T, D, true, false>)
                     : hpc == 2 ? decode_partition_tma_kernel<T, D, false, false, kTwo>
                                : decode_partition_tma_kernel<T, D, false, false>;
         const size_t smem = tma_fixed_smem(D, prm.num_seqs, prm.group) +
@@ -1991,7 +2046,7 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp_i
         // cache loads overlap a previous layer's merge pass (see the kernel)
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)grid);
-        cfg.blockDim = dim3(tma_threads(self_feed, stream_feed));
+        cfg.blockDim = dim3(tma_threads(self_feed, stream_feed, wide));
         cfg.dynamicSmemBytes = smem;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
@@ -2002,7 +2057,7 @@ pkv_status launch_decode_tma(const DecodeParams& prm_in, const MergeParams& mp_i
         if (cudaLaunchKernelEx(&cfg, kern, prm, tmk, tmv, nstages, hpi) != cudaSuccess)
             return PKV_ERR_CUDA;
         merge_cap = sms * merge_ctas_beside(reinterpret_cast<const void*>(kern),
-                                            tma_threads(self_feed, stream_feed), smem,
+                                            tma_threads(self_feed, stream_feed, wide), smem,
                                             reinterpret_cast<const void*>(
                                                 decode_merge_kernel<T, D>));
     }
