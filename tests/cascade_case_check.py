@@ -1,6 +1,7 @@
 """Child-process check of cascade decode against the oracle, run by
-test_cascade_item_split with the split choice in the environment
-(PKV_WARP_ITEMS, read once per process).  Exit status 0 = within tolerance."""
+test_cascade_suffix_splits_in_child with the split and feed choices in the
+environment (PKV_WARP_ITEMS, PKV_STREAM_FEED, read once per process).  Exit
+status 0 = within tolerance."""
 import sys
 
 import torch

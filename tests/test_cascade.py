@@ -131,13 +131,16 @@ def test_cascade_step_refuses_a_token_inside_the_prefix(cuda_device):
     assert int(slots[1]) == int(tables[1, 4]) * 16 and int(slots[2]) >= 0
 
 
-@pytest.mark.parametrize("split", ["0", "1"])
-def test_cascade_suffix_splits_in_child(split, cuda_device):
+@pytest.mark.parametrize("switch", [{"PKV_WARP_ITEMS": "1"}, {"PKV_WARP_ITEMS": "0"},
+                                    {"PKV_STREAM_FEED": "0"}],
+                         ids=["even_stream_producer", "items", "even_self_feeding"])
+def test_cascade_suffix_splits_in_child(switch, cuda_device):
     """The suffix pass split evenly over the consumer warps (the default when
-    the workspace holds the slots) and dealt as items (PKV_WARP_ITEMS=0), on
-    the same cases: 128 and 50 sequences, lengths inside, at and past the
-    prefix."""
-    env = dict(os.environ, PKV_WARP_ITEMS=split)
+    the workspace holds the slots) with its rings filled by the stream
+    producer, the same split with self-feeding warps (PKV_STREAM_FEED=0), and
+    dealt as items (PKV_WARP_ITEMS=0), on the same cases: 128 and 50
+    sequences, lengths inside, at and past the prefix."""
+    env = dict(os.environ, **switch)
     env["PYTHONPATH"] = os.pathsep.join([HERE, os.path.dirname(HERE), env.get("PYTHONPATH", "")])
     r = subprocess.run([sys.executable, os.path.join(HERE, "cascade_case_check.py")], env=env,
                        capture_output=True, text=True, timeout=600)

@@ -494,3 +494,20 @@ def test_bounded_wait_gives_up_and_reports(cuda_device):
     out, _ = _run_step(inp, cuda_device)
     assert pkv.pkv_device_status() == 0
     assert_attention_close(bits(out), want, oracle.BF16, "after a timed-out wait")
+
+
+@pytest.mark.parametrize("wide", ["1", "0"])
+def test_long_context_builds_in_child(wide, cuda_device):
+    """The one-head producer-warp pass in 12 warps (the default: setmaxnreg
+    hands the producer warpgroup's registers to the consumers) and in nine
+    (PKV_WIDE=0), each in a child process, against the oracle."""
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    env = dict(os.environ, PKV_WIDE=wide)
+    env["PYTHONPATH"] = os.pathsep.join([here, os.path.dirname(here), env.get("PYTHONPATH", "")])
+    r = subprocess.run([sys.executable, os.path.join(here, "decode_case_check.py")], env=env,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-2000:]
+    assert "ok" in r.stdout
