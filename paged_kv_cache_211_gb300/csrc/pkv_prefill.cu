@@ -1245,6 +1245,8 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
         const uint32_t sx = trow + X * kTcKeys;              // this tile's scores / P
         const uint32_t ox = trow + kOCol + X * D;            // this tile's O
         const float sl2 = p.scale_log2;
+        // rows start 2 D bytes apart: 32-byte aligned whenever out is
+        const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
         int J = 0, I = 0;
         bool ok = true;
         for (int rd = 0; rd * (int)gridDim.x < num_items && ok; ++rd) {
@@ -1382,14 +1384,27 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
                 tc_ld32(ox + 32 * c, o);
                 tc_wait_ld();
                 if (live_row) {
+                    uint32_t w[16];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float v[8];
+                    for (int u = 0; u < 16; ++u)
+                        w[u] = E::pack(__uint_as_float(o[2 * u]) * inv,
+                                       __uint_as_float(o[2 * u + 1]) * inv);
+                    if (out32) {
+                        // 32-byte stores: each fills a whole L2 sector
 #pragma unroll
-                        for (int u = 0; u < 8; ++u) v[u] = __uint_as_float(o[8 * e + u]) * inv;
-                        *reinterpret_cast<uint4*>(dst + 32 * c + 8 * e) =
-                            make_uint4(E::pack(v[0], v[1]), E::pack(v[2], v[3]),
-                                       E::pack(v[4], v[5]), E::pack(v[6], v[7]));
+                        for (int h = 0; h < 2; ++h)
+                            asm volatile(
+                                "st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n" ::"l"(
+                                    dst + 32 * c + 16 * h),
+                                "r"(w[8 * h]), "r"(w[8 * h + 1]), "r"(w[8 * h + 2]),
+                                "r"(w[8 * h + 3]), "r"(w[8 * h + 4]), "r"(w[8 * h + 5]),
+                                "r"(w[8 * h + 6]), "r"(w[8 * h + 7])
+                                : "memory");
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            *reinterpret_cast<uint4*>(dst + 32 * c + 8 * e) =
+                                make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
                     }
                 }
             }
