@@ -326,6 +326,14 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
+// One 32-byte store (a whole L2 sector; the address must be 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t (&w)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n" ::"l"(ptr),
+                 "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+                 "r"(w[7])
+                 : "memory");
+}
+
 __device__ __forceinline__ float max3(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -829,6 +837,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc_fence_after();
             const size_t orow = (size_t)(it.q0 + (live_row ? t : 0)) * Hq + it.h * g + (R - t * g);
             T* dst = static_cast<T*>(p.out) + orow * D;
+            // rows start 2 D (out) or 4 D (ws_o) bytes apart: 32-byte aligned with the base
+            const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
+            const bool ws32 = (reinterpret_cast<uintptr_t>(p.ws_o) & 31u) == 0;
             if constexpr (kPrefix) {
                 // partials of this row for the cascade's merge: o relative to M
                 if (live_row) {
@@ -842,31 +853,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tc_ld32(trow + kOCol + 32 * c, o0);
                 tc_ld32(trow + kOCol + 128 + 32 * c, o1);
                 tc_wait_ld();
+                // rows as 32-byte stores (whole L2 sectors) when the base is
+                // 32-byte aligned, else 16-byte ones
                 if constexpr (kPrefix) {
                     if (live_row) {
-                        float4* od = reinterpret_cast<float4*>(p.ws_o + orow * D + 32 * c);
+                        float* od = p.ws_o + orow * D + 32 * c;
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            od[e] = make_float4(
-                                __uint_as_float(o0[4 * e]) * w0 + __uint_as_float(o1[4 * e]) * w1,
-                                __uint_as_float(o0[4 * e + 1]) * w0 +
-                                    __uint_as_float(o1[4 * e + 1]) * w1,
-                                __uint_as_float(o0[4 * e + 2]) * w0 +
-                                    __uint_as_float(o1[4 * e + 2]) * w1,
-                                __uint_as_float(o0[4 * e + 3]) * w0 +
-                                    __uint_as_float(o1[4 * e + 3]) * w1);
+                        for (int e = 0; e < 4; ++e) {
+                            uint32_t w[8];
+#pragma unroll
+                            for (int u = 0; u < 8; ++u)
+                                w[u] = __float_as_uint(__uint_as_float(o0[8 * e + u]) * w0 +
+                                                       __uint_as_float(o1[8 * e + u]) * w1);
+                            if (ws32) {
+                                st_global_v8(od + 8 * e, w);
+                            } else {
+                                *reinterpret_cast<uint4*>(od + 8 * e) = make_uint4(w[0], w[1], w[2], w[3]);
+                                *reinterpret_cast<uint4*>(od + 8 * e + 4) =
+                                    make_uint4(w[4], w[5], w[6], w[7]);
+                            }
+                        }
                     }
                 } else if (live_row) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float v[8];
+                    for (int e = 0; e < 2; ++e) {
+                        uint32_t w[8];
 #pragma unroll
                         for (int u = 0; u < 8; ++u)
-                            v[u] = (__uint_as_float(o0[8 * e + u]) * w0 +
-                                    __uint_as_float(o1[8 * e + u]) * w1) * inv;
-                        *reinterpret_cast<uint4*>(dst + 32 * c + 8 * e) =
-                            make_uint4(E::pack(v[0], v[1]), E::pack(v[2], v[3]),
-                                       E::pack(v[4], v[5]), E::pack(v[6], v[7]));
+                            w[u] = E::pack((__uint_as_float(o0[16 * e + 2 * u]) * w0 +
+                                            __uint_as_float(o1[16 * e + 2 * u]) * w1) * inv,
+                                           (__uint_as_float(o0[16 * e + 2 * u + 1]) * w0 +
+                                            __uint_as_float(o1[16 * e + 2 * u + 1]) * w1) * inv);
+                        if (out32) {
+                            st_global_v8(dst + 32 * c + 16 * e, w);
+                        } else {
+                            *reinterpret_cast<uint4*>(dst + 32 * c + 16 * e) =
+                                make_uint4(w[0], w[1], w[2], w[3]);
+                            *reinterpret_cast<uint4*>(dst + 32 * c + 16 * e + 8) =
+                                make_uint4(w[4], w[5], w[6], w[7]);
+                        }
                     }
                 }
             }
@@ -1393,13 +1418,8 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
                         // 32-byte stores: each fills a whole L2 sector
 #pragma unroll
                         for (int h = 0; h < 2; ++h)
-                            asm volatile(
-                                "st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n" ::"l"(
-                                    dst + 32 * c + 16 * h),
-                                "r"(w[8 * h]), "r"(w[8 * h + 1]), "r"(w[8 * h + 2]),
-                                "r"(w[8 * h + 3]), "r"(w[8 * h + 4]), "r"(w[8 * h + 5]),
-                                "r"(w[8 * h + 6]), "r"(w[8 * h + 7])
-                                : "memory");
+                            st_global_v8(dst + 32 * c + 16 * h,
+                                         reinterpret_cast<const uint32_t(&)[8]>(w[8 * h]));
                     } else {
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
