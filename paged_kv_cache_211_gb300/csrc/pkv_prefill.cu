@@ -1417,9 +1417,12 @@ __global__ void __launch_bounds__(kTc2Threads, 1)
                     if (out32) {
                         // 32-byte stores: each fills a whole L2 sector
 #pragma unroll
-                        for (int h = 0; h < 2; ++h)
-                            st_global_v8(dst + 32 * c + 16 * h,
-                                         reinterpret_cast<const uint32_t(&)[8]>(w[8 * h]));
+                        for (int h = 0; h < 2; ++h) {
+                            uint32_t w8[8];
+#pragma unroll
+                            for (int u = 0; u < 8; ++u) w8[u] = w[8 * h + u];
+                            st_global_v8(dst + 32 * c + 16 * h, w8);
+                        }
                     } else {
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
